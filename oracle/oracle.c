@@ -1,0 +1,305 @@
+/*
+ * oracle.c -- plain, slow, obviously correct CPU oracle for the block-scaled GEMM.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link or
+ * call this file; only the tests, the smoke check and the CPU baseline leg of
+ * the benchmark use it.  It shares no code, header, table or constant with the
+ * CUDA library.
+ *
+ * What it computes (in FP64, no blocking, no fusion):
+ *
+ *   dense block-scaled GEMM (MXFP8 / MXFP4; "PyTorch on AMD GPUs gains a FlyDSL
+ *   backend", Interpretation: FP8 or packed FP4 operands with one E8M0 scale per
+ *   32 values along the reduction dimension; "Experimental FlyDSL GEMM backend
+ *   for TE PyTorch", Supported Data Types: MXFP8):
+ *
+ *     D[m][n] = sum_k  dec_a(Aop[m][k]) * 2^(sA[m][k/32]-127)
+ *                     * dec_b(Bop[n][k]) * 2^(sB[n][k/32]-127)
+ *
+ *   grouped groupwise FP8 ("Add FlyDSL grouped groupwise FP8 GEMM for ROCm",
+ *   introduction and the commit that fixes the activation-scale layout):
+ *
+ *     for row r of group g (local row l = r - M_start_g):
+ *     D[r][n] = sum_kb sX(g,l,kb) * sW[g][n/128][kb]
+ *                      * sum_{k in block kb} e4m3(X[r][k]) * e4m3(W[g][n][k])
+ *     with sX(g,l,kb) = sA[M_start_g*(K/128) + l + kb*m_g]  (per-group blocks).
+ *
+ * Decoding is by 256-entry (16 for E2M1) tables built from the format
+ * definitions (OCP E4M3FN, E5M2, E2M1, E8M0).  Every operand row is decoded
+ * once into an FP64 buffer, then plain sequential dot products are taken.
+ *
+ * Parity is pinned by the CPU test-suite: closed-form decode points, exact
+ * rational brute force on tiny inputs, unit-scale = plain matmul, power-of-two
+ * equivariance, layout equivalence, grouped = per-group dense concatenation,
+ * and the scale-factor relayout round trip.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { FMT_E4M3 = 0, FMT_E5M2 = 1, FMT_E2M1 = 2 };
+enum { LAYOUT_NT = 0, LAYOUT_NN = 1, LAYOUT_TN = 2 };
+
+/* ------------------------------------------------------------------------ */
+/* Decode tables, from the bit-level definitions of each format.             */
+/* ------------------------------------------------------------------------ */
+static double T_E4M3[256], T_E5M2[256], T_E2M1[16], T_E8M0[256];
+static pthread_once_t tables_once = PTHREAD_ONCE_INIT;
+
+static void build_tables(void) {
+  for (int c = 0; c < 256; ++c) {
+    /* E4M3FN: 1 sign, 4 exponent (bias 7), 3 mantissa; S.1111.111 is NaN, no inf. */
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) v = NAN;
+    else if (e == 0) v = ldexp((double)m, -9);            /* m/8 * 2^(1-7) */
+    else v = ldexp(8.0 + m, e - 10);                        /* (1+m/8) * 2^(e-7) */
+    T_E4M3[c] = s ? -v : v;
+
+    /* E5M2: 1 sign, 5 exponent (bias 15), 2 mantissa; exponent 31 is inf/NaN. */
+    e = (c >> 2) & 31; m = c & 3;
+    if (e == 31) v = (m == 0) ? INFINITY : NAN;
+    else if (e == 0) v = ldexp((double)m, -16);            /* m/4 * 2^(1-15) */
+    else v = ldexp(4.0 + m, e - 17);                        /* (1+m/4) * 2^(e-15) */
+    T_E5M2[c] = s ? -v : v;
+
+    /* E8M0: unsigned power of two 2^(c-127); 0xFF is NaN. */
+    T_E8M0[c] = (c == 255) ? NAN : ldexp(1.0, c - 127);
+  }
+  for (int c = 0; c < 16; ++c) {
+    /* E2M1: 1 sign, 2 exponent (bias 1), 1 mantissa, no inf/NaN. */
+    int s = c >> 3, e = (c >> 1) & 3, m = c & 1;
+    double v = (e == 0) ? 0.5 * m : ldexp(2.0 + m, e - 2);  /* (1+m/2)*2^(e-1) */
+    T_E2M1[c] = s ? -v : v;
+  }
+}
+
+static void init_tables(void) { pthread_once(&tables_once, build_tables); }
+
+/* Copies one decode table out (fmt 0 E4M3, 1 E5M2, 2 E2M1, 3 E8M0). */
+int oracle_decode_table(int which, double* out) {
+  init_tables();
+  switch (which) {
+    case 0: memcpy(out, T_E4M3, sizeof T_E4M3); return 256;
+    case 1: memcpy(out, T_E5M2, sizeof T_E5M2); return 256;
+    case 2: memcpy(out, T_E2M1, sizeof T_E2M1); return 16;
+    case 3: memcpy(out, T_E8M0, sizeof T_E8M0); return 256;
+    default: return -1;
+  }
+}
+
+/* Element (i, k) of the logical [rows, K] view of an operand.
+ * rowmajor_k: the data is stored [rows][K] (K contiguous);
+ * otherwise it is stored [K][rows] (rows contiguous).
+ * FP4 is packed two per byte along K, even k in the low nibble. */
+static double elem(const uint8_t* X, int fmt, int rowmajor_k, int64_t rows, int64_t K,
+                   int64_t i, int64_t k) {
+  if (fmt == FMT_E2M1) {
+    /* packed FP4 exists only K-contiguous */
+    uint8_t byte = X[i * (K / 2) + k / 2];
+    return T_E2M1[(k & 1) ? (byte >> 4) : (byte & 15)];
+  }
+  uint8_t code = rowmajor_k ? X[i * K + k] : X[k * rows + i];
+  return fmt == FMT_E4M3 ? T_E4M3[code] : T_E5M2[code];
+}
+
+/* Decode logical row i of an operand, with its E8M0 block scales applied, into out[K]. */
+static void decode_row_scaled(const uint8_t* X, const uint8_t* S, int fmt, int rowmajor_k,
+                              int64_t rows, int64_t K, int64_t i, double* out) {
+  int64_t kb = K / 32;
+  for (int64_t k = 0; k < K; ++k)
+    out[k] = elem(X, fmt, rowmajor_k, rows, K, i, k) * T_E8M0[S[i * kb + k / 32]];
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dense MX GEMM.                                                            */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  const uint8_t *A, *sA, *B, *sB;
+  int64_t M, N, K;
+  int a_fmt, b_fmt, a_kcontig, b_kcontig;
+  const int64_t* rows; int64_t nrows;   /* output rows to evaluate */
+  const double* Adec;                   /* [nrows][K] decoded, scaled rows of op(A) */
+  double* D;                            /* [nrows][N] */
+  int64_t n0, n1;                       /* this worker's column range */
+} dense_job;
+
+static void* dense_worker(void* p) {
+  dense_job* j = (dense_job*)p;
+  double* brow = (double*)malloc(sizeof(double) * (size_t)(j->K > 0 ? j->K : 1));
+  for (int64_t n = j->n0; n < j->n1; ++n) {
+    decode_row_scaled(j->B, j->sB, j->b_fmt, j->b_kcontig, j->N, j->K, n, brow);
+    for (int64_t r = 0; r < j->nrows; ++r) {
+      const double* a = j->Adec + r * j->K;
+      double acc = 0.0;
+      for (int64_t k = 0; k < j->K; ++k) acc += a[k] * brow[k];
+      j->D[r * j->N + n] = acc;
+    }
+  }
+  free(brow);
+  return NULL;
+}
+
+/* Splits [0, n) across nthreads workers and runs fn on each. */
+static int run_parallel(void* jobs, size_t job_size, int nthreads, void* (*fn)(void*)) {
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  for (int t = 0; t < nthreads; ++t)
+    pthread_create(&th[t], NULL, fn, (char*)jobs + (size_t)t * job_size);
+  for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+  free(th);
+  return 0;
+}
+
+/*
+ * D[r][n] for r over `rows` (or all M rows when rows == NULL) and all n.
+ * layout: 0 NT (A[M][K], B[N][K]), 1 NN (A[M][K], B[K][N]), 2 TN (A[K][M], B[K][N]).
+ * sA is [M][K/32], sB is [N][K/32], always indexed by (row of op(X), K block).
+ * Returns 0 on success, -1 on an unsupported combination.
+ */
+int oracle_mx_gemm(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
+                   int64_t M, int64_t N, int64_t K, int layout, int a_fmt, int b_fmt,
+                   const int64_t* rows, int64_t nrows, double* D, int nthreads) {
+  init_tables();
+  if (K % 32 != 0 || M < 0 || N < 0 || K < 0) return -1;
+  if ((a_fmt == FMT_E2M1) != (b_fmt == FMT_E2M1)) return -1;
+  if (a_fmt == FMT_E2M1 && layout != LAYOUT_NT) return -1;
+  int a_kcontig = (layout != LAYOUT_TN);
+  int b_kcontig = (layout == LAYOUT_NT);
+  if (rows == NULL) nrows = M;
+  if (nrows == 0 || N == 0) return 0;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > N) nthreads = (int)N;
+
+  double* Adec = (double*)malloc(sizeof(double) * (size_t)(nrows * (K > 0 ? K : 1)));
+  for (int64_t r = 0; r < nrows; ++r)
+    decode_row_scaled(A, sA, a_fmt, a_kcontig, M, K, rows ? rows[r] : r, Adec + r * K);
+
+  dense_job* jobs = (dense_job*)malloc(sizeof(dense_job) * (size_t)nthreads);
+  for (int t = 0; t < nthreads; ++t) {
+    dense_job j = {A, sA, B, sB, M, N, K, a_fmt, b_fmt, a_kcontig, b_kcontig,
+                   rows, nrows, Adec, D, N * t / nthreads, N * (t + 1) / nthreads};
+    jobs[t] = j;
+  }
+  run_parallel(jobs, sizeof(dense_job), nthreads, dense_worker);
+  free(jobs);
+  free(Adec);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Grouped groupwise FP8 GEMM.                                               */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  const uint8_t *W;
+  const double* Xdec;                   /* [nrows][K] decoded sampled rows of X */
+  const float *sX, *sW;
+  int64_t N, K, KB;
+  int64_t nrows;
+  const int64_t *row_of, *grp_of, *loc_of, *start_of, *msz_of; /* per sampled row */
+  int G;
+  double* D;
+  int64_t n0, n1;
+} grouped_job;
+
+static void* grouped_worker(void* p) {
+  grouped_job* j = (grouped_job*)p;
+  double* wrow = (double*)malloc(sizeof(double) * (size_t)j->K);
+  for (int g = 0; g < j->G; ++g) {
+    int any = 0;
+    for (int64_t r = 0; r < j->nrows; ++r) any |= (j->grp_of[r] == g);
+    if (!any) continue;
+    for (int64_t n = j->n0; n < j->n1; ++n) {
+      const uint8_t* w = j->W + ((int64_t)g * j->N + n) * j->K;
+      for (int64_t k = 0; k < j->K; ++k) wrow[k] = T_E4M3[w[k]];
+      for (int64_t r = 0; r < j->nrows; ++r) {
+        if (j->grp_of[r] != g) continue;
+        const double* xrow = j->Xdec + r * j->K;
+        double acc = 0.0;
+        for (int64_t kb = 0; kb < j->KB; ++kb) {
+          double part = 0.0;
+          for (int64_t k = kb * 128; k < kb * 128 + 128; ++k) part += xrow[k] * wrow[k];
+          double sx = (double)j->sX[j->start_of[r] * j->KB + j->loc_of[r] + kb * j->msz_of[r]];
+          double sw = (double)j->sW[((int64_t)g * (j->N / 128) + n / 128) * j->KB + kb];
+          acc += sx * sw * part;
+        }
+        j->D[r * j->N + n] = acc;
+      }
+    }
+  }
+  free(wrow);
+  return 0;
+}
+
+/*
+ * X [total_M][K] E4M3, sX per-group block layout FP32, W [G][N][K] E4M3,
+ * sW [G][N/128][K/128] FP32, m_sizes [G] int64 (host).  Output rows `rows`
+ * (global row ids; NULL = all total_M rows) into D[nrows][N].
+ * Returns 0, or -1 on bad arguments (negative size, sum != total_M, N or K % 128).
+ */
+int oracle_grouped_fp8_gemm(const uint8_t* X, const float* sX, const uint8_t* W, const float* sW,
+                            const int64_t* m_sizes, int G, int64_t total_M, int64_t N, int64_t K,
+                            const int64_t* rows, int64_t nrows, double* D, int nthreads) {
+  init_tables();
+  if (N % 128 != 0 || K % 128 != 0 || G < 1) return -1;
+  int64_t sum = 0;
+  for (int g = 0; g < G; ++g) { if (m_sizes[g] < 0) return -1; sum += m_sizes[g]; }
+  if (sum != total_M) return -1;
+  if (rows == NULL) nrows = total_M;
+  if (nrows == 0 || N == 0) return 0;
+
+  int64_t* meta = (int64_t*)malloc(sizeof(int64_t) * (size_t)(5 * nrows));
+  int64_t *row_of = meta, *grp_of = meta + nrows, *loc_of = meta + 2 * nrows,
+          *start_of = meta + 3 * nrows, *msz_of = meta + 4 * nrows;
+  for (int64_t r = 0; r < nrows; ++r) {
+    int64_t row = rows ? rows[r] : r;
+    if (row < 0 || row >= total_M) { free(meta); return -1; }
+    int64_t start = 0;
+    int g = 0;
+    while (row >= start + m_sizes[g]) { start += m_sizes[g]; ++g; }
+    row_of[r] = row; grp_of[r] = g; loc_of[r] = row - start; start_of[r] = start;
+    msz_of[r] = m_sizes[g];
+  }
+  double* Xdec = (double*)malloc(sizeof(double) * (size_t)(nrows * K));
+  for (int64_t r = 0; r < nrows; ++r)
+    for (int64_t k = 0; k < K; ++k) Xdec[r * K + k] = T_E4M3[X[row_of[r] * K + k]];
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > N) nthreads = (int)N;
+  grouped_job* jobs = (grouped_job*)malloc(sizeof(grouped_job) * (size_t)nthreads);
+  for (int t = 0; t < nthreads; ++t) {
+    grouped_job j = {W, Xdec, sX, sW, N, K, K / 128, nrows, row_of, grp_of, loc_of, start_of,
+                     msz_of, G, D, N * t / nthreads, N * (t + 1) / nthreads};
+    jobs[t] = j;
+  }
+  run_parallel(jobs, sizeof(grouped_job), nthreads, grouped_worker);
+  free(jobs);
+  free(Xdec);
+  free(meta);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Scale-factor relayout (integer permutation).                              */
+/*                                                                           */
+/* Target: the tensor-core block-scale layout of 128-row x 4-block atoms of  */
+/* 512 bytes, atom (rb, kg) at byte (rb*KG + kg)*512, and inside an atom     */
+/* row r, block k at (r%32)*16 + (r/32)*4 + k.  Row blocks are padded to an  */
+/* even count (RB = 2*ceil(rows/256)) and block groups to an even count      */
+/* (KG = 2*ceil(kblocks/8)); padding bytes hold 127 (the E8M0 code of 1.0).  */
+/* ------------------------------------------------------------------------ */
+int64_t oracle_scale_tiled_bytes(int64_t rows, int64_t kblocks) {
+  int64_t RB = 2 * ((rows + 255) / 256), KG = 2 * ((kblocks + 7) / 8);
+  return RB * KG * 512;
+}
+
+void oracle_scale_relayout(const uint8_t* s, int64_t rows, int64_t kblocks, uint8_t* out) {
+  int64_t KG = 2 * ((kblocks + 7) / 8);
+  int64_t total = oracle_scale_tiled_bytes(rows, kblocks);
+  for (int64_t i = 0; i < total; ++i) out[i] = 127;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t kb = 0; kb < kblocks; ++kb) {
+      int64_t rb = r / 128, rr = r % 128, kg = kb / 4, kk = kb % 4;
+      out[(rb * KG + kg) * 512 + (rr % 32) * 16 + (rr / 32) * 4 + kk] = s[r * kblocks + kb];
+    }
+}

@@ -1,0 +1,334 @@
+"""Pins that tie the CPU oracle to something other than itself.
+
+Each ``pin_*`` function raises AssertionError when the oracle (the shared library
+handle ``lib``; None = the built oracle) disagrees with a fact fixed by the
+format definitions, exact arithmetic or an independent library routine.  The
+mutation tests run the same pins against copies of the oracle with a planted
+mistake and require each copy to fail at least one of them.
+"""
+from __future__ import annotations
+
+import os
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+import oracle
+import synthetic
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+# OCP E2M1 magnitudes for codes 0..7 (sign in bit 3).
+E2M1_VALUES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+E4M3_ONE = 0x38  # exponent field 7 (= bias), mantissa 0
+
+
+def torch_decode(codes: np.ndarray, fmt: str) -> np.ndarray:
+    """Decode uint8 codes with PyTorch's float8 dtypes (or the OCP E2M1 list)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    if fmt == "e2m1":
+        v = np.array(E2M1_VALUES, dtype=np.float64)
+        mag = v[c & 7]
+        return np.where(c & 8, -mag, mag)
+    dt = torch.float8_e4m3fn if fmt == "e4m3" else torch.float8_e5m2
+    return torch.from_numpy(c).view(dt).to(torch.float64).numpy()
+
+
+def unpack_fp4(packed: np.ndarray) -> np.ndarray:
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty((p.shape[0], p.shape[1] * 2), dtype=np.uint8)
+    out[:, 0::2] = p & 15
+    out[:, 1::2] = p >> 4
+    return out
+
+
+def logical_codes(X, fmt, kcontig, rows, K):
+    """[rows, K] view of stored codes (unpacking FP4; transposing MN-major storage)."""
+    if fmt == "e2m1":
+        return unpack_fp4(np.asarray(X).reshape(rows, K // 2))
+    X = np.asarray(X).reshape((rows, K) if kcontig else (K, rows))
+    return X if kcontig else X.T
+
+
+def random_finite_codes(g: np.random.Generator, shape, fmt) -> np.ndarray:
+    if fmt == "e2m1":
+        return g.integers(0, 16, size=shape, dtype=np.uint8)
+    c = g.integers(0, 256, size=shape, dtype=np.uint8)
+    if fmt == "e4m3":
+        bad = (c & 0x7F) == 0x7F
+    else:
+        bad = ((c >> 2) & 31) == 31
+    return np.where(bad, c & 0xF0, c).astype(np.uint8)
+
+
+# ---------------------------------------------------------------- decoding
+def pin_decode_points(lib=None):
+    e4 = oracle.decode_table("e4m3", lib)
+    e5 = oracle.decode_table("e5m2", lib)
+    e2 = oracle.decode_table("e2m1", lib)
+    e8 = oracle.decode_table("e8m0", lib)
+    assert e4[0x7E] == 448.0 and e4[0x08] == 2.0 ** -6 and e4[0x01] == 2.0 ** -9
+    assert e4[0xFE] == -448.0 and e4[E4M3_ONE] == 1.0 and e4[0x00] == 0.0
+    assert np.isnan(e4[0x7F]) and np.isnan(e4[0xFF])
+    assert e5[0x7B] == 57344.0 and e5[0x04] == 2.0 ** -14 and e5[0x01] == 2.0 ** -16
+    assert e5[0x3C] == 1.0 and np.isinf(e5[0x7C]) and np.isnan(e5[0x7D])
+    assert list(e2[:8]) == E2M1_VALUES and list(-e2[8:]) == E2M1_VALUES
+    assert e8[127] == 1.0 and e8[0] == 2.0 ** -127 and e8[254] == 2.0 ** 127
+    assert np.isnan(e8[255])
+
+
+def pin_decode_vs_torch(lib=None):
+    codes = np.arange(256, dtype=np.uint8)
+    for fmt in ("e4m3", "e5m2"):
+        ours = oracle.decode_table(fmt, lib)
+        ref = torch_decode(codes, fmt)
+        same = (ours == ref) | (np.isnan(ours) & np.isnan(ref))
+        assert same.all(), f"{fmt} codes differ: {np.nonzero(~same)[0][:8]}"
+
+
+# ---------------------------------------------------------------- dense
+def exact_dense(A, sA, B, sB, M, N, K, layout, a_fmt, b_fmt):
+    """Exact rational D = sum_k a*2^(sa-127) * b*2^(sb-127) (torch decode)."""
+    a = torch_decode(logical_codes(A, a_fmt, layout != "TN", M, K), a_fmt)
+    b = torch_decode(logical_codes(B, b_fmt, layout == "NT", N, K), b_fmt)
+    D = np.empty((M, N), dtype=object)
+    for m in range(M):
+        for n in range(N):
+            s = Fraction(0)
+            for k in range(K):
+                ea = Fraction(2) ** (int(sA[m, k // 32]) - 127)
+                eb = Fraction(2) ** (int(sB[n, k // 32]) - 127)
+                s += Fraction(a[m, k]) * ea * Fraction(b[n, k]) * eb
+            D[m, n] = s
+    return D
+
+
+def tiny_case(seed, M, N, K, layout, a_fmt, b_fmt, scale_lo=120, scale_hi=134):
+    g = np.random.default_rng([7, seed])
+    a_log = random_finite_codes(g, (M, K), a_fmt)
+    b_log = random_finite_codes(g, (N, K), b_fmt)
+    sA = g.integers(scale_lo, scale_hi + 1, size=(M, K // 32), dtype=np.uint8)
+    sB = g.integers(scale_lo, scale_hi + 1, size=(N, K // 32), dtype=np.uint8)
+    if a_fmt == "e2m1":
+        A, B = synthetic.pack_fp4(a_log), synthetic.pack_fp4(b_log)
+    else:
+        A = a_log if layout != "TN" else np.ascontiguousarray(a_log.T)
+        B = b_log if layout == "NT" else np.ascontiguousarray(b_log.T)
+    return A, sA, B, sB
+
+
+DENSE_COMBOS = [(l, a, b) for l in ("NT", "NN", "TN")
+                for a, b in (("e4m3", "e4m3"), ("e4m3", "e5m2"), ("e5m2", "e4m3"),
+                             ("e5m2", "e5m2"))] + [("NT", "e2m1", "e2m1")]
+
+
+def pin_dense_bruteforce(lib=None):
+    for i, (layout, af, bf) in enumerate(DENSE_COMBOS):
+        for (M, N, K) in ((4, 4, 32), (4, 4, 64), (3, 5, 96)):
+            A, sA, B, sB = tiny_case(i * 10 + K, M, N, K, layout, af, bf)
+            got = oracle.mx_gemm(A, sA, B, sB, M, N, K, layout, af, bf, nthreads=2, lib=lib)
+            ex = exact_dense(A, sA, B, sB, M, N, K, layout, af, bf)
+            for m in range(M):
+                for n in range(N):
+                    # a sequential FP64 sum is within (K-1)*2^-53*sum|terms| of exact;
+                    # use a generous multiple of 2^-50 of the result scale
+                    bound = 2.0 ** -40 * max(1.0, abs(float(ex[m, n])))
+                    assert abs(got[m, n] - float(ex[m, n])) <= bound, (layout, af, bf, M, N, K, m, n)
+    # FP4 with unit scales is exact in FP64 (small dyadic sums)
+    A, sA, B, sB = tiny_case(99, 4, 4, 64, "NT", "e2m1", "e2m1", 127, 127)
+    got = oracle.mx_gemm(A, sA, B, sB, 4, 4, 64, "NT", "e2m1", "e2m1", lib=lib)
+    ex = exact_dense(A, sA, B, sB, 4, 4, 64, "NT", "e2m1", "e2m1")
+    assert all(Fraction(got[m, n]) == ex[m, n] for m in range(4) for n in range(4))
+
+
+def pin_dense_unit_scales(lib=None):
+    """All scale codes 127: D equals the FP64 matmul of the torch-decoded operands."""
+    for i, (layout, af, bf) in enumerate(DENSE_COMBOS):
+        M, N, K = 9, 7, 128
+        A, sA, B, sB = tiny_case(500 + i, M, N, K, layout, af, bf, 127, 127)
+        got = oracle.mx_gemm(A, sA, B, sB, M, N, K, layout, af, bf, lib=lib)
+        a = torch_decode(logical_codes(A, af, layout != "TN", M, K), af)
+        b = torch_decode(logical_codes(B, bf, layout == "NT", N, K), bf)
+        ref = a @ b.T
+        tol = 2.0 ** -40 * np.abs(a) @ np.abs(b).T
+        assert np.all(np.abs(got - ref) <= tol + 0.0), (layout, af, bf)
+
+
+def pin_dense_pow2(lib=None):
+    """Adding k to every sA code scales D by exactly 2^k; per-row and per-column too."""
+    M, N, K = 6, 5, 96
+    for i, (layout, af, bf) in enumerate(DENSE_COMBOS):
+        A, sA, B, sB = tiny_case(900 + i, M, N, K, layout, af, bf)
+        base = oracle.mx_gemm(A, sA, B, sB, M, N, K, layout, af, bf, lib=lib)
+        for k in (-3, 5):
+            D = oracle.mx_gemm(A, (sA.astype(int) + k).astype(np.uint8), B, sB, M, N, K,
+                               layout, af, bf, lib=lib)
+            assert np.array_equal(D, base * 2.0 ** k)
+        rk = np.arange(M) - 2
+        D = oracle.mx_gemm(A, (sA.astype(int) + rk[:, None]).astype(np.uint8), B, sB, M, N, K,
+                           layout, af, bf, lib=lib)
+        assert np.array_equal(D, base * (2.0 ** rk)[:, None])
+        ck = 3 - np.arange(N)
+        D = oracle.mx_gemm(A, sA, B, (sB.astype(int) + ck[:, None]).astype(np.uint8), M, N, K,
+                           layout, af, bf, lib=lib)
+        assert np.array_equal(D, base * (2.0 ** ck)[None, :])
+
+
+def pin_dense_layouts(lib=None):
+    """NT on (A, B) equals NN on (A, B^T) and TN on (A^T, B^T), bitwise."""
+    M, N, K = 7, 6, 160
+    for i, (af, bf) in enumerate((("e4m3", "e4m3"), ("e5m2", "e4m3"), ("e4m3", "e5m2"))):
+        A, sA, B, sB = tiny_case(1300 + i, M, N, K, "NT", af, bf)
+        nt = oracle.mx_gemm(A, sA, B, sB, M, N, K, "NT", af, bf, lib=lib)
+        nn = oracle.mx_gemm(A, sA, np.ascontiguousarray(B.T), sB, M, N, K, "NN", af, bf, lib=lib)
+        tn = oracle.mx_gemm(np.ascontiguousarray(A.T), sA, np.ascontiguousarray(B.T), sB, M, N, K,
+                            "TN", af, bf, lib=lib)
+        assert np.array_equal(nt, nn) and np.array_equal(nt, tn)
+        rows = np.array([5, 0, 3])
+        assert np.array_equal(oracle.mx_gemm(A, sA, B, sB, M, N, K, "NT", af, bf, rows=rows,
+                                             lib=lib), nt[rows])
+
+
+# ---------------------------------------------------------------- grouped
+def grouped_reference(case):
+    """Per-group dense sums with numpy matmuls over each 128-K block (row-major scales)."""
+    X, W, sW = case["X"], case["W"], case["sW"]
+    sx = case["sx_rowmajor"]
+    N, K = case["N"], case["K"]
+    xd = torch_decode(X, "e4m3")
+    out = np.zeros((X.shape[0], N))
+    start = 0
+    for g, m in enumerate(case["m_sizes"].tolist()):
+        wd = torch_decode(W[g], "e4m3")
+        for kb in range(K // 128):
+            ks = slice(kb * 128, kb * 128 + 128)
+            part = xd[start:start + m, ks] @ wd[:, ks].T
+            scale = sx[start:start + m, kb][:, None].astype(np.float64) * \
+                np.repeat(sW[g, :, kb].astype(np.float64), 128)[None, :]
+            out[start:start + m] += scale * part
+        start += m
+    return out
+
+
+def pin_grouped_concat(lib=None):
+    for case_id, sizes in enumerate(([0, 37, 128, 0, 1, 90, 129, 3], [300], [0, 0, 5, 0],
+                                     [1, 0, 127, 129, 0, 2, 64, 11])):
+        ms = np.array(sizes, dtype=np.int64)
+        case = synthetic.grouped_operands((40, case_id), ms, 256, 384)
+        got = oracle.grouped_fp8_gemm(case["X"], case["sX"], case["W"], case["sW"], ms, 256, 384,
+                                      lib=lib)
+        ref = grouped_reference(case)
+        assert got.shape == ref.shape == (int(ms.sum()), 256)
+        assert np.allclose(got, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max()), sizes
+
+
+def pin_grouped_g1_transpose(lib=None):
+    """With G = 1 the per-group block layout is the plain [K/128, total_M] transpose."""
+    ms = np.array([200], dtype=np.int64)
+    case = synthetic.grouped_operands((41, 0), ms, 128, 512)
+    sx_t = np.ascontiguousarray(case["sx_rowmajor"].T).reshape(-1)
+    a = oracle.grouped_fp8_gemm(case["X"], case["sX"], case["W"], case["sW"], ms, 128, 512, lib=lib)
+    b = oracle.grouped_fp8_gemm(case["X"], sx_t, case["W"], case["sW"], ms, 128, 512, lib=lib)
+    assert np.array_equal(a, b)
+
+
+def probe_rowgroup(m_sizes, N, K, kb_hot):
+    """Row/group index probe: every D[r, n] = ((l mod 256) + 1) * 2^g, exact in BF16.
+
+    W codes are all 1.0; X is 0 except X[r, 128*kb_hot] = 1; sX(g,l,kb_hot) =
+    (l mod 256) + 1 and 7 elsewhere; sW[g][:][kb_hot] = 2^g and 5 elsewhere.
+    """
+    ms = np.asarray(m_sizes, dtype=np.int64)
+    G, T, KB = ms.size, int(ms.sum()), K // 128
+    X = np.zeros((T, K), dtype=np.uint8)
+    X[:, 128 * kb_hot] = E4M3_ONE
+    W = np.full((G, N, K), E4M3_ONE, dtype=np.uint8)
+    sx = np.full((T, KB), 7.0, dtype=np.float32)
+    expect = np.zeros((T, N), dtype=np.float64)
+    sW = np.full((G, N // 128, KB), 5.0, dtype=np.float32)
+    start = 0
+    for g, m in enumerate(ms.tolist()):
+        loc = np.arange(m)
+        sx[start:start + m, kb_hot] = (loc % 256) + 1
+        sW[g, :, kb_hot] = 2.0 ** g
+        expect[start:start + m] = (((loc % 256) + 1) * 2.0 ** g)[:, None]
+        start += m
+    sX = synthetic.to_group_block_layout(sx, ms)
+    return dict(X=X, sX=sX, W=W, sW=sW, m_sizes=ms, N=N, K=K), expect
+
+
+def probe_column(m_sizes, N, K):
+    """Column probe: D[r, n] = ((n mod 8) + 1) * 2^(n/128 mod 8) for every row."""
+    ms = np.asarray(m_sizes, dtype=np.int64)
+    G, T, KB = ms.size, int(ms.sum()), K // 128
+    X = np.zeros((T, K), dtype=np.uint8)
+    X[:, 0] = E4M3_ONE
+    n = np.arange(N)
+    W = np.zeros((G, N, K), dtype=np.uint8)
+    W[:, :, 0] = synthetic.encode(((n % 8) + 1).astype(np.float32), "e4m3")[None, :]
+    sW = np.full((G, N // 128, KB), 3.0, dtype=np.float32)
+    sW[:, :, 0] = (2.0 ** (np.arange(N // 128) % 8))[None, :]
+    sX = synthetic.to_group_block_layout(np.ones((T, KB), dtype=np.float32), ms)
+    expect = np.broadcast_to((((n % 8) + 1) * 2.0 ** ((n // 128) % 8))[None, :], (T, N))
+    return dict(X=X, sX=sX, W=W, sW=sW, m_sizes=ms, N=N, K=K), np.array(expect)
+
+
+def pin_grouped_probes(lib=None):
+    for sizes in ([3, 0, 300, 1, 0, 129, 2, 5], [260], [0, 0, 0, 7]):
+        for kb_hot in (0, 1, 2):
+            case, expect = probe_rowgroup(sizes, 256, 384, kb_hot)
+            got = oracle.grouped_fp8_gemm(case["X"], case["sX"], case["W"], case["sW"],
+                                          case["m_sizes"], 256, 384, lib=lib)
+            assert np.array_equal(got, expect), (sizes, kb_hot)
+        case, expect = probe_column(sizes, 1024, 256)
+        got = oracle.grouped_fp8_gemm(case["X"], case["sX"], case["W"], case["sW"],
+                                      case["m_sizes"], 1024, 256, lib=lib)
+        assert np.array_equal(got, expect), sizes
+
+
+# ---------------------------------------------------------------- relayout
+def load_atom_positions():
+    """(row, kblock, byte offset) triples from the hand-derived golden fixture."""
+    out = []
+    with open(os.path.join(GOLDEN, "sf_atom_positions.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                r, k, off = (int(t) for t in line.split())
+                out.append((r, k, off))
+    return out
+
+
+def pin_relayout(lib=None):
+    # sizes: row blocks padded to an even count of 128-row blocks, block groups to even
+    assert oracle.scale_tiled_bytes(1, 1, lib) == 2 * 2 * 512
+    assert oracle.scale_tiled_bytes(256, 8, lib) == 2 * 2 * 512
+    assert oracle.scale_tiled_bytes(257, 9, lib) == 4 * 4 * 512
+    rows, kblocks = 300, 11
+    RB, KG = 4, 4
+    # identify every output byte's source (row, kblock) with two passes of distinct values
+    r_ids = np.repeat((np.arange(rows) % 251)[:, None], kblocks, axis=1).astype(np.uint8)
+    k_ids = np.repeat(np.arange(kblocks)[None, :], rows, axis=0).astype(np.uint8)
+    hi = np.repeat((np.arange(rows) // 251)[:, None], kblocks, axis=1).astype(np.uint8)
+    out_r = oracle.scale_relayout(r_ids, lib)
+    out_k = oracle.scale_relayout(k_ids, lib)
+    out_h = oracle.scale_relayout(hi, lib)
+    ones = oracle.scale_relayout(np.zeros((rows, kblocks), dtype=np.uint8), lib)
+    assert out_r.size == RB * KG * 512
+    is_data = ones == 0
+    assert is_data.sum() == rows * kblocks            # every input byte appears once
+    assert np.all(ones[~is_data] == 127)              # padding holds the code of 1.0
+    src_r = out_h[is_data].astype(int) * 251 + out_r[is_data].astype(int)
+    src_k = out_k[is_data].astype(int)
+    assert len(set(zip(src_r.tolist(), src_k.tolist()))) == rows * kblocks
+    pos = {(r, k): p for r, k, p in zip(src_r.tolist(), src_k.tolist(),
+                                        np.nonzero(is_data)[0].tolist())}
+    for r, k, off in load_atom_positions():
+        rb, kg = r // 128, k // 4
+        assert pos[(r, k)] == (rb * KG + kg) * 512 + off, (r, k)
+
+
+ALL_PINS = [pin_decode_points, pin_decode_vs_torch, pin_dense_bruteforce, pin_dense_unit_scales,
+            pin_dense_pow2, pin_dense_layouts, pin_grouped_concat, pin_grouped_g1_transpose,
+            pin_grouped_probes, pin_relayout]

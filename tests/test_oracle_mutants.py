@@ -1,0 +1,47 @@
+"""Plant plausible mistakes in copies of the oracle and require the pins to catch
+each one.  Shows that the pins constrain every part of the oracle's arithmetic."""
+import os
+
+import pytest
+
+import oracle
+from tests import _pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, original text, mutated text) -- each a mistake a careful reader could make
+MUTANTS = [
+    ("e4m3_bias_off_by_one", "v = ldexp(8.0 + m, e - 10);", "v = ldexp(8.0 + m, e - 11);"),
+    ("e4m3_subnormal_scale", "v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
+    ("e5m2_mantissa_width", "v = ldexp(4.0 + m, e - 17);", "v = ldexp(4.0 + m, e - 16);"),
+    ("e2m1_subnormal", "0.5 * m", "1.0 * m"),
+    ("e8m0_bias", "ldexp(1.0, c - 127)", "ldexp(1.0, c - 128)"),
+    ("scale_block_width", "S[i * kb + k / 32]", "S[i * kb + k / 64]"),
+    ("mn_major_read_transposed", "X[k * rows + i]", "X[i * K + k]"),
+    ("nn_treated_as_nt", "int b_kcontig = (layout == LAYOUT_NT);", "int b_kcontig = 1;"),
+    ("grouped_sx_rowmajor_in_group",
+     "j->start_of[r] * j->KB + j->loc_of[r] + kb * j->msz_of[r]",
+     "j->start_of[r] * j->KB + j->loc_of[r] * j->KB + kb"),
+    ("grouped_sw_drops_nblock",
+     "sW[((int64_t)g * (j->N / 128) + n / 128) * j->KB + kb]",
+     "sW[((int64_t)g * (j->N / 128)) * j->KB + kb]"),
+    ("grouped_block_boundary", "k < kb * 128 + 128", "k < kb * 128 + 64"),
+    ("relayout_line_order", "(rr % 32) * 16 + (rr / 32) * 4 + kk", "(rr / 4) * 16 + (rr % 4) * 4 + kk"),
+    ("relayout_atom_order", "(rb * KG + kg) * 512", "(kg * 2 + rb) * 512"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(tmp_path, name, old, new):
+    text = open(SRC).read()
+    assert text.count(old) >= 1, f"mutation anchor missing: {old}"
+    mutated = tmp_path / "oracle_mutant.c"
+    mutated.write_text(text.replace(old, new))
+    lib = oracle.bind(oracle.compile_c(str(mutated), str(tmp_path / "libmutant.so")))
+    failures = []
+    for pin in _pins.ALL_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, ValueError, KeyError, IndexError):
+            failures.append(pin.__name__)
+    assert failures, f"no pin caught mutant {name}"

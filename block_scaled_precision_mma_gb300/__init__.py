@@ -1,0 +1,192 @@
+"""Python binding of libbsmma, the sm_103a block-scaled GEMM library.
+
+Argument marshalling only: every entry point forwards device pointers, int64
+sizes and the current CUDA stream to the C ABI declared in ``include/bsmma.h``;
+all arithmetic runs in the library's CUDA kernels.  There is no fallback: if the
+shared library is missing or fails to load, every call raises.
+
+Functions mirror the C names:
+
+* :func:`mx_gemm`, :func:`mx_gemm_tiled` -- dense MXFP8 / MXFP4 GEMM, BF16 out.
+* :func:`grouped_fp8_gemm` -- grouped groupwise FP8 GEMM, BF16 out.
+* :func:`mx_scale_relayout`, :func:`mx_scale_tiled_bytes` -- scale-factor relayout.
+* :func:`device_status`, :func:`reserve_workspace`, :func:`set_wait_limit_ns`,
+  :func:`launch_count`, :func:`probe_wait_timeout`, :func:`status_string`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB_PATH, build
+
+__all__ = ["mx_gemm", "mx_gemm_tiled", "grouped_fp8_gemm", "mx_scale_relayout",
+           "mx_scale_tiled_bytes", "device_status", "reserve_workspace", "set_wait_limit_ns",
+           "launch_count", "probe_wait_timeout", "status_string", "BsmmaError", "load",
+           "LAYOUTS", "FORMATS", "build", "LIB_PATH"]
+
+LAYOUTS = {"NT": 0, "NN": 1, "TN": 2}
+FORMATS = {"e4m3": 0, "e5m2": 1, "e2m1": 2}
+STATUS = ["BSMMA_OK", "BSMMA_ERR_INVALID_ARG", "BSMMA_ERR_UNSUPPORTED", "BSMMA_ERR_MISALIGNED",
+          "BSMMA_ERR_WORKSPACE", "BSMMA_ERR_CUDA", "BSMMA_DEV_TIMEOUT", "BSMMA_DEV_BAD_MSIZES"]
+
+_lib = None
+_lock = threading.Lock()
+
+
+class BsmmaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        name = STATUS[code] if 0 <= code < len(STATUS) else f"status {code}"
+        super().__init__(f"{where}: {name}")
+
+
+def load(path: str | None = None):
+    """Loads libbsmma.so (built in-tree by ``build()``) and declares its ABI."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"libbsmma.so not built ({path}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.mx_gemm.argtypes = [p, p, p, p, p, i64, i64, i64, i32, i32, i32, p]
+        lib.mx_gemm_tiled.argtypes = [p, p, p, p, p, i64, i64, i64, i32, i32, i32, p]
+        lib.grouped_fp8_gemm.argtypes = [p, p, p, p, p, p, i64, i32, i64, i64, p]
+        lib.mx_scale_relayout.argtypes = [p, i64, i64, p, p]
+        lib.mx_scale_tiled_bytes.argtypes = [i64, i64]
+        lib.mx_scale_tiled_bytes.restype = i64
+        lib.bsmma_reserve_workspace.argtypes = [i64, p]
+        lib.bsmma_device_status.argtypes = [p]
+        lib.bsmma_set_wait_limit_ns.argtypes = [i64]
+        lib.bsmma_status_string.argtypes = [i32]
+        lib.bsmma_status_string.restype = ctypes.c_char_p
+        lib.bsmma_launch_count.argtypes = []
+        lib.bsmma_launch_count.restype = i64
+        lib.bsmma_probe_wait_timeout.argtypes = [i64, p]
+        for name in ("mx_gemm", "mx_gemm_tiled", "grouped_fp8_gemm", "mx_scale_relayout",
+                     "bsmma_reserve_workspace", "bsmma_device_status", "bsmma_set_wait_limit_ns",
+                     "bsmma_probe_wait_timeout"):
+            getattr(lib, name).restype = i32
+        _lib = lib
+        return lib
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream) if hasattr(s, "cuda_stream") else int(s)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise BsmmaError(code, where)
+
+
+def mx_gemm(A, sA, B, sB, layout="NT", a_fmt="e4m3", b_fmt="e4m3", out=None, M=None, N=None,
+            K=None, stream=None, tiled=False):
+    """D = op(A) . op(B)^T in BF16 for MX operands (see ``mx_gemm`` in bsmma.h).
+
+    A, B: 1-byte tensors in the storage layout of `layout` (FP4 packed, NT only);
+    sA [M, K/32], sB [N, K/32] uint8 E8M0 codes (or tiled buffers when
+    ``tiled=True``).  Sizes are taken from the shapes unless given.
+    """
+    fp4 = a_fmt == "e2m1"
+    if M is None or N is None or K is None:
+        if layout == "NT":
+            M, kk = A.shape
+            N = B.shape[0]
+        elif layout == "NN":
+            M, kk = A.shape
+            N = B.shape[1]
+        else:
+            kk, M = A.shape
+            N = B.shape[1]
+        K = kk * 2 if fp4 else kk
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    fn = load().mx_gemm_tiled if tiled else load().mx_gemm
+    _check(fn(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(out), M, N, K, LAYOUTS[layout],
+              FORMATS[a_fmt], FORMATS[b_fmt], _stream(stream)),
+           "mx_gemm_tiled" if tiled else "mx_gemm")
+    return out
+
+
+def mx_gemm_tiled(A, sA_tiled, B, sB_tiled, layout="NT", a_fmt="e4m3", b_fmt="e4m3", out=None,
+                  M=None, N=None, K=None, stream=None):
+    """``mx_gemm`` with scales already relayouted by :func:`mx_scale_relayout`."""
+    return mx_gemm(A, sA_tiled, B, sB_tiled, layout, a_fmt, b_fmt, out, M, N, K, stream,
+                   tiled=True)
+
+
+def grouped_fp8_gemm(X, sX, W, sW, m_sizes, out=None, stream=None):
+    """Grouped groupwise FP8 GEMM (see ``grouped_fp8_gemm`` in bsmma.h).
+
+    X [total_M, K] E4M3 codes, sX float32 per-group block layout, W [G, N, K] E4M3,
+    sW float32 [G, N/128, K/128], m_sizes int64 [G] on the device.
+    """
+    total_M, K = X.shape
+    G, N, _ = W.shape
+    if m_sizes.dtype != torch.int64 or m_sizes.numel() != G or m_sizes.dim() != 1:
+        raise ValueError("m_sizes must be a 1-D int64 tensor of length G")
+    if out is None:
+        out = torch.empty((total_M, N), dtype=torch.bfloat16, device=W.device)
+    _check(load().grouped_fp8_gemm(_ptr(X) if total_M else None, _ptr(sX) if total_M else None,
+                                   _ptr(W), _ptr(sW), _ptr(out) if total_M else None,
+                                   _ptr(m_sizes), total_M, G, N, K, _stream(stream)),
+           "grouped_fp8_gemm")
+    return out
+
+
+def mx_scale_tiled_bytes(rows: int, kblocks: int) -> int:
+    return int(load().mx_scale_tiled_bytes(rows, kblocks))
+
+
+def mx_scale_relayout(s_plain, out=None, stream=None):
+    """Plain E8M0 scales [rows, kblocks] -> tensor-core atom layout (flat uint8)."""
+    rows, kblocks = s_plain.shape
+    if out is None:
+        out = torch.empty(mx_scale_tiled_bytes(rows, kblocks), dtype=torch.uint8,
+                          device=s_plain.device)
+    _check(load().mx_scale_relayout(_ptr(s_plain), rows, kblocks, _ptr(out), _stream(stream)),
+           "mx_scale_relayout")
+    return out
+
+
+def reserve_workspace(nbytes: int, stream=None):
+    _check(load().bsmma_reserve_workspace(nbytes, _stream(stream)), "bsmma_reserve_workspace")
+
+
+def device_status(stream=None) -> int:
+    """Synchronises the stream; returns and clears the latched device status code."""
+    return int(load().bsmma_device_status(_stream(stream)))
+
+
+def set_wait_limit_ns(ns: int):
+    _check(load().bsmma_set_wait_limit_ns(int(ns)), "bsmma_set_wait_limit_ns")
+
+
+def launch_count() -> int:
+    return int(load().bsmma_launch_count())
+
+
+def status_string(code: int) -> str:
+    return load().bsmma_status_string(int(code)).decode()
+
+
+def probe_wait_timeout(limit_ns: int, stream=None) -> int:
+    return int(load().bsmma_probe_wait_timeout(int(limit_ns), _stream(stream)))

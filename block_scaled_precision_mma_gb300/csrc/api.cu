@@ -1,0 +1,307 @@
+// api.cu -- the C ABI: argument validation, per-device state, the scale workspace,
+// the device-status word, tensor-map encoding and the wait-timeout probe.
+//
+// Validation follows the source pages' preconditions: 64-bit extents everywhere
+// (launch arguments that overflowed 32 bits: "Experimental FlyDSL GEMM backend for
+// TE PyTorch", BF16 skipped shapes; "Add FlyDSL grouped groupwise FP8 GEMM for
+// ROCm", the commit passing operands with their natural shape), N and K multiples
+// of 128 and m_sizes of length G for the grouped GEMM (same page, introduction and
+// the format/rank check commit), OCP FP8 formats only.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace bsmma {
+
+// Latched device-side status, one per device that loads the library.
+__device__ int g_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ready[kMaxDevices];
+std::atomic<int64_t> g_launches{0};
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+struct Workspace {
+  int device;
+  cudaStream_t stream;
+  void* ptr;
+  int64_t bytes;
+};
+std::vector<Workspace> g_ws;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+const DeviceInfo* current_device(bsmma_status* err) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *err = BSMMA_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_dev_ready[dev]) {
+    DeviceInfo d;
+    d.device = dev;
+    void* status = nullptr;
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaGetSymbolAddress(&status, g_device_status) != cudaSuccess) {
+      *err = BSMMA_ERR_CUDA;
+      return nullptr;
+    }
+    d.status = static_cast<int*>(status);
+    g_dev[dev] = d;
+    g_dev_ready[dev] = true;
+  }
+  return &g_dev[dev];
+}
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
+void count_launches(int n) { g_launches += n; }
+
+bsmma_status encode_tmap_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                            uint64_t row_stride, uint32_t box_inner, uint32_t box_outer) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return BSMMA_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+  }
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BSMMA_OK : BSMMA_ERR_INVALID_ARG;
+}
+
+namespace {
+
+__global__ void wait_probe_kernel(int* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // Nothing ever arrives on `bar`: the bounded wait must give up and latch a timeout.
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, limit_ns, &abort_flag, status);
+}
+
+constexpr int64_t kMaxTmaDim = (int64_t(1) << 32) - 1;
+constexpr int64_t kMaxStride = (int64_t(1) << 40) - 16;
+
+bsmma_status validate_dense(const void* A, const void* sA, const void* B, const void* sB,
+                            const void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
+                            bsmma_fmt a_fmt, bsmma_fmt b_fmt) {
+  if (M < 0 || N < 0 || K < 0 || K % 32 != 0) return BSMMA_ERR_INVALID_ARG;
+  if (layout < BSMMA_NT || layout > BSMMA_TN) return BSMMA_ERR_INVALID_ARG;
+  if (a_fmt < BSMMA_E4M3 || a_fmt > BSMMA_E2M1 || b_fmt < BSMMA_E4M3 || b_fmt > BSMMA_E2M1)
+    return BSMMA_ERR_INVALID_ARG;
+  const bool fp4a = a_fmt == BSMMA_E2M1, fp4b = b_fmt == BSMMA_E2M1;
+  if (fp4a != fp4b) return BSMMA_ERR_UNSUPPORTED;
+  if (fp4a && layout != BSMMA_NT) return BSMMA_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return BSMMA_OK;
+  if (!D) return BSMMA_ERR_INVALID_ARG;
+  if (N % 8 != 0 || !aligned16(D)) return BSMMA_ERR_MISALIGNED;
+  if (K == 0) return BSMMA_OK;
+  if (!A || !B || !sA || !sB) return BSMMA_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(sA) || !aligned16(sB))
+    return BSMMA_ERR_MISALIGNED;
+  if (layout != BSMMA_NT && N % 16 != 0) return BSMMA_ERR_MISALIGNED;
+  if (layout == BSMMA_TN && M % 16 != 0) return BSMMA_ERR_MISALIGNED;
+  if (M > kMaxTmaDim || N > kMaxTmaDim || K > kMaxTmaDim) return BSMMA_ERR_INVALID_ARG;
+  if (M > kMaxStride || N > kMaxStride || K > kMaxStride) return BSMMA_ERR_INVALID_ARG;
+  // tile ids are 32-bit
+  if ((M + 127) / 128 * ((N + 255) / 256) > INT32_MAX / 2) return BSMMA_ERR_INVALID_ARG;
+  return BSMMA_OK;
+}
+
+// Workspace of at least `bytes` for (current device, stream).
+bsmma_status get_workspace(int64_t bytes, cudaStream_t stream, void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BSMMA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace* w = nullptr;
+  for (auto& e : g_ws)
+    if (e.device == dev && e.stream == stream) w = &e;
+  if (w && w->bytes >= bytes) {
+    *out = w->ptr;
+    return BSMMA_OK;
+  }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return BSMMA_ERR_CUDA;
+  if (cap != cudaStreamCaptureStatusNone) return BSMMA_ERR_WORKSPACE;
+  int64_t grow = bytes + bytes / 4 + 4096;
+  void* p = nullptr;
+  if (cudaMalloc(&p, static_cast<size_t>(grow)) != cudaSuccess) return BSMMA_ERR_CUDA;
+  if (w) {
+    // earlier kernels on this stream may still read the old buffer
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+      cudaFree(p);
+      return BSMMA_ERR_CUDA;
+    }
+    cudaFree(w->ptr);
+    w->ptr = p;
+    w->bytes = grow;
+  } else {
+    g_ws.push_back(Workspace{dev, stream, p, grow});
+  }
+  *out = p;
+  return BSMMA_OK;
+}
+
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+}  // namespace bsmma
+
+using namespace bsmma;
+
+extern "C" {
+
+int64_t mx_scale_tiled_bytes(int64_t rows, int64_t kblocks) {
+  if (rows <= 0 || kblocks <= 0) return 0;
+  return 2 * ((rows + 255) / 256) * 2 * ((kblocks + 7) / 8) * 512;
+}
+
+bsmma_status mx_scale_relayout(const uint8_t* s_plain, int64_t rows, int64_t kblocks,
+                               uint8_t* s_tiled, bsmma_stream stream) {
+  if (rows < 0 || kblocks < 0) return BSMMA_ERR_INVALID_ARG;
+  if (rows == 0 || kblocks == 0) return BSMMA_OK;
+  if (!s_plain || !s_tiled) return BSMMA_ERR_INVALID_ARG;
+  if (!aligned16(s_tiled)) return BSMMA_ERR_MISALIGNED;
+  return launch_relayout(s_plain, rows, kblocks, s_tiled, nullptr, 0, 0, nullptr,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+bsmma_status mx_gemm_tiled(const void* A, const uint8_t* sA_tiled, const void* B,
+                           const uint8_t* sB_tiled, void* D, int64_t M, int64_t N, int64_t K,
+                           bsmma_layout layout, bsmma_fmt a_fmt, bsmma_fmt b_fmt,
+                           bsmma_stream stream) {
+  bsmma_status st = validate_dense(A, sA_tiled, B, sB_tiled, D, M, N, K, layout, a_fmt, b_fmt);
+  if (st != BSMMA_OK || M == 0 || N == 0) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return cuda_ok(cudaMemsetAsync(D, 0, static_cast<size_t>(M * N * 2), s));
+  return launch_mx_gemm(A, sA_tiled, B, sB_tiled, D, M, N, K, layout, a_fmt, b_fmt, s);
+}
+
+bsmma_status mx_gemm(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB, void* D,
+                     int64_t M, int64_t N, int64_t K, bsmma_layout layout, bsmma_fmt a_fmt,
+                     bsmma_fmt b_fmt, bsmma_stream stream) {
+  bsmma_status st = validate_dense(A, sA, B, sB, D, M, N, K, layout, a_fmt, b_fmt);
+  if (st != BSMMA_OK || M == 0 || N == 0) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return cuda_ok(cudaMemsetAsync(D, 0, static_cast<size_t>(M * N * 2), s));
+  const int64_t bytes_a = align_up(mx_scale_tiled_bytes(M, K / 32), 256);
+  const int64_t bytes_b = mx_scale_tiled_bytes(N, K / 32);
+  void* ws = nullptr;
+  st = get_workspace(bytes_a + bytes_b, s, &ws);
+  if (st != BSMMA_OK) return st;
+  uint8_t* ta = static_cast<uint8_t*>(ws);
+  uint8_t* tb = ta + bytes_a;
+  st = launch_relayout(sA, M, K / 32, ta, sB, N, K / 32, tb, s);
+  if (st != BSMMA_OK) return st;
+  return launch_mx_gemm(A, ta, B, tb, D, M, N, K, layout, a_fmt, b_fmt, s);
+}
+
+bsmma_status grouped_fp8_gemm(const uint8_t* A, const float* sA, const uint8_t* B,
+                              const float* sB, void* D, const int64_t* m_sizes, int64_t total_M,
+                              int G, int64_t N, int64_t K, bsmma_stream stream) {
+  if (G < 1 || G > 64 || total_M < 0 || N <= 0 || K <= 0) return BSMMA_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 128 != 0) return BSMMA_ERR_INVALID_ARG;
+  if (!B || !sB || !m_sizes) return BSMMA_ERR_INVALID_ARG;
+  if (total_M > 0 && (!A || !sA || !D)) return BSMMA_ERR_INVALID_ARG;
+  if (!aligned16(B) || (total_M > 0 && (!aligned16(A) || !aligned16(D))) ||
+      (reinterpret_cast<uintptr_t>(m_sizes) & 7u) != 0)
+    return BSMMA_ERR_MISALIGNED;
+  if (total_M >= INT32_MAX || static_cast<int64_t>(G) * N >= INT32_MAX || K > kMaxStride)
+    return BSMMA_ERR_INVALID_ARG;
+  return launch_grouped(A, sA, B, sB, D, m_sizes, total_M, G, N, K,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+bsmma_status bsmma_reserve_workspace(int64_t bytes, bsmma_stream stream) {
+  if (bytes < 0) return BSMMA_ERR_INVALID_ARG;
+  void* p = nullptr;
+  return get_workspace(bytes, reinterpret_cast<cudaStream_t>(stream), &p);
+}
+
+bsmma_status bsmma_device_status(bsmma_stream stream) {
+  bsmma_status st;
+  const DeviceInfo* dev = current_device(&st);
+  if (!dev) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int v = 0, zero = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return BSMMA_ERR_CUDA;
+  if (cudaMemcpy(&v, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return BSMMA_ERR_CUDA;
+  return static_cast<bsmma_status>(v);
+}
+
+bsmma_status bsmma_set_wait_limit_ns(int64_t ns) {
+  if (ns <= 0) return BSMMA_ERR_INVALID_ARG;
+  g_wait_limit_ns = static_cast<uint64_t>(ns);
+  return BSMMA_OK;
+}
+
+const char* bsmma_status_string(bsmma_status s) {
+  switch (s) {
+    case BSMMA_OK: return "BSMMA_OK";
+    case BSMMA_ERR_INVALID_ARG: return "BSMMA_ERR_INVALID_ARG";
+    case BSMMA_ERR_UNSUPPORTED: return "BSMMA_ERR_UNSUPPORTED";
+    case BSMMA_ERR_MISALIGNED: return "BSMMA_ERR_MISALIGNED";
+    case BSMMA_ERR_WORKSPACE: return "BSMMA_ERR_WORKSPACE";
+    case BSMMA_ERR_CUDA: return "BSMMA_ERR_CUDA";
+    case BSMMA_DEV_TIMEOUT: return "BSMMA_DEV_TIMEOUT";
+    case BSMMA_DEV_BAD_MSIZES: return "BSMMA_DEV_BAD_MSIZES";
+    default: return "BSMMA_UNKNOWN_STATUS";
+  }
+}
+
+int64_t bsmma_launch_count(void) { return g_launches.load(); }
+
+bsmma_status bsmma_probe_wait_timeout(int64_t limit_ns, bsmma_stream stream) {
+  if (limit_ns <= 0 || limit_ns > 10000000000ll) return BSMMA_ERR_INVALID_ARG;
+  bsmma_status st;
+  const DeviceInfo* dev = current_device(&st);
+  if (!dev) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  st = bsmma_device_status(stream);   // clear anything latched before
+  if (st == BSMMA_ERR_CUDA) return st;
+  wait_probe_kernel<<<1, 32, 0, s>>>(dev->status, static_cast<uint64_t>(limit_ns));
+  count_launches(1);
+  if (cudaGetLastError() != cudaSuccess) return BSMMA_ERR_CUDA;
+  return bsmma_device_status(stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,319 @@
+// grouped_gemm.cu -- grouped groupwise FP8 GEMM for sm_103a.
+//
+// X [total_M][K] E4M3 with one FP32 scale per row per 128-K block (per-group block
+// layout), W [G][N][K] E4M3 with one FP32 scale per 128x128 block, groups of uneven
+// or zero size, BF16 output ("Add FlyDSL grouped groupwise FP8 GEMM for ROCm":
+// introduction; the commit that replaced the host tile map by in-kernel group
+// resolution; the commit that fixed the activation-scale layout; Architecture
+// support: FP32 scales applied in software per scale block).
+//
+// One persistent, warp-specialised launch, grid = #SMs at most:
+//   every CTA reads m_sizes (int64, device memory), checks it (no negative entry,
+//   sum == total_M; otherwise nothing is written and a status is latched) and
+//   prefix-sums it into shared memory; a flat tile id -> (group, 128-row block of
+//   that group, 128-column block).  Empty groups own no tiles; no tile spans two
+//   groups; rows past a group's end are computed but never stored.
+//   warp 0      TMA producer: 128x128 X and W tiles into a 6-stage ring;
+//   warp 1      lane 0 issues kind::f8f6f4 MMAs: each 128-K block goes into a fresh
+//               FP32 partial in tensor memory (two partial slots, so the MMA of block
+//               kb+1 overlaps the fold of block kb);
+//   warps 2-9   fold: acc += sX(row,kb) * sW(g,nblk,kb) * partial in FP32 registers,
+//               then BF16 round-to-nearest-even and masked 16-byte stores.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace bsmma {
+namespace {
+
+constexpr int kBM = 128, kBN = 128, kBK = 128;
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr int kStages = 6;
+constexpr int kTileBytes = 128 * 128;
+constexpr int kStageBytes = 2 * kTileBytes;
+constexpr uint32_t kTmemCols = 256;   // two 128-column partial slots
+constexpr int kMaxG = 64;
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 2048;
+
+struct GroupedParams {
+  const float* sX;
+  const float* sW;
+  __nv_bfloat16* D;
+  const int64_t* m_sizes;
+  int64_t total_M, N;
+  int G, num_n_tiles, num_kb;
+  uint32_t idesc;
+  int* status;
+  uint64_t limit_ns;
+};
+
+struct GroupTable {
+  int64_t start[kMaxG + 1];   // first row of each group
+  int64_t size[kMaxG];
+  int tile_start[kMaxG + 1];  // first 128-row block id of each group
+  int bad;
+};
+
+// Group owning 128-row block `mt` (tile_start is non-decreasing; empty groups own none).
+__device__ __forceinline__ int find_group(const GroupTable& gt, int G, int mt) {
+  int g = 0;
+  for (int i = 1; i < G; ++i)
+    if (gt.tile_start[i] <= mt) g = i;
+  return g;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_fp8_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                       const GroupedParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* p_full = empty + kStages;      // [2]
+  uint64_t* p_empty = p_full + 2;          // [2]
+  uint64_t* drain = p_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  GroupTable& gt = *reinterpret_cast<GroupTable*>(
+      reinterpret_cast<uint8_t*>(full) + 512);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.G;
+  if (threadIdx.x < G) gt.size[threadIdx.x] = p.m_sizes[threadIdx.x];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int64_t row = 0;
+    int tiles = 0, bad = 0;
+    for (int g = 0; g < G; ++g) {
+      const int64_t m = gt.size[g];
+      if (m < 0 || m > p.total_M) bad = 1;
+      gt.start[g] = row;
+      gt.tile_start[g] = tiles;
+      if (!bad) {
+        row += m;
+        tiles += static_cast<int>((m + kBM - 1) / kBM);
+      }
+    }
+    if (row != p.total_M) bad = 1;
+    gt.start[G] = row;
+    gt.tile_start[G] = tiles;
+    gt.bad = bad;
+    if (bad && blockIdx.x == 0) report_status(p.status, kDevBadMSizes);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&p_full[s], 1);
+      mbar_init(&p_empty[s], kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmX);
+    prefetch_tmap(&tmW);
+  }
+  __syncthreads();
+  if (gt.bad) return;   // uniform across the block; nothing allocated, nothing written
+
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int NT = p.num_n_tiles, KB = p.num_kb;
+  const int total_tiles = gt.tile_start[G] * NT;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_parity = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        const int mt = t / NT, nt = t - (t / NT) * NT;
+        const int g = find_group(gt, G, mt);
+        const int row0 = static_cast<int>(gt.start[g] + static_cast<int64_t>(mt - gt.tile_start[g]) * kBM);
+        const int wrow0 = static_cast<int>(static_cast<int64_t>(g) * p.N + static_cast<int64_t>(nt) * kBN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.limit_ns, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          uint8_t* dst = ring + stage * kStageBytes;
+          tma_load_2d(&tmX, &full[stage], dst, kb * kBK, row0);
+          tma_load_2d(&tmW, &full[stage], dst + kTileBytes, kb * kBK, wrow0);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      for (int s = 0; s < kStages; ++s)
+        if (armed & (1u << s)) {
+          volatile int no_abort = 0;
+          mbar_wait(&full[s], (armed_parity >> s) & 1u, p.limit_ns / 4 + 1, &no_abort, nullptr);
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0, pcount = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        for (int kb = 0; kb < KB; ++kb) {
+          const uint32_t slot = pcount & 1;
+          if (!mbar_wait(&full[stage], phase, p.limit_ns, abort_flag, p.status) ||
+              !mbar_wait(&p_empty[slot], ((pcount >> 1) & 1) ^ 1, p.limit_ns, abort_flag,
+                         p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(ring + stage * kStageBytes);
+          const uint32_t b_base = a_base + kTileBytes;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            mma_f8f6f4(tmem + slot * kBN, make_sdesc(a_base + j * 32, 16, 1024, kSwizzle128B),
+                       make_sdesc(b_base + j * 32, 16, 1024, kSwizzle128B), p.idesc, j != 0);
+          tc_commit(&empty[stage]);
+          tc_commit(&p_full[slot]);
+          ++pcount;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      tc_commit(drain);
+      volatile int no_abort = 0;
+      mbar_wait(drain, 0, p.limit_ns, &no_abort, nullptr);
+    }
+  } else {
+    // -------------------------------------------------------------- fold + epilogue
+    const int q = warp & 3;           // tensor-memory lane quarter
+    const int h = (warp - 2) >> 2;    // 64-column half of the tile
+    uint32_t pcount = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+      const int mt = t / NT, nt = t - (t / NT) * NT;
+      const int g = find_group(gt, G, mt);
+      const int64_t m_g = gt.size[g];
+      const int64_t l = static_cast<int64_t>(mt - gt.tile_start[g]) * kBM + q * 32 + lane;
+      const bool valid = l < m_g;
+      const float* sx = p.sX + gt.start[g] * KB + l;   // + kb * m_g
+      const float* sw = p.sW + (static_cast<int64_t>(g) * NT + nt) * KB;
+      float acc[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+      // two blocks of scale prefetch ahead of the fold
+      float sx0 = valid ? __ldg(sx) : 0.f, sw0 = __ldg(sw);
+      float sx1 = (valid && KB > 1) ? __ldg(sx + m_g) : 0.f, sw1 = KB > 1 ? __ldg(sw + 1) : 0.f;
+      for (int kb = 0; kb < KB; ++kb) {
+        float sx2 = 0.f, sw2 = 0.f;
+        if (kb + 2 < KB) {
+          sx2 = valid ? __ldg(sx + (kb + 2) * m_g) : 0.f;
+          sw2 = __ldg(sw + kb + 2);
+        }
+        const uint32_t slot = pcount & 1;
+        if (!mbar_wait(&p_full[slot], (pcount >> 1) & 1, p.limit_ns, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t r0[32], r1[32];
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + slot * kBN + h * 64;
+        tmem_ld32(taddr, r0);
+        tmem_ld32(taddr + 32, r1);
+        tmem_ld_wait(r0);
+        reg_fence(r1);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_empty[slot]);
+        ++pcount;
+        const float s = sx0 * sw0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = fmaf(s, __uint_as_float(r0[i]), acc[i]);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[32 + i] = fmaf(s, __uint_as_float(r1[i]), acc[32 + i]);
+        sx0 = sx1; sw0 = sw1; sx1 = sx2; sw1 = sw2;
+      }
+      if (!ok) break;
+      if (valid) {
+        const int64_t row = gt.start[g] + l;
+        __nv_bfloat16* out = p.D + row * p.N + static_cast<int64_t>(nt) * kBN + h * 64;
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          st_global_v4(out + v * 8, pack_bf16x2(acc[v * 8 + 0], acc[v * 8 + 1]),
+                       pack_bf16x2(acc[v * 8 + 2], acc[v * 8 + 3]),
+                       pack_bf16x2(acc[v * 8 + 4], acc[v * 8 + 5]),
+                       pack_bf16x2(acc[v * 8 + 6], acc[v * 8 + 7]));
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+bsmma_status launch_grouped(const uint8_t* X, const float* sX, const uint8_t* W, const float* sW,
+                            void* D, const int64_t* m_sizes, int64_t total_M, int G, int64_t N,
+                            int64_t K, cudaStream_t stream) {
+  bsmma_status st;
+  const DeviceInfo* dev = current_device(&st);
+  if (!dev) return st;
+  static_assert(sizeof(GroupTable) + 512 <= 2048, "group table fits its shared-memory slot");
+  CUtensorMap tx, tw;
+  // With no rows there is no X tile to load; W's address stands in for the map.
+  st = encode_tmap_u8(&tx, total_M > 0 ? static_cast<const void*>(X) : W, K,
+                      total_M > 0 ? total_M : 1, K, 128, 128);
+  if (st != BSMMA_OK) return st;
+  st = encode_tmap_u8(&tw, W, K, static_cast<uint64_t>(G) * N, K, 128, 128);
+  if (st != BSMMA_OK) return st;
+  GroupedParams p;
+  p.sX = sX;
+  p.sW = sW;
+  p.D = static_cast<__nv_bfloat16*>(D);
+  p.m_sizes = m_sizes;
+  p.total_M = total_M;
+  p.N = N;
+  p.G = G;
+  p.num_n_tiles = static_cast<int>(N / kBN);
+  p.num_kb = static_cast<int>(K / kBK);
+  p.idesc = idesc_f8f6f4(0, 0, 0, 0, kBM, kBN);
+  p.status = dev->status;
+  p.limit_ns = wait_limit_ns();
+  const int64_t bound = ((total_M + kBM - 1) / kBM + G) * p.num_n_tiles;
+  int64_t grid = bound < dev->sm_count ? bound : dev->sm_count;
+  if (grid < 1) grid = 1;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(grouped_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
+      return BSMMA_ERR_CUDA;
+    attr_set = true;
+  }
+  grouped_fp8_kernel<<<static_cast<int>(grid), kThreads, kSmemBytes, stream>>>(tx, tw, p);
+  count_launches(1);
+  return cuda_ok(cudaGetLastError());
+}
+
+}  // namespace bsmma

@@ -1,0 +1,44 @@
+// internal.h -- host-side interfaces shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "bsmma.h"
+
+namespace bsmma {
+
+// Per-device facts the launchers need.
+struct DeviceInfo {
+  int device;
+  int sm_count;
+  int* status;   // device address of the latched device-status word
+};
+
+// Info for the current device (initialised on first use).  Returns nullptr and
+// sets *err on failure.
+const DeviceInfo* current_device(bsmma_status* err);
+
+uint64_t wait_limit_ns();
+void count_launches(int n);
+
+// Encodes a 2-D uint8 tensor map with 128-byte swizzle: `inner` contiguous bytes per
+// row, `outer` rows `row_stride` bytes apart, box of box_inner x box_outer.
+bsmma_status encode_tmap_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                            uint64_t row_stride, uint32_t box_inner, uint32_t box_outer);
+
+// Launchers (arguments already validated by the entry points).
+bsmma_status launch_relayout(const uint8_t* s0, int64_t rows0, int64_t kb0, uint8_t* out0,
+                             const uint8_t* s1, int64_t rows1, int64_t kb1, uint8_t* out1,
+                             cudaStream_t stream);
+bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, const uint8_t* sfb,
+                            void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
+                            bsmma_fmt a_fmt, bsmma_fmt b_fmt, cudaStream_t stream);
+bsmma_status launch_grouped(const uint8_t* X, const float* sX, const uint8_t* W, const float* sW,
+                            void* D, const int64_t* m_sizes, int64_t total_M, int G, int64_t N,
+                            int64_t K, cudaStream_t stream);
+
+inline bsmma_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? BSMMA_OK : BSMMA_ERR_CUDA; }
+
+}  // namespace bsmma

@@ -1,0 +1,166 @@
+/*
+ * bsmma.h -- C ABI of the GB300 (sm_103a) block-scaled GEMM library (libbsmma.so).
+ *
+ * Operations
+ *   D = (A (.) sA) . (B (.) sB)^T, FP32 accumulation, BF16 output, where A and B
+ *   hold FP8 (E4M3 / E5M2) or packed FP4 (E2M1) codes and sA / sB hold one E8M0
+ *   scale per 32 consecutive values along K (MXFP8 / MXFP4).  Source: "PyTorch on
+ *   AMD GPUs gains a FlyDSL backend", Interpretation (FP8 or packed FP4 operands,
+ *   one E8M0 scale per 32 values along the reduction dimension, MXFP8 and MXFP4
+ *   scaled GEMM); "Experimental FlyDSL GEMM backend for TE PyTorch", Supported
+ *   Data Types (MXFP8, mixed E4M3/E5M2) and Validation (TN, NN and NT layouts).
+ *
+ *   The grouped groupwise FP8 GEMM: X E4M3 with one FP32 scale per row per 128-K
+ *   block, W[G][N][K] E4M3 with one FP32 scale per 128x128 block, uneven or empty
+ *   groups, BF16 output.  Source: "Add FlyDSL grouped groupwise FP8 GEMM for
+ *   ROCm", introduction, Testing, and the commit that fixes the activation-scale
+ *   layout (per-group blocks).
+ *
+ * Conventions shared by every entry point
+ *   - Every data pointer is caller-owned DEVICE memory of the current CUDA device;
+ *     D is caller-allocated.  The library never frees or retains caller memory.
+ *   - Matrices are dense and row-major with int64 extents.  Base pointers must be
+ *     16-byte aligned.
+ *   - All work is enqueued on `stream` (the CUDA stream handle, cudaStream_t; NULL
+ *     is the legacy default stream).  No entry point synchronises the stream,
+ *     except bsmma_device_status, bsmma_probe_wait_timeout and the growth of a
+ *     workspace (see mx_gemm).
+ *   - Errors are return codes; nothing is thrown across the ABI.  Argument errors
+ *     are detected on the host before any launch and leave D untouched.  Errors
+ *     detected on the device (a timed-out wait, inconsistent m_sizes) are latched
+ *     in a per-device status word that bsmma_device_status reads and clears.
+ *   - Entry points may be called from several host threads.
+ */
+#ifndef BSMMA_H
+#define BSMMA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                        /* identical to cudaStream_t */
+typedef struct CUstream_st* bsmma_stream;
+
+typedef enum {
+  BSMMA_OK = 0,
+  BSMMA_ERR_INVALID_ARG = 1,   /* bad size, null pointer, bad enum value          */
+  BSMMA_ERR_UNSUPPORTED = 2,   /* valid but unsupported format / layout combination */
+  BSMMA_ERR_MISALIGNED = 3,    /* pointer or row stride violates 16-byte alignment */
+  BSMMA_ERR_WORKSPACE = 4,     /* workspace would have to grow during stream capture */
+  BSMMA_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed               */
+  BSMMA_DEV_TIMEOUT = 6,       /* a device-side wait exceeded its limit           */
+  BSMMA_DEV_BAD_MSIZES = 7     /* m_sizes negative or not summing to total_M      */
+} bsmma_status;
+
+/* Layout letters in row-major operator form: NT D = A . B^T, NN D = A . B,
+ * TN D = A^T . B (the Linear forward, dgrad and wgrad GEMMs). */
+typedef enum { BSMMA_NT = 0, BSMMA_NN = 1, BSMMA_TN = 2 } bsmma_layout;
+
+typedef enum { BSMMA_E4M3 = 0, BSMMA_E5M2 = 1, BSMMA_E2M1 = 2 } bsmma_fmt;
+
+/*
+ * mx_gemm -- dense MXFP8 / MXFP4 GEMM, D[M][N] (BF16) = op(A) . op(B)^T.
+ *
+ *   layout NT: A is [M][K], B is [N][K]   (both K-contiguous)
+ *          NN: A is [M][K], B is [K][N]   (B N-contiguous)
+ *          TN: A is [K][M], B is [K][N]   (both MN-contiguous)
+ *   FP8 codes take one byte each.  E2M1 is packed two per byte along K (even k in
+ *   the low nibble), rows of K/2 bytes, and is supported for NT only and only with
+ *   both operands E2M1; other combinations return BSMMA_ERR_UNSUPPORTED.
+ *   sA is [M][K/32], sB is [N][K/32] E8M0 codes (uint8), always indexed by
+ *   (row of the logical operand op(X), K block), whatever the data layout.
+ *
+ * Preconditions: M, N, K >= 0; K % 32 == 0; row strides of A, B a multiple of 16
+ * bytes (NN/TN: N % 16 == 0, TN: M % 16 == 0); N % 8 == 0 (16-byte rows of D).
+ * M == 0 or N == 0 is a no-op; K == 0 writes D = 0.
+ *
+ * The scales are first rearranged (mx_scale_relayout) into a library-owned
+ * device workspace kept per (device, stream), which grows when needed: growing
+ * synchronises `stream` once, and returns BSMMA_ERR_WORKSPACE if the stream is
+ * being captured (call bsmma_reserve_workspace before capture).  Calls on the
+ * same stream are ordered; calls on different streams use different workspaces.
+ * Two kernel launches per call (relayout, GEMM).
+ */
+bsmma_status mx_gemm(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
+                     void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
+                     bsmma_fmt a_fmt, bsmma_fmt b_fmt, bsmma_stream stream);
+
+/*
+ * mx_gemm_tiled -- mx_gemm with the scales already in the tensor-core atom layout
+ * produced by mx_scale_relayout (sA_tiled for M rows, sB_tiled for N rows, each
+ * of mx_scale_tiled_bytes(rows, K/32) bytes).  Lets callers relayout static
+ * weight scales once.  One kernel launch; allocates nothing.
+ */
+bsmma_status mx_gemm_tiled(const void* A, const uint8_t* sA_tiled, const void* B,
+                           const uint8_t* sB_tiled, void* D, int64_t M, int64_t N, int64_t K,
+                           bsmma_layout layout, bsmma_fmt a_fmt, bsmma_fmt b_fmt,
+                           bsmma_stream stream);
+
+/*
+ * grouped_fp8_gemm -- grouped groupwise FP8 GEMM, one launch.
+ *
+ *   A = X [total_M][K] E4M3 codes, rows of group g are [M_start_g, M_start_g+m_g)
+ *       with M_start_g = m_sizes[0] + ... + m_sizes[g-1].
+ *   sA  FP32 activation scales, one per row per 128-K block, in the per-group block
+ *       layout: group g starts at element M_start_g*(K/128) and holds (local row l,
+ *       block kb) at l + kb*m_g.
+ *   B = W [G][N][K] E4M3 codes;  sB FP32 [G][N/128][K/128] weight scales.
+ *   D [total_M][N] BF16: row r of group g gets
+ *       sum_kb sA(g,l,kb) * sB[g][n/128][kb] * sum_{k in kb} X[r][k] * W[g][n][k].
+ *   m_sizes: int64 [G] in DEVICE memory; the host never reads it (the call is
+ *       capture-safe).  total_M is the row count of X and D.  Empty groups produce
+ *       no work and no writes.  If an entry is negative or the entries do not sum
+ *       to total_M, the kernel writes nothing and latches BSMMA_DEV_BAD_MSIZES.
+ * Preconditions: N % 128 == 0, K % 128 == 0, 1 <= G <= 64, total_M >= 0.
+ */
+bsmma_status grouped_fp8_gemm(const uint8_t* A, const float* sA, const uint8_t* B,
+                              const float* sB, void* D, const int64_t* m_sizes, int64_t total_M,
+                              int G, int64_t N, int64_t K, bsmma_stream stream);
+
+/*
+ * mx_scale_relayout -- rearranges plain E8M0 scales s_plain [rows][kblocks] into the
+ * tensor-core block-scale layout: atoms of 128 rows x 4 K-blocks (512 bytes),
+ * atom (rb, kg) at byte (rb*KG + kg)*512, row r / block k of an atom at byte
+ * (r%32)*16 + (r/32)*4 + k.  Row blocks are padded to RB = 2*ceil(rows/256), block
+ * groups to KG = 2*ceil(kblocks/8); padding holds 127 (the code of 1.0).
+ * s_tiled must hold mx_scale_tiled_bytes(rows, kblocks) bytes.  One launch.
+ */
+bsmma_status mx_scale_relayout(const uint8_t* s_plain, int64_t rows, int64_t kblocks,
+                               uint8_t* s_tiled, bsmma_stream stream);
+
+/* Size in bytes of the tiled scale layout for [rows][kblocks] scales. */
+int64_t mx_scale_tiled_bytes(int64_t rows, int64_t kblocks);
+
+/* Grows the current (device, stream) scale workspace to at least `bytes`
+ * (call before capturing mx_gemm into a CUDA graph). */
+bsmma_status bsmma_reserve_workspace(int64_t bytes, bsmma_stream stream);
+
+/* Synchronises `stream`, then returns and clears the current device's latched
+ * device-side status (BSMMA_OK, BSMMA_DEV_TIMEOUT or BSMMA_DEV_BAD_MSIZES). */
+bsmma_status bsmma_device_status(bsmma_stream stream);
+
+/* Sets the limit of every device-side wait, in nanoseconds (default 2e9). */
+bsmma_status bsmma_set_wait_limit_ns(int64_t ns);
+
+/* Human-readable name of a status code (static storage). */
+const char* bsmma_status_string(bsmma_status status);
+
+/* Number of kernels this library has launched in this process. */
+int64_t bsmma_launch_count(void);
+
+/*
+ * bsmma_probe_wait_timeout -- runs the library's bounded mbarrier wait on a
+ * barrier that nothing ever completes, with a limit of `limit_ns`, and returns the
+ * device status it latches (expected: BSMMA_DEV_TIMEOUT).  Exercises the failure
+ * path of every kernel's waits without faulting or hanging the GPU; the context
+ * stays usable.  Synchronises `stream`.
+ */
+bsmma_status bsmma_probe_wait_timeout(int64_t limit_ns, bsmma_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSMMA_H */

@@ -1,0 +1,122 @@
+"""Dense MXFP8 / MXFP4 GEMM on the GPU against the CPU oracle, element by element,
+within |gpu - oracle| <= 2^-8 |oracle| + 2^-12 max|oracle| (BF16 output rounding
+costs at most 2^-9 relative; the rest covers FP32 accumulation order)."""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_precision_mma_gb300 as bs
+import oracle
+import synthetic
+from tests.gpu_common import assert_close, run_dense, sample_rows, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    bs.build()
+    bs.load()
+    torch.cuda.init()
+
+
+def check(c, rows=None, tiled=False):
+    got = run_dense(c, tiled=tiled)
+    ref = oracle.mx_gemm(c["A"], c["sA"], c["B"], c["sB"], c["M"], c["N"], c["K"], c["layout"],
+                         c["a_fmt"], c["b_fmt"], rows=rows)
+    assert_close(got if rows is None else got[rows], ref,
+                 f'{c["layout"]} {c["a_fmt"]}x{c["b_fmt"]} {c["M"]}x{c["N"]}x{c["K"]}')
+    return got
+
+
+# (M, N, K, layout, a_fmt, b_fmt): several tiles, ragged M/N/K tails, every
+# format pair and layout
+SMALL = [
+    (256, 256, 256, "NT", "e4m3", "e4m3"),       # the 256^3 configuration
+    (200, 264, 96, "NT", "e4m3", "e4m3"),
+    (384, 512, 640, "NT", "e4m3", "e5m2"),
+    (130, 136, 160, "NT", "e5m2", "e5m2"),
+    (136, 264, 32, "NT", "e5m2", "e4m3"),
+    (256, 384, 256, "NN", "e4m3", "e4m3"),
+    (136, 272, 224, "NN", "e4m3", "e5m2"),
+    (272, 400, 192, "TN", "e4m3", "e4m3"),
+    (144, 272, 416, "TN", "e5m2", "e4m3"),
+    (256, 256, 256, "NT", "e2m1", "e2m1"),
+    (200, 264, 96, "NT", "e2m1", "e2m1"),
+    (384, 520, 800, "NT", "e2m1", "e2m1"),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "-".join(map(str, s)))
+def test_dense_small(shape):
+    M, N, K, layout, af, bf = shape
+    check(synthetic.mx_operands((2, SMALL.index(shape)), M, N, K, layout, af, bf))
+
+
+@pytest.mark.parametrize("layout,af", [("NT", "e4m3"), ("NN", "e4m3"), ("TN", "e4m3"),
+                                       ("NT", "e2m1")])
+def test_dense_persistent_many_tiles(layout, af):
+    """More tiles than SMs: every CTA loops over several tiles (accumulator reuse,
+    pipeline phase wrap-around)."""
+    M, N, K = 2176, 4352, 384
+    c = synthetic.mx_operands((2, 500), M, N, K, layout, af, af)
+    check(c, rows=sample_rows(M, 96, 1))
+
+
+def test_tiled_scales_match_plain():
+    c = synthetic.mx_operands((2, 600), 384, 512, 512, "NT", "e4m3", "e4m3")
+    a = run_dense(c)
+    b = run_dense(c, tiled=True)
+    assert np.array_equal(a, b)
+
+
+def test_deterministic():
+    c = synthetic.mx_operands((2, 601), 512, 768, 1024, "NN", "e4m3", "e5m2")
+    assert np.array_equal(run_dense(c), run_dense(c))
+
+
+@pytest.mark.parametrize("lo,hi", [(100, 154), (1, 12), (242, 254)])
+def test_scale_code_range(lo, hi):
+    """Scale codes across the E8M0 range, including 2^-126 and 2^127, with the A and B
+    codes paired so that every product of two scales stays near 1."""
+    c = synthetic.mx_operands((2, 602 + lo), 256, 256, 128, "NT", "e4m3", "e4m3")
+    g = np.random.default_rng([5, lo])
+    c["sA"] = g.integers(lo, hi + 1, size=c["sA"].shape).astype(np.uint8)
+    c["sB"] = g.integers(254 - hi, 254 - lo + 1, size=c["sB"].shape).astype(np.uint8)
+    check(c)
+
+
+def test_k_zero_writes_zeros():
+    A = torch.zeros((128, 0), dtype=torch.uint8, device="cuda")
+    D = torch.full((128, 256), 3.0, dtype=torch.bfloat16, device="cuda")
+    bs.mx_gemm(A, A, A, A, "NT", out=D, M=128, N=256, K=0)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(D).item() == 0
+
+
+# Full-size configurations, sampled output rows against the oracle.
+FULL = [
+    ((4096, 14336, 4096), "NT", "e4m3", "e4m3"),
+    ((4096, 4096, 14336), "NT", "e4m3", "e4m3"),
+    ((8192, 8192, 8192), "NT", "e4m3", "e4m3"),
+    ((8192, 8192, 8192), "NT", "e4m3", "e5m2"),
+    ((8192, 8192, 8192), "NT", "e2m1", "e2m1"),
+    ((1024, 14336, 4096), "NT", "e2m1", "e2m1"),
+]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("shape,layout,af,bf", FULL, ids=lambda v: str(v))
+def test_dense_full_size_sampled(shape, layout, af, bf):
+    M, N, K = shape
+    c = synthetic.mx_operands((2 if af != "e2m1" else 3, 0), M, N, K, layout, af, bf)
+    check(c, rows=sample_rows(M, 24, M + N + K))
+
+
+@pytest.mark.slow
+def test_linear_triple_sampled():
+    """fwd (NT), dgrad (NN), wgrad (TN) of X[8192,4096], W[14336,4096], dY[8192,14336]."""
+    t = synthetic.linear_triple((5, 0))
+    for name in ("fwd", "dgrad", "wgrad"):
+        c = t[name]
+        check(c, rows=sample_rows(c["M"], 16, 7))

@@ -1,0 +1,129 @@
+"""Grouped groupwise FP8 GEMM on the GPU against the CPU oracle.  The group / row /
+column indexing is checked bit-exactly with index probes whose every output is an
+exact BF16 value; random data is checked within |gpu - oracle| <= 2^-8 |oracle| +
+2^-12 max|oracle|."""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_precision_mma_gb300 as bs
+import oracle
+import synthetic
+from tests import _pins
+from tests.gpu_common import assert_close, guarded_out, guards_intact, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    bs.build()
+    bs.load()
+    torch.cuda.init()
+
+
+def run_grouped(c, guard=True):
+    ms = np.asarray(c["m_sizes"], dtype=np.int64)
+    T, N = int(ms.sum()), c["N"]
+    X, sX, W, sW, m = (to_dev(c[k]) for k in ("X", "sX", "W", "sW", "m_sizes"))
+    buf, out = guarded_out(max(T, 1), N)
+    out = out[:T] if T else None
+    D = bs.grouped_fp8_gemm(X, sX, W, sW, m, out=out)
+    torch.cuda.synchronize()
+    st = bs.device_status()
+    assert st == 0, bs.status_string(st)
+    if T:
+        assert guards_intact(buf, T, N), "write outside D"
+    return D.float().cpu().numpy().astype(np.float64)
+
+
+SPLITS = [
+    [3, 0, 300, 1, 0, 129, 2, 5],
+    [260],
+    [0, 0, 0, 7],
+    [1, 0, 127, 129, 0, 2, 64, 11],
+    [128, 128, 0, 256],
+    [0] * 63 + [130],
+]
+
+
+@pytest.mark.parametrize("sizes", SPLITS, ids=lambda s: f"G{len(s)}_T{sum(s)}")
+@pytest.mark.parametrize("kb_hot", [0, 1, 2])
+def test_rowgroup_probe_bit_exact(sizes, kb_hot):
+    c, expect = _pins.probe_rowgroup(sizes, 256, 384, kb_hot)
+    got = run_grouped(c)
+    assert np.array_equal(got, expect)
+
+
+@pytest.mark.parametrize("sizes", SPLITS[:4], ids=lambda s: f"G{len(s)}_T{sum(s)}")
+def test_column_probe_bit_exact(sizes):
+    c, expect = _pins.probe_column(sizes, 1024, 256)
+    assert np.array_equal(run_grouped(c), expect)
+
+
+@pytest.mark.parametrize("sizes", SPLITS, ids=lambda s: f"G{len(s)}_T{sum(s)}")
+def test_grouped_random_small(sizes):
+    ms = np.array(sizes, dtype=np.int64)
+    c = synthetic.grouped_operands((40, len(sizes) + sum(sizes)), ms, 256, 640)
+    got = run_grouped(c)
+    ref = oracle.grouped_fp8_gemm(c["X"], c["sX"], c["W"], c["sW"], ms, 256, 640)
+    assert_close(got, ref, f"grouped {sizes}")
+
+
+def test_grouped_many_tiles():
+    """More tiles than SMs so every CTA loops, with uneven and empty groups."""
+    ms = synthetic.gen_m_sizes(2000, 3)
+    c = synthetic.grouped_operands((40, 77), ms, 1280, 512)
+    got = run_grouped(c)
+    ref = oracle.grouped_fp8_gemm(c["X"], c["sX"], c["W"], c["sW"], ms, 1280, 512)
+    assert_close(got, ref, "grouped many tiles")
+
+
+def test_grouped_deterministic():
+    ms = synthetic.gen_m_sizes(1024, 1)
+    c = synthetic.grouped_operands((40, 78), ms, 512, 768)
+    assert np.array_equal(run_grouped(c), run_grouped(c))
+
+
+def test_grouped_empty_total():
+    c = synthetic.grouped_operands((40, 79), np.zeros(8, dtype=np.int64), 256, 256)
+    got = run_grouped(c)
+    assert got.shape == (0, 256)
+
+
+@pytest.mark.parametrize("bad", [[10, -1, 11, 0], [10, 5, 4, 0], [30, 0, 0, 0]])
+def test_bad_m_sizes_writes_nothing(bad):
+    """Negative sizes or a sum different from total_M: the kernel writes nothing and
+    latches BSMMA_DEV_BAD_MSIZES."""
+    N, K, T = 256, 256, 20
+    g = synthetic.grouped_operands((40, 80), np.array([20, 0, 0, 0]), N, K)
+    X, sX, W, sW = (to_dev(g[k]) for k in ("X", "sX", "W", "sW"))
+    m = torch.tensor(bad, dtype=torch.int64, device="cuda")
+    D = torch.full((T, N), 5.0, dtype=torch.bfloat16, device="cuda")
+    bs.grouped_fp8_gemm(X, sX, W, sW, m, out=D)
+    assert bs.device_status() == 7
+    assert bool((D.float() == 5.0).all())
+
+
+# the nine grouped configurations (G = 8), sampled rows: first and last row of
+# every group plus random rows
+FULL = [(t, n, k) for t in (128, 1024, 16384) for (n, k) in ((2048, 7168), (7168, 2304),
+                                                              (16384, 6656))]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("T,N,K", FULL)
+def test_grouped_full_size_sampled(T, N, K):
+    ms = synthetic.gen_m_sizes(T, FULL.index((T, N, K)))
+    c = synthetic.grouped_operands((4, FULL.index((T, N, K))), ms, N, K)
+    got = run_grouped(c)
+    starts = np.concatenate([[0], np.cumsum(ms)[:-1]])
+    rows = set()
+    for s, m in zip(starts.tolist(), ms.tolist()):
+        if m:
+            rows |= {s, s + m - 1, s + m // 2}
+    rng = np.random.default_rng([9, T, N])
+    rows |= set(rng.integers(0, T, size=16).tolist())
+    rows = np.array(sorted(rows), dtype=np.int64)
+    ref = oracle.grouped_fp8_gemm(c["X"], c["sX"], c["W"], c["sW"], ms, N, K, rows=rows)
+    assert_close(got[rows], ref, f"grouped {T}x{N}x{K}")

@@ -1,0 +1,478 @@
+"""Benchmark of the block-scaled GEMM hot path on GB300.
+
+Default workload (one "step"): the dense MXFP8 NT GEMMs
+    (M,N,K) = (4096,14336,4096), (4096,4096,14336), (8192,8192,8192)  E4M3 x E4M3
+    (M,N,K) = (8192,8192,8192)                                        E4M3 x E5M2
+each one pass of the path: scale relayout of sA and sB, then the tcgen05 GEMM.
+Inputs are seeded N(0,1) values quantised per 32-wide K block (E8M0 scale
+2^(floor(log2 amax) - emax)), resident in HBM before timing.  L2 is flushed (256
+MiB write) before every GEMM, outside the timed events.
+
+Other workloads (``--workload``): mxfp4_dense (8192^3 and 1024x14336x4096),
+grouped_fp8 (G=8, totM 128/1024/16384 x three (N,K)), linear_triple (fwd/dgrad/
+wgrad of X[8192,4096], W[14336,4096], dY[8192,14336]), mxfp8_256 (256^3).
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead
+(on a bounded row sample of the same workload, on the host cores).  Multi-GPU
+runs are independent replicas (no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MX/FP8 GEMM TFLOPS (2MNK/s) and % of GB300 block-scaled tensor peak"
+FALLBACK_BF16_TFLOPS = 1900.0        # used only when MEASURED_PEAKS.json is absent
+NOMINAL_RATIO = {"fp8": 4.5 / 2.25, "fp4": 13.5 / 2.25}
+
+
+# ----------------------------------------------------------------------------- workloads
+def workload_spec(name: str):
+    """List of GEMM descriptions for one step."""
+    if name == "mxfp8_dense":
+        return [dict(kind="dense", M=4096, N=14336, K=4096, layout="NT", a="e4m3", b="e4m3", key=(2, 10)),
+                dict(kind="dense", M=4096, N=4096, K=14336, layout="NT", a="e4m3", b="e4m3", key=(2, 11)),
+                dict(kind="dense", M=8192, N=8192, K=8192, layout="NT", a="e4m3", b="e4m3", key=(2, 12)),
+                dict(kind="dense", M=8192, N=8192, K=8192, layout="NT", a="e4m3", b="e5m2", key=(2, 13))]
+    if name == "mxfp8_256":
+        return [dict(kind="dense", M=256, N=256, K=256, layout="NT", a="e4m3", b="e4m3", key=(1, 0))]
+    if name == "mxfp4_dense":
+        return [dict(kind="dense", M=8192, N=8192, K=8192, layout="NT", a="e2m1", b="e2m1", key=(3, 10)),
+                dict(kind="dense", M=1024, N=14336, K=4096, layout="NT", a="e2m1", b="e2m1", key=(3, 11))]
+    if name == "linear_triple":
+        return [dict(kind="triple", part=p, key=(5, 0)) for p in ("fwd", "dgrad", "wgrad")]
+    if name == "grouped_fp8":
+        out = []
+        for i, (t, n, k) in enumerate((t, n, k) for t in (128, 1024, 16384)
+                                      for (n, k) in ((2048, 7168), (7168, 2304), (16384, 6656))):
+            out.append(dict(kind="grouped", T=t, N=n, K=k, case=i))
+        return out
+    raise SystemExit(f"unknown workload {name}")
+
+
+WORKLOAD_TEXT = {
+    "mxfp8_dense": "MXFP8 dense NT: (4096,14336,4096),(4096,4096,14336),(8192,8192,8192) E4M3xE4M3 "
+                   "+ (8192,8192,8192) E4M3xE5M2; E8M0 per 32 along K; BF16 out",
+    "mxfp8_256": "MXFP8 NT 256^3 E4M3xE4M3",
+    "mxfp4_dense": "MXFP4 dense NT: 8192^3 and (1024,14336,4096), packed E2M1, E8M0 per 32",
+    "linear_triple": "MXFP8 Linear triple: fwd NT (8192,14336,4096), dgrad NN (8192,4096,14336), "
+                     "wgrad TN (14336,4096,8192)",
+    "grouped_fp8": "grouped groupwise FP8, G=8, totM in {128,1024,16384} x (N,K) in "
+                   "{(2048,7168),(7168,2304),(16384,6656)}; seeded uneven m_sizes with 2 empty groups",
+}
+
+
+def flops_of(g) -> float:
+    if g["kind"] == "grouped":
+        return 2.0 * g["T"] * g["N"] * g["K"]
+    return 2.0 * g["M"] * g["N"] * g["K"]
+
+
+def make_inputs(g):
+    """Host numpy operands for one GEMM description."""
+    import synthetic
+    if g["kind"] == "dense":
+        return synthetic.mx_operands(g["key"], g["M"], g["N"], g["K"], g["layout"], g["a"], g["b"])
+    if g["kind"] == "triple":
+        global _TRIPLE
+        if "_TRIPLE" not in globals() or _TRIPLE is None:
+            _TRIPLE = synthetic.linear_triple(g["key"])
+        c = _TRIPLE[g["part"]]
+        g.update(M=c["M"], N=c["N"], K=c["K"])
+        return c
+    ms = synthetic.gen_m_sizes(g["T"], g["case"])
+    return synthetic.grouped_operands((4, g["case"]), ms, g["N"], g["K"])
+
+
+_TRIPLE = None
+
+
+# ----------------------------------------------------------------------------- helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("hbm_gbs", 6800.0)), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group("gloo")
+        return dist
+    return None
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_scaled_precision_mma_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu summary, if
+    it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
+    try:
+        kv = {}
+        for line in open(path):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+        if kv.get("kernel_sources_sha256_16") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import block_scaled_precision_mma_gb300 as bs
+
+    ws, rank, local = dist_env()
+    dist = init_dist(ws)
+    torch.cuda.set_device(local)
+    bs.build()
+    bs.load()
+    dev = torch.device("cuda", local)
+    spec = workload_spec(args.workload)
+
+    gemms = []
+    for g in spec:
+        c = make_inputs(g)
+        if g["kind"] == "grouped":
+            t = {k: torch.from_numpy(np.ascontiguousarray(c[k])).to(dev)
+                 for k in ("X", "sX", "W", "sW", "m_sizes")}
+            t["D"] = torch.empty((g["T"], g["N"]), dtype=torch.bfloat16, device=dev)
+            host = {k: torch.from_numpy(np.ascontiguousarray(c[k])).pin_memory()
+                    for k in ("X", "sX", "W", "sW", "m_sizes")}
+        else:
+            t = {k: torch.from_numpy(np.ascontiguousarray(c[k])).to(dev) for k in ("A", "sA", "B", "sB")}
+            t["D"] = torch.empty((g["M"], g["N"]), dtype=torch.bfloat16, device=dev)
+            t["tA"] = torch.empty(bs.mx_scale_tiled_bytes(g["M"], g["K"] // 32), dtype=torch.uint8, device=dev)
+            t["tB"] = torch.empty(bs.mx_scale_tiled_bytes(g["N"], g["K"] // 32), dtype=torch.uint8, device=dev)
+            host = {k: torch.from_numpy(np.ascontiguousarray(c[k])).pin_memory()
+                    for k in ("A", "sA", "B", "sB")}
+            g.setdefault("layout", c["layout"])
+            g.setdefault("a", c["a_fmt"])
+            g.setdefault("b", c["b_fmt"])
+        host["D"] = torch.empty(t["D"].shape, dtype=torch.bfloat16).pin_memory()
+        gemms.append((g, t, host))
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    step_flops = sum(flops_of(g) for g, _, _ in gemms)
+
+    def one_gemm(g, t, ev):
+        """Relayout (a2) + GEMM (a3-a6); events: [start, after relayout, end]."""
+        ev[0].record(stream)
+        if g["kind"] == "grouped":
+            ev[1].record(stream)
+            bs.grouped_fp8_gemm(t["X"], t["sX"], t["W"], t["sW"], t["m_sizes"], out=t["D"])
+        else:
+            bs.mx_scale_relayout(t["sA"], out=t["tA"])
+            bs.mx_scale_relayout(t["sB"], out=t["tB"])
+            ev[1].record(stream)
+            bs.mx_gemm_tiled(t["A"], t["tA"], t["B"], t["tB"], g["layout"], g["a"], g["b"],
+                             out=t["D"], M=g["M"], N=g["N"], K=g["K"])
+        ev[2].record(stream)
+
+    def step(events):
+        for (g, t, _), ev in zip(gemms, events):
+            flush.zero_()
+            one_gemm(g, t, ev)
+
+    mk = lambda: [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in gemms]
+    for _ in range(args.warmup):
+        step(mk())
+    torch.cuda.synchronize()
+    if bs.device_status() != 0:
+        raise SystemExit("device status error during warm-up")
+    all_events = [mk() for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    n_launch0 = bs.launch_count()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            step(all_events[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    n_launch = bs.launch_count() - n_launch0
+    st = bs.device_status()
+    if st != 0:
+        raise SystemExit(f"device status {bs.status_string(st)}")
+    total_ms = sum(ev[0].elapsed_time(ev[2]) for evs in all_events for ev in evs)
+    gemm_ms = sum(ev[1].elapsed_time(ev[2]) for evs in all_events for ev in evs)
+    per_gemm_ms = [sum(evs[j][1].elapsed_time(evs[j][2]) for evs in all_events) / args.steps
+                   for j in range(len(gemms))]
+
+    # ------------------------------------------------------------- end to end (host buffers)
+    e2e_events = []
+    h2d = sum(sum(v.numel() * v.element_size() for k, v in h.items() if k != "D") for _, _, h in gemms)
+    d2h = sum(h["D"].numel() * h["D"].element_size() for _, _, h in gemms)
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        for g, t, h in gemms:
+            if g["kind"] == "grouped":
+                for k in ("X", "sX", "W", "sW", "m_sizes"):
+                    t[k].copy_(h[k], non_blocking=True)
+                bs.grouped_fp8_gemm(t["X"], t["sX"], t["W"], t["sW"], t["m_sizes"], out=t["D"])
+            else:
+                for k in ("A", "sA", "B", "sB"):
+                    t[k].copy_(h[k], non_blocking=True)
+                bs.mx_gemm(t["A"], t["sA"], t["B"], t["sB"], g["layout"], g["a"], g["b"],
+                           out=t["D"], M=g["M"], N=g["N"], K=g["K"])
+            h["D"].copy_(t["D"], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    ms_per_step = total_ms / args.steps
+    if dist:
+        import torch as _t
+        v = _t.tensor([ms_per_step, gemm_ms / args.steps, e2e_ms], dtype=_t.float64)
+        dist.all_reduce(v, op=dist.ReduceOp.MAX)
+        ms_per_step, gemm_step_ms, e2e_ms = v.tolist()
+    else:
+        gemm_step_ms = gemm_ms / args.steps
+    if rank != 0:
+        return
+
+    bf16_peak, _, peak_src = measured_peaks()
+    is_fp4 = args.workload == "mxfp4_dense"
+    peak = bf16_peak * NOMINAL_RATIO["fp4" if is_fp4 else "fp8"]
+    achieved = step_flops / (gemm_step_ms * 1e-3) / 1e12
+    value = ws * step_flops / (ms_per_step * 1e-3) / 1e12
+    kernel = "grouped_fp8_kernel" if args.workload == "grouped_fp8" else "mx_gemm_kernel"
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOPS",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "mxfp4(e2m1)+e8m0->f32acc" if is_fp4 else "mxfp8(e4m3/e5m2)+e8m0->f32acc",
+        "data": "synthetic (seeded N(0,1), MX-quantised)",
+        "config": {"workload": args.workload + ": " + WORKLOAD_TEXT[args.workload],
+                   "l2": "flushed before every GEMM by a 256 MiB write outside the timed events",
+                   "parallelism": f"replicas x{ws}",
+                   "per_gemm_kernel_ms": [round(x, 4) for x in per_gemm_ms]},
+        "roofline": {"bound": "tensor", "kernel": kernel, "achieved": round(achieved, 1),
+                     "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_src} bf16 dense x nominal "
+                                    f"{'fp4' if is_fp4 else 'fp8'}/bf16 ratio, burst",
+                     "traffic": recorded_traffic(args.workload)},
+        "e2e": {"value": round(ws * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "api": "mx_gemm / grouped_fp8_gemm with host->device copies of every input "
+                       "and device->host copy of D inside the timed region"},
+        "gpu_launches": int(n_launch),
+        "clocks": clk.summary(),
+        "wall_s_timed": round(wall, 3),
+    }
+    if args.workload == "grouped_fp8":
+        line["roofline"]["bound"] = "mixed (HBM for totM<=1024, tensor for 16384)"
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(spec, budget_s=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def time_oracle_sample(spec, rows_per_gemm: int, inputs_cache: dict, nthreads: int):
+    """Runs the oracle on `rows_per_gemm` sampled output rows (all columns) of every
+    GEMM of the step; returns (seconds, flops)."""
+    import oracle
+    secs, flops = 0.0, 0.0
+    for i, g in enumerate(spec):
+        if i not in inputs_cache:
+            inputs_cache[i] = make_inputs(dict(g))
+        c = inputs_cache[i]
+        if g["kind"] == "grouped":
+            T = int(np.asarray(c["m_sizes"]).sum())
+            rows = np.random.default_rng([8, i]).choice(T, size=min(rows_per_gemm, T), replace=False)
+            t0 = time.perf_counter()
+            oracle.grouped_fp8_gemm(c["X"], c["sX"], c["W"], c["sW"], c["m_sizes"], g["N"], g["K"],
+                                    rows=np.sort(rows), nthreads=nthreads)
+            secs += time.perf_counter() - t0
+            flops += 2.0 * len(rows) * g["N"] * g["K"]
+        else:
+            M = c["M"]
+            rows = np.random.default_rng([8, i]).choice(M, size=min(rows_per_gemm, M), replace=False)
+            t0 = time.perf_counter()
+            oracle.mx_gemm(c["A"], c["sA"], c["B"], c["sB"], c["M"], c["N"], c["K"], c["layout"],
+                           c["a_fmt"], c["b_fmt"], rows=np.sort(rows), nthreads=nthreads)
+            secs += time.perf_counter() - t0
+            flops += 2.0 * len(rows) * c["N"] * c["K"]
+    return secs, flops
+
+
+def cpu_baseline(spec, budget_s: float = 15.0):
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    cache = {}
+    s, f = time_oracle_sample(spec, 4, cache, cores)       # calibration
+    rows = int(max(4, min(4096, 4 * budget_s / max(s, 1e-3))))
+    s, f = time_oracle_sample(spec, rows, cache, cores)
+    return {"value": round(f / s / 1e12, 6), "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+            "sample": f"{rows} random output rows x all N columns of each GEMM of the step "
+                      f"({f / 2:.3e} MACs, {s:.1f} s, FP64 table-decode oracle)"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    spec = workload_spec(args.workload)
+    cores = os.cpu_count() or 1
+    cache = {}
+    s, _ = time_oracle_sample(spec, 2, cache, cores)        # calibration + input generation
+    per_step_budget = max(0.2, args.ref_seconds / max(1, args.steps + args.warmup))
+    rows = int(max(1, min(4096, 2 * per_step_budget / max(s, 1e-3))))
+    for _ in range(args.warmup):
+        time_oracle_sample(spec, rows, cache, cores)
+    secs, flops = 0.0, 0.0
+    for _ in range(args.steps):
+        a, b = time_oracle_sample(spec, rows, cache, cores)
+        secs += a
+        flops += b
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOPS",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), MX-quantised)",
+        "config": {"workload": args.workload + ": " + WORKLOAD_TEXT[args.workload],
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {rows} random output rows x all N columns of each GEMM"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mxfp8_dense",
+                    choices=["mxfp8_dense", "mxfp8_256", "mxfp4_dense", "linear_triple", "grouped_fp8"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-seconds", type=float, default=120.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -25,6 +25,7 @@ from .build import LIB_PATH, build
 
 __all__ = ["mx_gemm", "mx_gemm_tiled", "grouped_fp8_gemm", "mx_scale_relayout",
            "mx_scale_tiled_bytes", "device_status", "reserve_workspace", "set_wait_limit_ns",
+           "set_dense_variant",
            "launch_count", "probe_wait_timeout", "status_string", "BsmmaError", "load",
            "LAYOUTS", "FORMATS", "build", "LIB_PATH"]
 
@@ -64,6 +65,7 @@ def load(path: str | None = None):
         lib.bsmma_reserve_workspace.argtypes = [i64, p]
         lib.bsmma_device_status.argtypes = [p]
         lib.bsmma_set_wait_limit_ns.argtypes = [i64]
+        lib.bsmma_set_dense_variant.argtypes = [i32]
         lib.bsmma_status_string.argtypes = [i32]
         lib.bsmma_status_string.restype = ctypes.c_char_p
         lib.bsmma_launch_count.argtypes = []
@@ -71,6 +73,7 @@ def load(path: str | None = None):
         lib.bsmma_probe_wait_timeout.argtypes = [i64, p]
         for name in ("mx_gemm", "mx_gemm_tiled", "grouped_fp8_gemm", "mx_scale_relayout",
                      "bsmma_reserve_workspace", "bsmma_device_status", "bsmma_set_wait_limit_ns",
+                     "bsmma_set_dense_variant",
                      "bsmma_probe_wait_timeout"):
             getattr(lib, name).restype = i32
         _lib = lib
@@ -178,6 +181,11 @@ def device_status(stream=None) -> int:
 
 def set_wait_limit_ns(ns: int):
     _check(load().bsmma_set_wait_limit_ns(int(ns)), "bsmma_set_wait_limit_ns")
+
+
+def set_dense_variant(variant: int):
+    """0 automatic, 1 single-CTA tiles, 2 CTA pairs sharing a multicast B tile."""
+    _check(load().bsmma_set_dense_variant(int(variant)), "bsmma_set_dense_variant")
 
 
 def launch_count() -> int:

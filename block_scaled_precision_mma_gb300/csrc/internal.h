@@ -21,6 +21,7 @@ struct DeviceInfo {
 const DeviceInfo* current_device(bsmma_status* err);
 
 uint64_t wait_limit_ns();
+int dense_variant();   // 0 automatic, 1 single CTAs, 2 CTA pairs
 void count_launches(int n);
 
 // Encodes a 2-D uint8 tensor map with 128-byte swizzle: `inner` contiguous bytes per

@@ -34,6 +34,7 @@ constexpr uint32_t kSfaCol = 256;   // 4 slots x 8 columns
 constexpr uint32_t kSfbCol = 288;   // 4 slots x 16 columns
 constexpr uint32_t kSfSlots = 4;
 constexpr int kSmemLimit = 232448;  // 227 KB of dynamic shared memory per block
+constexpr bool kPairDefault = false;
 
 template <int BN, bool FP4>
 struct Cfg {
@@ -63,11 +64,28 @@ struct DenseParams {
   uint64_t limit_ns;
 };
 
-template <int BN, bool FP4, bool A_MN, bool B_MN>
+// Scheduling unit u -> output tile (mt, nt).  Single CTAs take one tile per unit;
+// a CTA pair (2-CTA cluster) takes two vertically adjacent tiles that share their
+// B tile, which each CTA loads half of and multicasts to both.
+template <bool PAIR>
+__device__ __forceinline__ void unit_tile(const DenseParams& p, int u, uint32_t rank, int& mt,
+                                          int& nt) {
+  if (PAIR) {
+    const int nmp = (p.num_m_tiles + 1) >> 1;
+    nt = u / nmp;
+    mt = (u - nt * nmp) * 2 + static_cast<int>(rank);
+  } else {
+    nt = u / p.num_m_tiles;
+    mt = u - nt * p.num_m_tiles;
+  }
+}
+
+template <int BN, bool FP4, bool A_MN, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const DenseParams p) {
   using C = Cfg<BN, FP4>;
+  static_assert(!PAIR || BN == 256, "a CTA pair splits a 256-wide B tile");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -84,10 +102,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  constexpr uint16_t kPairMask = 3;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], PAIR ? 2 : 1);   // a pair frees a stage only when both MMAs are done
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, kEpiWarps);
@@ -103,9 +123,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();   // the peer's barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total_tiles = p.num_m_tiles * p.num_n_tiles;
+  const int total_units = PAIR ? ((p.num_m_tiles + 1) >> 1) * p.num_n_tiles
+                               : p.num_m_tiles * p.num_n_tiles;
+  const int first_unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int unit_stride = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -113,8 +137,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_parity = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-        const int mt = t % p.num_m_tiles, nt = t / p.num_m_tiles;
+      for (int u = first_unit; ok && u < total_units; u += unit_stride) {
+        int mt, nt;
+        unit_tile<PAIR>(p, u, rank, mt, nt);
         for (int ks = 0; ks < p.num_k_stages; ++ks) {
           if (!mbar_wait(&empty[stage], phase ^ 1, p.limit_ns, abort_flag, p.status)) {
             ok = false;
@@ -127,22 +152,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* b_dst = sB + stage * C::kBBytes;
           if (A_MN) tma_load_2d(&tmA, &full[stage], a_dst, mt * kBM, ks * 128);
           else      tma_load_2d(&tmA, &full[stage], a_dst, ks * 128, mt * kBM);
-          if (B_MN) {
-#pragma unroll
-            for (int j = 0; j < BN / 128; ++j)
-              tma_load_2d(&tmB, &full[stage], b_dst + j * 16384, nt * BN + j * 128, ks * 128);
-          } else {
-            tma_load_2d(&tmB, &full[stage], b_dst, ks * 128, nt * BN);
-          }
           bulk_load(sSFA + stage * C::kSfaBytes,
                     p.sfa + (static_cast<int64_t>(mt) * p.sfa_kg + ks * C::kAP) * 512,
                     C::kSfaBytes, &full[stage]);
+          if (PAIR) {
+            // this CTA's 128-row half of the B tile and of its scales, to both CTAs
+            const int r = static_cast<int>(rank);
+            if (B_MN)
+              tma_load_2d_mc(&tmB, &full[stage], b_dst + r * 16384, nt * BN + r * 128, ks * 128,
+                             kPairMask);
+            else
+              tma_load_2d_mc(&tmB, &full[stage], b_dst + r * 16384, ks * 128, nt * BN + r * 128,
+                             kPairMask);
+            bulk_load_mc(sSFB + stage * C::kSfbBytes + r * C::kAP * 512,
+                         p.sfb + ((static_cast<int64_t>(nt) * 2 + r) * p.sfb_kg + ks * C::kAP) * 512,
+                         C::kAP * 512, &full[stage], kPairMask);
+          } else {
+            if (B_MN) {
 #pragma unroll
-          for (int rb = 0; rb < BN / 128; ++rb)
-            bulk_load(sSFB + stage * C::kSfbBytes + rb * C::kAP * 512,
-                      p.sfb + ((static_cast<int64_t>(nt) * (BN / 128) + rb) * p.sfb_kg +
-                               ks * C::kAP) * 512,
-                      C::kAP * 512, &full[stage]);
+              for (int j = 0; j < BN / 128; ++j)
+                tma_load_2d(&tmB, &full[stage], b_dst + j * 16384, nt * BN + j * 128, ks * 128);
+            } else {
+              tma_load_2d(&tmB, &full[stage], b_dst, ks * 128, nt * BN);
+            }
+#pragma unroll
+            for (int rb = 0; rb < BN / 128; ++rb)
+              bulk_load(sSFB + stage * C::kSfbBytes + rb * C::kAP * 512,
+                        p.sfb + ((static_cast<int64_t>(nt) * (BN / 128) + rb) * p.sfb_kg +
+                                 ks * C::kAP) * 512,
+                        C::kAP * 512, &full[stage]);
+          }
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1;
@@ -163,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, kiter = 0;
       bool ok = true;
       int local = 0;
-      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++local) {
+      for (int u = first_unit; ok && u < total_units; u += unit_stride, ++local) {
         if (!mbar_wait(acc_empty, (local & 1) ^ 1, p.limit_ns, abort_flag, p.status)) break;
         tc_fence_after();
         for (int ks = 0; ks < p.num_k_stages; ++ks) {
@@ -202,7 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_mxf8f6f4(tmem, ad, bd, p.idesc | idesc_sf_id(j, j), sfa_t, sfb_t, acc);
             }
           }
-          tc_commit(&empty[stage]);
+          if (PAIR) tc_commit_mc(&empty[stage], kPairMask);
+          else tc_commit(&empty[stage]);
           ++kiter;
           if (++stage == C::kStages) {
             stage = 0;
@@ -223,8 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;                // tensor-memory lane quarter of this warp
     const int h = (warp - 2) >> 2;         // which half of the tile's columns
     int local = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++local) {
-      const int mt = t % p.num_m_tiles, nt = t / p.num_m_tiles;
+    for (int u = first_unit; u < total_units; u += unit_stride, ++local) {
+      int mt, nt;
+      unit_tile<PAIR>(p, u, rank, mt, nt);
       if (!mbar_wait(acc_full, local & 1, p.limit_ns, abort_flag, p.status)) break;
       tc_fence_after();
       uint32_t r[kChunks][32];
@@ -262,23 +303,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // neither CTA of a pair leaves while its peer may still signal its barriers
+  if (PAIR) cluster_sync();
 }
 
-template <int BN, bool FP4, bool A_MN, bool B_MN>
+template <int BN, bool FP4, bool A_MN, bool B_MN, bool PAIR>
 bsmma_status launch_dense(const CUtensorMap& ta, const CUtensorMap& tb, const DenseParams& p,
-                          int grid, cudaStream_t stream) {
+                          int sm_count, cudaStream_t stream) {
   using C = Cfg<BN, FP4>;
-  auto kern = mx_gemm_kernel<BN, FP4, A_MN, B_MN>;
-  static bool attr_set = false;   // benign race: setting the attribute twice is harmless
-  if (!attr_set) {
+  auto kern = mx_gemm_kernel<BN, FP4, A_MN, B_MN, PAIR>;
+  static int max_clusters = -1;   // benign race: every thread computes the same value
+  if (max_clusters < 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
       return BSMMA_ERR_CUDA;
-    attr_set = true;
+    int n = sm_count;
+    if (PAIR) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) !=
+          cudaSuccess)
+        return BSMMA_ERR_CUDA;
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2 * sm_count, 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = C::kSmemBytes;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1)
+        return BSMMA_ERR_CUDA;
+    }
+    max_clusters = n;
   }
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(ta, tb, p);
+  const int64_t units = PAIR ? static_cast<int64_t>((p.num_m_tiles + 1) / 2) * p.num_n_tiles
+                             : static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
+  const int64_t slots = PAIR ? max_clusters : sm_count;   // co-resident CTAs (pairs)
+  const int grid = static_cast<int>((units < slots ? units : slots) * (PAIR ? 2 : 1));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = PAIR ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
   count_launches(1);
-  return cuda_ok(cudaGetLastError());
+  return cuda_ok(e == cudaSuccess ? cudaGetLastError() : e);
+}
+
+// Which dense variant runs (see bsmma_set_dense_variant): CTA pairs or single CTAs.
+bool use_pair(int num_m_tiles) {
+  const int v = dense_variant();
+  if (v == 1) return false;
+  if (v == 2) return num_m_tiles >= 1;
+  return kPairDefault && num_m_tiles >= 2;
 }
 
 }  // namespace
@@ -298,8 +384,10 @@ bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, co
   else
     st = encode_tmap_u8(&ta, A, kbytes, M, kbytes, 128, 128);
   if (st != BSMMA_OK) return st;
+  const int num_m_tiles = static_cast<int>((M + kBM - 1) / kBM);
+  const bool pair = use_pair(num_m_tiles);
   if (layout == BSMMA_NT)
-    st = encode_tmap_u8(&tb, B, kbytes, N, kbytes, 128, BN);
+    st = encode_tmap_u8(&tb, B, kbytes, N, kbytes, 128, pair ? 128 : BN);
   else
     st = encode_tmap_u8(&tb, B, N, K, N, 128, 128);
   if (st != BSMMA_OK) return st;
@@ -312,7 +400,7 @@ bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, co
   p.N = N;
   p.sfa_kg = 2 * ((K / 32 + 7) / 8);   // block groups per row block of the tiled layout
   p.sfb_kg = p.sfa_kg;
-  p.num_m_tiles = static_cast<int>((M + kBM - 1) / kBM);
+  p.num_m_tiles = num_m_tiles;
   p.num_n_tiles = static_cast<int>((N + BN - 1) / BN);
   p.num_k_stages = static_cast<int>((static_cast<int64_t>(kbytes) + 127) / 128);
   const uint32_t af = fp4 ? 1u : static_cast<uint32_t>(a_fmt);   // kind::mxf4 codes E2M1 as 1
@@ -320,13 +408,20 @@ bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, co
   p.idesc = idesc_block_scaled(af, bf, layout == BSMMA_TN, layout != BSMMA_NT, kBM, BN);
   p.status = dev->status;
   p.limit_ns = wait_limit_ns();
-  const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
-  const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
-  if (fp4) return launch_dense<BN, true, false, false>(ta, tb, p, grid, stream);
+  const int sms = dev->sm_count;
+  if (pair) {
+    if (fp4) return launch_dense<BN, true, false, false, true>(ta, tb, p, sms, stream);
+    switch (layout) {
+      case BSMMA_NT: return launch_dense<BN, false, false, false, true>(ta, tb, p, sms, stream);
+      case BSMMA_NN: return launch_dense<BN, false, false, true, true>(ta, tb, p, sms, stream);
+      default:       return launch_dense<BN, false, true, true, true>(ta, tb, p, sms, stream);
+    }
+  }
+  if (fp4) return launch_dense<BN, true, false, false, false>(ta, tb, p, sms, stream);
   switch (layout) {
-    case BSMMA_NT: return launch_dense<BN, false, false, false>(ta, tb, p, grid, stream);
-    case BSMMA_NN: return launch_dense<BN, false, false, true>(ta, tb, p, grid, stream);
-    default:       return launch_dense<BN, false, true, true>(ta, tb, p, grid, stream);
+    case BSMMA_NT: return launch_dense<BN, false, false, false, false>(ta, tb, p, sms, stream);
+    case BSMMA_NN: return launch_dense<BN, false, false, true, false>(ta, tb, p, sms, stream);
+    default:       return launch_dense<BN, false, true, true, false>(ta, tb, p, sms, stream);
   }
 }
 

@@ -144,6 +144,12 @@ bsmma_status bsmma_device_status(bsmma_stream stream);
 /* Sets the limit of every device-side wait, in nanoseconds (default 2e9). */
 bsmma_status bsmma_set_wait_limit_ns(int64_t ns);
 
+/* Selects the dense kernel variant for later mx_gemm / mx_gemm_tiled calls:
+ * 0 automatic (default), 1 one CTA per 128x256 tile, 2 CTA pairs (2-CTA clusters
+ * computing two vertically adjacent tiles that share one multicast B tile).  All
+ * variants compute the same result; this is a tuning and testing control. */
+bsmma_status bsmma_set_dense_variant(int variant);
+
 /* Human-readable name of a status code (static storage). */
 const char* bsmma_status_string(bsmma_status status);
 

@@ -20,6 +20,14 @@ def _lib():
     torch.cuda.init()
 
 
+@pytest.fixture(params=[1, 2], ids=["single", "pair"])
+def variant(request):
+    """Runs the test with one-CTA tiles and with CTA pairs sharing a multicast B tile."""
+    bs.set_dense_variant(request.param)
+    yield request.param
+    bs.set_dense_variant(0)
+
+
 def check(c, rows=None, tiled=False):
     got = run_dense(c, tiled=tiled)
     ref = oracle.mx_gemm(c["A"], c["sA"], c["B"], c["sB"], c["M"], c["N"], c["K"], c["layout"],
@@ -48,14 +56,14 @@ SMALL = [
 
 
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: "-".join(map(str, s)))
-def test_dense_small(shape):
+def test_dense_small(shape, variant):
     M, N, K, layout, af, bf = shape
     check(synthetic.mx_operands((2, SMALL.index(shape)), M, N, K, layout, af, bf))
 
 
 @pytest.mark.parametrize("layout,af", [("NT", "e4m3"), ("NN", "e4m3"), ("TN", "e4m3"),
                                        ("NT", "e2m1")])
-def test_dense_persistent_many_tiles(layout, af):
+def test_dense_persistent_many_tiles(layout, af, variant):
     """More tiles than SMs: every CTA loops over several tiles (accumulator reuse,
     pipeline phase wrap-around)."""
     M, N, K = 2176, 4352, 384
@@ -107,14 +115,14 @@ FULL = [
 
 @pytest.mark.slow
 @pytest.mark.parametrize("shape,layout,af,bf", FULL, ids=lambda v: str(v))
-def test_dense_full_size_sampled(shape, layout, af, bf):
+def test_dense_full_size_sampled(shape, layout, af, bf, variant):
     M, N, K = shape
     c = synthetic.mx_operands((2 if af != "e2m1" else 3, 0), M, N, K, layout, af, bf)
     check(c, rows=sample_rows(M, 24, M + N + K))
 
 
 @pytest.mark.slow
-def test_linear_triple_sampled():
+def test_linear_triple_sampled(variant):
     """fwd (NT), dgrad (NN), wgrad (TN) of X[8192,4096], W[14336,4096], dY[8192,14336]."""
     t = synthetic.linear_triple((5, 0))
     for name in ("fwd", "dgrad", "wgrad"):

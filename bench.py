@@ -181,6 +181,16 @@ def init_dist(ws):
     return None
 
 
+def reduce_max(values, dist):
+    """Element-wise max over ranks (gloo all-reduce on CPU); identity for one process."""
+    if dist is None:
+        return list(values)
+    import torch
+    v = torch.tensor(list(values), dtype=torch.float64)
+    dist.all_reduce(v, op=dist.ReduceOp.MAX)
+    return v.tolist()
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_scaled_precision_mma_gb300", "csrc")
@@ -322,14 +332,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
-    ms_per_step = total_ms / args.steps
-    if dist:
-        import torch as _t
-        v = _t.tensor([ms_per_step, gemm_ms / args.steps, e2e_ms], dtype=_t.float64)
-        dist.all_reduce(v, op=dist.ReduceOp.MAX)
-        ms_per_step, gemm_step_ms, e2e_ms = v.tolist()
-    else:
-        gemm_step_ms = gemm_ms / args.steps
+    ms_per_step, gemm_step_ms, e2e_ms = reduce_max(
+        [total_ms / args.steps, gemm_ms / args.steps, e2e_ms], dist)
     if rank != 0:
         return
 

@@ -227,6 +227,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     bs.build()
     bs.load()
+    bs.set_dense_variant(args.dense_variant)
     dev = torch.device("cuda", local)
     spec = workload_spec(args.workload)
 
@@ -319,7 +320,10 @@ def run_ours(args):
                            out=t["D"], M=g["M"], N=g["N"], K=g["K"])
             h["D"].copy_(t["D"], non_blocking=True)
 
-    e2e_step()
+    if args.no_e2e:
+        e2e_steps = 0
+    else:
+        e2e_step()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -330,7 +334,7 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps if e2e_steps else float("nan")
 
     ms_per_step, gemm_step_ms, e2e_ms = reduce_max(
         [total_ms / args.steps, gemm_ms / args.steps, e2e_ms], dist)
@@ -359,16 +363,18 @@ def run_ours(args):
         "config": {"workload": args.workload + ": " + WORKLOAD_TEXT[args.workload],
                    "l2": "flushed before every GEMM by a 256 MiB write outside the timed events",
                    "parallelism": f"replicas x{ws}",
+                   "dense_variant": args.dense_variant,
                    "per_gemm_kernel_ms": [round(x, 4) for x in per_gemm_ms]},
         "roofline": {"bound": "tensor", "kernel": kernel, "achieved": round(achieved, 1),
                      "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_src} bf16 dense x nominal "
                                     f"{'fp4' if is_fp4 else 'fp8'}/bf16 ratio, burst",
                      "traffic": recorded_traffic(args.workload)},
-        "e2e": {"value": round(ws * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "api": "mx_gemm / grouped_fp8_gemm with host->device copies of every input "
-                       "and device->host copy of D inside the timed region"},
+        "e2e": None if args.no_e2e else {
+            "value": round(ws * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "api": "mx_gemm / grouped_fp8_gemm with host->device copies of every input "
+                   "and device->host copy of D inside the timed region"},
         "gpu_launches": int(n_launch),
         "clocks": clk.summary(),
         "wall_s_timed": round(wall, 3),
@@ -467,6 +473,9 @@ def main():
     ap.add_argument("--workload", default="mxfp8_dense",
                     choices=["mxfp8_dense", "mxfp8_256", "mxfp4_dense", "linear_triple", "grouped_fp8"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
+    ap.add_argument("--dense-variant", type=int, default=0, choices=[0, 1, 2],
+                    help="0 automatic, 1 single-CTA tiles, 2 CTA pairs (tuning only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     args = ap.parse_args()

@@ -25,7 +25,7 @@ from .build import LIB_PATH, build
 
 __all__ = ["mx_gemm", "mx_gemm_tiled", "grouped_fp8_gemm", "mx_scale_relayout",
            "mx_scale_tiled_bytes", "device_status", "reserve_workspace", "set_wait_limit_ns",
-           "set_dense_variant",
+           "set_dense_variant", "set_grouped_tile_width",
            "launch_count", "probe_wait_timeout", "status_string", "BsmmaError", "load",
            "LAYOUTS", "FORMATS", "build", "LIB_PATH"]
 
@@ -66,6 +66,7 @@ def load(path: str | None = None):
         lib.bsmma_device_status.argtypes = [p]
         lib.bsmma_set_wait_limit_ns.argtypes = [i64]
         lib.bsmma_set_dense_variant.argtypes = [i32]
+        lib.bsmma_set_grouped_tile_width.argtypes = [i32]
         lib.bsmma_status_string.argtypes = [i32]
         lib.bsmma_status_string.restype = ctypes.c_char_p
         lib.bsmma_launch_count.argtypes = []
@@ -73,7 +74,7 @@ def load(path: str | None = None):
         lib.bsmma_probe_wait_timeout.argtypes = [i64, p]
         for name in ("mx_gemm", "mx_gemm_tiled", "grouped_fp8_gemm", "mx_scale_relayout",
                      "bsmma_reserve_workspace", "bsmma_device_status", "bsmma_set_wait_limit_ns",
-                     "bsmma_set_dense_variant",
+                     "bsmma_set_dense_variant", "bsmma_set_grouped_tile_width",
                      "bsmma_probe_wait_timeout"):
             getattr(lib, name).restype = i32
         _lib = lib
@@ -186,6 +187,11 @@ def set_wait_limit_ns(ns: int):
 def set_dense_variant(variant: int):
     """0 automatic, 1 single-CTA tiles, 2 CTA pairs sharing a multicast B tile."""
     _check(load().bsmma_set_dense_variant(int(variant)), "bsmma_set_dense_variant")
+
+
+def set_grouped_tile_width(width: int):
+    """0 automatic, 128 or 256 columns per grouped tile."""
+    _check(load().bsmma_set_grouped_tile_width(int(width)), "bsmma_set_grouped_tile_width")
 
 
 def launch_count() -> int:

@@ -29,15 +29,23 @@
 namespace bsmma {
 namespace {
 
-constexpr int kBM = 128, kBN = 128, kBK = 128;
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
-constexpr int kStages = 6;
-constexpr int kTileBytes = 128 * 128;
-constexpr int kStageBytes = 2 * kTileBytes;
-constexpr uint32_t kTmemCols = 256;   // two 128-column partial slots
+constexpr int kBM = 128, kBK = 128;
 constexpr int kMaxG = 64;
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 2048;
+constexpr int kATileBytes = kBM * kBK;
+
+// Tile 128 x BN; each of the 8 fold warps owns one 32-lane quarter x BN/2 columns.
+template <int BN>
+struct GCfg {
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kCols = BN / 2;        // accumulator columns per fold warp
+  static constexpr int kThreads = (2 + kEpiWarps) * 32;
+  static constexpr int kBTileBytes = BN * kBK;
+  static constexpr int kStageBytes = kATileBytes + kBTileBytes;
+  static constexpr int kStages = BN == 128 ? 6 : 4;
+  static constexpr uint32_t kTmemCols = 2 * BN;   // two partial slots
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 2048;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
 
 struct GroupedParams {
   const float* sX;
@@ -66,9 +74,13 @@ __device__ __forceinline__ int find_group(const GroupTable& gt, int G, int mt) {
   return g;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN>
+__global__ void __maxnreg__(200)
     grouped_fp8_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                        const GroupedParams p) {
+  using C = GCfg<BN>;
+  constexpr int kStages = C::kStages, kStageBytes = C::kStageBytes, kEpiWarps = C::kEpiWarps;
+  constexpr uint32_t kTmemCols = C::kTmemCols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -143,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mt = t / NT, nt = t - (t / NT) * NT;
         const int g = find_group(gt, G, mt);
         const int row0 = static_cast<int>(gt.start[g] + static_cast<int64_t>(mt - gt.tile_start[g]) * kBM);
-        const int wrow0 = static_cast<int>(static_cast<int64_t>(g) * p.N + static_cast<int64_t>(nt) * kBN);
+        const int wrow0 = static_cast<int>(static_cast<int64_t>(g) * p.N + static_cast<int64_t>(nt) * BN);
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, p.limit_ns, abort_flag, p.status)) {
             ok = false;
@@ -154,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           uint8_t* dst = ring + stage * kStageBytes;
           tma_load_2d(&tmX, &full[stage], dst, kb * kBK, row0);
-          tma_load_2d(&tmW, &full[stage], dst + kTileBytes, kb * kBK, wrow0);
+          tma_load_2d(&tmW, &full[stage], dst + kATileBytes, kb * kBK, wrow0);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
@@ -184,10 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t a_base = smem_u32(ring + stage * kStageBytes);
-          const uint32_t b_base = a_base + kTileBytes;
+          const uint32_t b_base = a_base + kATileBytes;
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            mma_f8f6f4(tmem + slot * kBN, make_sdesc(a_base + j * 32, 16, 1024, kSwizzle128B),
+            mma_f8f6f4(tmem + slot * BN, make_sdesc(a_base + j * 32, 16, 1024, kSwizzle128B),
                        make_sdesc(b_base + j * 32, 16, 1024, kSwizzle128B), p.idesc, j != 0);
           tc_commit(&empty[stage]);
           tc_commit(&p_full[slot]);
@@ -204,8 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- fold + epilogue
+    constexpr int kCols = C::kCols;
     const int q = warp & 3;           // tensor-memory lane quarter
-    const int h = (warp - 2) >> 2;    // 64-column half of the tile
+    const int h = (warp - 2) >> 2;    // which half of the tile's columns
     uint32_t pcount = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
@@ -215,18 +228,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t l = static_cast<int64_t>(mt - gt.tile_start[g]) * kBM + q * 32 + lane;
       const bool valid = l < m_g;
       const float* sx = p.sX + gt.start[g] * KB + l;   // + kb * m_g
-      const float* sw = p.sW + (static_cast<int64_t>(g) * NT + nt) * KB;
-      float acc[64];
+      // weight scales of the 128-column block(s) of this warp's columns
+      const float* sw = p.sW + (static_cast<int64_t>(g) * (p.N / 128) +
+                                static_cast<int64_t>(nt) * (BN / 128)) * KB;
+      constexpr int kSwPerWarp = kCols >= 128 ? kCols / 128 : 1;   // 128-col blocks per warp
+      const int sw_blk0 = (h * kCols) / 128;
+      float acc[kCols];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) acc[i] = 0.f;
-      // two blocks of scale prefetch ahead of the fold
-      float sx0 = valid ? __ldg(sx) : 0.f, sw0 = __ldg(sw);
-      float sx1 = (valid && KB > 1) ? __ldg(sx + m_g) : 0.f, sw1 = KB > 1 ? __ldg(sw + 1) : 0.f;
+      for (int i = 0; i < kCols; ++i) acc[i] = 0.f;
+      // scales for block kb are loaded one block ahead of their use
+      float sx_next = valid ? __ldg(sx) : 0.f;
+      float sw_next[kSwPerWarp];
+#pragma unroll
+      for (int b = 0; b < kSwPerWarp; ++b) sw_next[b] = __ldg(sw + (sw_blk0 + b) * KB);
       for (int kb = 0; kb < KB; ++kb) {
-        float sx2 = 0.f, sw2 = 0.f;
-        if (kb + 2 < KB) {
-          sx2 = valid ? __ldg(sx + (kb + 2) * m_g) : 0.f;
-          sw2 = __ldg(sw + kb + 2);
+        const float sx_cur = sx_next;
+        float sw_cur[kSwPerWarp];
+#pragma unroll
+        for (int b = 0; b < kSwPerWarp; ++b) sw_cur[b] = sw_next[b];
+        if (kb + 1 < KB) {
+          sx_next = valid ? __ldg(sx + (kb + 1) * m_g) : 0.f;
+#pragma unroll
+          for (int b = 0; b < kSwPerWarp; ++b) sw_next[b] = __ldg(sw + (sw_blk0 + b) * KB + kb + 1);
         }
         const uint32_t slot = pcount & 1;
         if (!mbar_wait(&p_full[slot], (pcount >> 1) & 1, p.limit_ns, abort_flag, p.status)) {
@@ -234,29 +257,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        uint32_t r0[32], r1[32];
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + slot * kBN + h * 64;
-        tmem_ld32(taddr, r0);
-        tmem_ld32(taddr + 32, r1);
-        tmem_ld_wait(r0);
-        reg_fence(r1);
+        const uint32_t taddr =
+            tmem + (static_cast<uint32_t>(q * 32) << 16) + slot * BN + h * kCols;
+#pragma unroll
+        for (int c = 0; c < kCols / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c * 32, r);
+          tmem_ld_wait(r);
+          const float s = sx_cur * sw_cur[(c * 32) / 128];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(s, __uint_as_float(r[i]), acc[c * 32 + i]);
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_empty[slot]);
         ++pcount;
-        const float s = sx0 * sw0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = fmaf(s, __uint_as_float(r0[i]), acc[i]);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[32 + i] = fmaf(s, __uint_as_float(r1[i]), acc[32 + i]);
-        sx0 = sx1; sw0 = sw1; sx1 = sx2; sw1 = sw2;
       }
       if (!ok) break;
       if (valid) {
         const int64_t row = gt.start[g] + l;
-        __nv_bfloat16* out = p.D + row * p.N + static_cast<int64_t>(nt) * kBN + h * 64;
+        __nv_bfloat16* out = p.D + row * p.N + static_cast<int64_t>(nt) * BN + h * kCols;
 #pragma unroll
-        for (int v = 0; v < 8; ++v)
+        for (int v = 0; v < kCols / 8; ++v)
           st_global_v4(out + v * 8, pack_bf16x2(acc[v * 8 + 0], acc[v * 8 + 1]),
                        pack_bf16x2(acc[v * 8 + 2], acc[v * 8 + 3]),
                        pack_bf16x2(acc[v * 8 + 4], acc[v * 8 + 5]),
@@ -272,6 +294,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+template <int BN>
+bsmma_status launch_grouped_bn(const CUtensorMap& tx, const CUtensorMap& tw, GroupedParams p,
+                               int64_t total_M, int G, int sm_count, cudaStream_t stream) {
+  using C = GCfg<BN>;
+  p.num_n_tiles = static_cast<int>(p.N / BN);
+  p.idesc = idesc_f8f6f4(0, 0, 0, 0, kBM, BN);
+  const int64_t bound = ((total_M + kBM - 1) / kBM + G) * p.num_n_tiles;
+  int64_t grid = bound < sm_count ? bound : sm_count;
+  if (grid < 1) grid = 1;
+  static bool attr_set = false;   // benign race: setting the attribute twice is harmless
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(grouped_fp8_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
+      return BSMMA_ERR_CUDA;
+    attr_set = true;
+  }
+  grouped_fp8_kernel<BN><<<static_cast<int>(grid), C::kThreads, C::kSmemBytes, stream>>>(tx, tw, p);
+  count_launches(1);
+  return cuda_ok(cudaGetLastError());
+}
+
 }  // namespace
 
 bsmma_status launch_grouped(const uint8_t* X, const float* sX, const uint8_t* W, const float* sW,
@@ -281,12 +324,19 @@ bsmma_status launch_grouped(const uint8_t* X, const float* sX, const uint8_t* W,
   const DeviceInfo* dev = current_device(&st);
   if (!dev) return st;
   static_assert(sizeof(GroupTable) + 512 <= 2048, "group table fits its shared-memory slot");
+  // Wide tiles halve the W traffic per flop when there are enough rows to fill the
+  // GPU with them; narrow tiles keep every SM streaming W when rows are few.
+  const bool wide = (N % 256 == 0) &&
+                    ((total_M + kBM - 1) / kBM) * (N / 256) >= 2 * static_cast<int64_t>(dev->sm_count) &&
+                    grouped_tile_width() != 128;
+  const bool force_wide = grouped_tile_width() == 256 && N % 256 == 0;
+  const int bn = (wide || force_wide) ? 256 : 128;
   CUtensorMap tx, tw;
   // With no rows there is no X tile to load; W's address stands in for the map.
   st = encode_tmap_u8(&tx, total_M > 0 ? static_cast<const void*>(X) : W, K,
                       total_M > 0 ? total_M : 1, K, 128, 128);
   if (st != BSMMA_OK) return st;
-  st = encode_tmap_u8(&tw, W, K, static_cast<uint64_t>(G) * N, K, 128, 128);
+  st = encode_tmap_u8(&tw, W, K, static_cast<uint64_t>(G) * N, K, 128, bn);
   if (st != BSMMA_OK) return st;
   GroupedParams p;
   p.sX = sX;
@@ -296,24 +346,11 @@ bsmma_status launch_grouped(const uint8_t* X, const float* sX, const uint8_t* W,
   p.total_M = total_M;
   p.N = N;
   p.G = G;
-  p.num_n_tiles = static_cast<int>(N / kBN);
   p.num_kb = static_cast<int>(K / kBK);
-  p.idesc = idesc_f8f6f4(0, 0, 0, 0, kBM, kBN);
   p.status = dev->status;
   p.limit_ns = wait_limit_ns();
-  const int64_t bound = ((total_M + kBM - 1) / kBM + G) * p.num_n_tiles;
-  int64_t grid = bound < dev->sm_count ? bound : dev->sm_count;
-  if (grid < 1) grid = 1;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(grouped_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
-      return BSMMA_ERR_CUDA;
-    attr_set = true;
-  }
-  grouped_fp8_kernel<<<static_cast<int>(grid), kThreads, kSmemBytes, stream>>>(tx, tw, p);
-  count_launches(1);
-  return cuda_ok(cudaGetLastError());
+  if (bn == 256) return launch_grouped_bn<256>(tx, tw, p, total_M, G, dev->sm_count, stream);
+  return launch_grouped_bn<128>(tx, tw, p, total_M, G, dev->sm_count, stream);
 }
 
 }  // namespace bsmma

@@ -22,6 +22,7 @@ const DeviceInfo* current_device(bsmma_status* err);
 
 uint64_t wait_limit_ns();
 int dense_variant();   // 0 automatic, 1 single CTAs, 2 CTA pairs
+int grouped_tile_width();   // 0 automatic, 128 or 256
 void count_launches(int n);
 
 // Encodes a 2-D uint8 tensor map with 128-byte swizzle: `inner` contiguous bytes per

@@ -150,6 +150,12 @@ bsmma_status bsmma_set_wait_limit_ns(int64_t ns);
  * variants compute the same result; this is a tuning and testing control. */
 bsmma_status bsmma_set_dense_variant(int variant);
 
+/* Selects the grouped kernel's tile width for later grouped_fp8_gemm calls: 0
+ * automatic (default: 256 when the wide tiles fill the GPU at least twice and N %
+ * 256 == 0, else 128), 128 or 256 (used only when N % 256 == 0).  Same result;
+ * a tuning and testing control. */
+bsmma_status bsmma_set_grouped_tile_width(int width);
+
 /* Human-readable name of a status code (static storage). */
 const char* bsmma_status_string(bsmma_status status);
 

@@ -22,6 +22,14 @@ def _lib():
     torch.cuda.init()
 
 
+@pytest.fixture(params=[128, 256], ids=["bn128", "bn256"])
+def gwidth(request):
+    """Runs the test with 128- and 256-column grouped tiles."""
+    bs.set_grouped_tile_width(request.param)
+    yield request.param
+    bs.set_grouped_tile_width(0)
+
+
 def run_grouped(c, guard=True):
     ms = np.asarray(c["m_sizes"], dtype=np.int64)
     T, N = int(ms.sum()), c["N"]
@@ -49,20 +57,20 @@ SPLITS = [
 
 @pytest.mark.parametrize("sizes", SPLITS, ids=lambda s: f"G{len(s)}_T{sum(s)}")
 @pytest.mark.parametrize("kb_hot", [0, 1, 2])
-def test_rowgroup_probe_bit_exact(sizes, kb_hot):
+def test_rowgroup_probe_bit_exact(sizes, kb_hot, gwidth):
     c, expect = _pins.probe_rowgroup(sizes, 256, 384, kb_hot)
     got = run_grouped(c)
     assert np.array_equal(got, expect)
 
 
 @pytest.mark.parametrize("sizes", SPLITS[:4], ids=lambda s: f"G{len(s)}_T{sum(s)}")
-def test_column_probe_bit_exact(sizes):
+def test_column_probe_bit_exact(sizes, gwidth):
     c, expect = _pins.probe_column(sizes, 1024, 256)
     assert np.array_equal(run_grouped(c), expect)
 
 
 @pytest.mark.parametrize("sizes", SPLITS, ids=lambda s: f"G{len(s)}_T{sum(s)}")
-def test_grouped_random_small(sizes):
+def test_grouped_random_small(sizes, gwidth):
     ms = np.array(sizes, dtype=np.int64)
     c = synthetic.grouped_operands((40, len(sizes) + sum(sizes)), ms, 256, 640)
     got = run_grouped(c)
@@ -70,12 +78,12 @@ def test_grouped_random_small(sizes):
     assert_close(got, ref, f"grouped {sizes}")
 
 
-def test_grouped_many_tiles():
+def test_grouped_many_tiles(gwidth):
     """More tiles than SMs so every CTA loops, with uneven and empty groups."""
     ms = synthetic.gen_m_sizes(2000, 3)
-    c = synthetic.grouped_operands((40, 77), ms, 1280, 512)
+    c = synthetic.grouped_operands((40, 77), ms, 1536, 512)
     got = run_grouped(c)
-    ref = oracle.grouped_fp8_gemm(c["X"], c["sX"], c["W"], c["sW"], ms, 1280, 512)
+    ref = oracle.grouped_fp8_gemm(c["X"], c["sX"], c["W"], c["sW"], ms, 1536, 512)
     assert_close(got, ref, "grouped many tiles")
 
 
@@ -113,7 +121,7 @@ FULL = [(t, n, k) for t in (128, 1024, 16384) for (n, k) in ((2048, 7168), (7168
 
 @pytest.mark.slow
 @pytest.mark.parametrize("T,N,K", FULL)
-def test_grouped_full_size_sampled(T, N, K):
+def test_grouped_full_size_sampled(T, N, K, gwidth):
     ms = synthetic.gen_m_sizes(T, FULL.index((T, N, K)))
     c = synthetic.grouped_operands((4, FULL.index((T, N, K))), ms, N, K)
     got = run_grouped(c)

@@ -74,8 +74,10 @@ __device__ __forceinline__ int find_group(const GroupTable& gt, int G, int mt) {
   return g;
 }
 
+// 10 warps share an SM's four register-file quarters (16384 registers each) as
+// 3+3+2+2 warps, so a thread may hold at most 16384 / (3 * 32) = 170 registers.
 template <int BN>
-__global__ void __maxnreg__(200)
+__global__ void __maxnreg__(168)
     grouped_fp8_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                        const GroupedParams p) {
   using C = GCfg<BN>;
@@ -260,13 +262,13 @@ __global__ void __maxnreg__(200)
         const uint32_t taddr =
             tmem + (static_cast<uint32_t>(q * 32) << 16) + slot * BN + h * kCols;
 #pragma unroll
-        for (int c = 0; c < kCols / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(taddr + c * 32, r);
-          tmem_ld_wait(r);
-          const float s = sx_cur * sw_cur[(c * 32) / 128];
+        for (int c = 0; c < kCols / 16; ++c) {
+          uint32_t r[16];
+          tmem_ld16(taddr + c * 16, r);
+          tmem_ld_wait16(r);
+          const float s = sx_cur * sw_cur[(c * 16) / 128];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(s, __uint_as_float(r[i]), acc[c * 32 + i]);
+          for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(s, __uint_as_float(r[i]), acc[c * 16 + i]);
         }
         tc_fence_before();
         __syncwarp();

@@ -34,7 +34,7 @@ constexpr uint32_t kSfaCol = 256;   // 4 slots x 8 columns
 constexpr uint32_t kSfbCol = 288;   // 4 slots x 16 columns
 constexpr uint32_t kSfSlots = 4;
 constexpr int kSmemLimit = 232448;  // 227 KB of dynamic shared memory per block
-constexpr bool kPairDefault = false;
+constexpr bool kPairDefault = true;
 
 template <int BN, bool FP4>
 struct Cfg {
@@ -66,22 +66,30 @@ struct DenseParams {
 
 // Scheduling unit u -> output tile (mt, nt).  Single CTAs take one tile per unit;
 // a CTA pair (2-CTA cluster) takes two vertically adjacent tiles that share their
-// B tile, which each CTA loads half of and multicasts to both.
+// B tile, which each CTA loads half of and multicasts to both.  Units walk the
+// output in bands of kBandRows tile rows, along N inside a band, so that the CTAs
+// running at the same time touch a compact block of A and B that stays in L2.
+constexpr int kBandRows = 16;
+
 template <bool PAIR>
 __device__ __forceinline__ void unit_tile(const DenseParams& p, int u, uint32_t rank, int& mt,
                                           int& nt) {
-  if (PAIR) {
-    const int nmp = (p.num_m_tiles + 1) >> 1;
-    nt = u / nmp;
-    mt = (u - nt * nmp) * 2 + static_cast<int>(rank);
-  } else {
-    nt = u / p.num_m_tiles;
-    mt = u - nt * p.num_m_tiles;
-  }
+  const int rows = PAIR ? (p.num_m_tiles + 1) >> 1 : p.num_m_tiles;   // unit rows
+  const int band = PAIR ? kBandRows / 2 : kBandRows;
+  const int per_band = band * p.num_n_tiles;
+  const int b = u / per_band;
+  const int r0 = b * band;
+  const int h = rows - r0 < band ? rows - r0 : band;
+  const int v = u - b * per_band;
+  const int ur = r0 + v % h;
+  nt = v / h;
+  mt = PAIR ? ur * 2 + static_cast<int>(rank) : ur;
 }
 
+// 10 warps share an SM's four register-file quarters (16384 registers each) as
+// 3+3+2+2 warps, so a thread may hold at most 16384 / (3 * 32) = 170 registers.
 template <int BN, bool FP4, bool A_MN, bool B_MN, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(168)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const DenseParams p) {
   using C = Cfg<BN, FP4>;
@@ -288,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int v = 0; v < 4; ++v) {
             const int o = c * 32 + v * 8;
             if (col0 + o < p.N)
-              st_global_v4(out + o,
+              st_global_v4_cs(out + o,
                            pack_bf16x2(__uint_as_float(r[c][v * 8 + 0]), __uint_as_float(r[c][v * 8 + 1])),
                            pack_bf16x2(__uint_as_float(r[c][v * 8 + 2]), __uint_as_float(r[c][v * 8 + 3])),
                            pack_bf16x2(__uint_as_float(r[c][v * 8 + 4]), __uint_as_float(r[c][v * 8 + 5])),

@@ -23,7 +23,7 @@ import torch
 
 from .build import LIB_PATH, build
 
-__all__ = ["mx_gemm", "mx_gemm_tiled", "grouped_fp8_gemm", "mx_scale_relayout",
+__all__ = ["mx_gemm", "mx_gemm_tiled", "mx_gemm_noalloc", "grouped_fp8_gemm", "mx_scale_relayout",
            "mx_scale_tiled_bytes", "device_status", "reserve_workspace", "set_wait_limit_ns",
            "set_dense_variant", "set_grouped_tile_width",
            "launch_count", "probe_wait_timeout", "status_string", "BsmmaError", "load",
@@ -32,7 +32,8 @@ __all__ = ["mx_gemm", "mx_gemm_tiled", "grouped_fp8_gemm", "mx_scale_relayout",
 LAYOUTS = {"NT": 0, "NN": 1, "TN": 2}
 FORMATS = {"e4m3": 0, "e5m2": 1, "e2m1": 2}
 STATUS = ["BSMMA_OK", "BSMMA_ERR_INVALID_ARG", "BSMMA_ERR_UNSUPPORTED", "BSMMA_ERR_MISALIGNED",
-          "BSMMA_ERR_WORKSPACE", "BSMMA_ERR_CUDA", "BSMMA_DEV_TIMEOUT", "BSMMA_DEV_BAD_MSIZES"]
+          "BSMMA_ERR_WORKSPACE", "BSMMA_ERR_CUDA", "BSMMA_DEV_TIMEOUT", "BSMMA_DEV_BAD_MSIZES",
+          "BSMMA_ERR_SCRATCH_LIMIT"]
 
 _lib = None
 _lock = threading.Lock()
@@ -58,6 +59,7 @@ def load(path: str | None = None):
         p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         lib.mx_gemm.argtypes = [p, p, p, p, p, i64, i64, i64, i32, i32, i32, p]
         lib.mx_gemm_tiled.argtypes = [p, p, p, p, p, i64, i64, i64, i32, i32, i32, p]
+        lib.mx_gemm_noalloc.argtypes = [p, p, p, p, p, i64, i64, i64, i32, i32, i32, p]
         lib.grouped_fp8_gemm.argtypes = [p, p, p, p, p, p, i64, i32, i64, i64, p]
         lib.mx_scale_relayout.argtypes = [p, i64, i64, p, p]
         lib.mx_scale_tiled_bytes.argtypes = [i64, i64]
@@ -72,7 +74,8 @@ def load(path: str | None = None):
         lib.bsmma_launch_count.argtypes = []
         lib.bsmma_launch_count.restype = i64
         lib.bsmma_probe_wait_timeout.argtypes = [i64, p]
-        for name in ("mx_gemm", "mx_gemm_tiled", "grouped_fp8_gemm", "mx_scale_relayout",
+        for name in ("mx_gemm", "mx_gemm_tiled", "mx_gemm_noalloc", "grouped_fp8_gemm",
+                     "mx_scale_relayout",
                      "bsmma_reserve_workspace", "bsmma_device_status", "bsmma_set_wait_limit_ns",
                      "bsmma_set_dense_variant", "bsmma_set_grouped_tile_width",
                      "bsmma_probe_wait_timeout"):
@@ -127,6 +130,20 @@ def mx_gemm(A, sA, B, sB, layout="NT", a_fmt="e4m3", b_fmt="e4m3", out=None, M=N
     _check(fn(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(out), M, N, K, LAYOUTS[layout],
               FORMATS[a_fmt], FORMATS[b_fmt], _stream(stream)),
            "mx_gemm_tiled" if tiled else "mx_gemm")
+    return out
+
+
+def mx_gemm_noalloc(A, sA, B, sB, layout="NT", a_fmt="e4m3", b_fmt="e4m3", out=None, M=None,
+                    N=None, K=None, stream=None):
+    """``mx_gemm`` without any device allocation (scales go to the library's fixed
+    16 MiB array; see ``mx_gemm_noalloc`` in bsmma.h).  ``out`` must be given."""
+    if out is None:
+        raise ValueError("mx_gemm_noalloc allocates nothing: pass out=")
+    if M is None or N is None or K is None:
+        raise ValueError("mx_gemm_noalloc: pass M, N and K")
+    _check(load().mx_gemm_noalloc(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(out), M, N, K,
+                                  LAYOUTS[layout], FORMATS[a_fmt], FORMATS[b_fmt],
+                                  _stream(stream)), "mx_gemm_noalloc")
     return out
 
 

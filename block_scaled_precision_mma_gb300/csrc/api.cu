@@ -123,32 +123,6 @@ __global__ void wait_probe_kernel(int* status, uint64_t limit_ns) {
 constexpr int64_t kMaxTmaDim = (int64_t(1) << 32) - 1;
 constexpr int64_t kMaxStride = (int64_t(1) << 40) - 16;
 
-bsmma_status validate_dense(const void* A, const void* sA, const void* B, const void* sB,
-                            const void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
-                            bsmma_fmt a_fmt, bsmma_fmt b_fmt) {
-  if (M < 0 || N < 0 || K < 0 || K % 32 != 0) return BSMMA_ERR_INVALID_ARG;
-  if (layout < BSMMA_NT || layout > BSMMA_TN) return BSMMA_ERR_INVALID_ARG;
-  if (a_fmt < BSMMA_E4M3 || a_fmt > BSMMA_E2M1 || b_fmt < BSMMA_E4M3 || b_fmt > BSMMA_E2M1)
-    return BSMMA_ERR_INVALID_ARG;
-  const bool fp4a = a_fmt == BSMMA_E2M1, fp4b = b_fmt == BSMMA_E2M1;
-  if (fp4a != fp4b) return BSMMA_ERR_UNSUPPORTED;
-  if (fp4a && layout != BSMMA_NT) return BSMMA_ERR_UNSUPPORTED;
-  if (M == 0 || N == 0) return BSMMA_OK;
-  if (!D) return BSMMA_ERR_INVALID_ARG;
-  if (N % 8 != 0 || !aligned16(D)) return BSMMA_ERR_MISALIGNED;
-  if (K == 0) return BSMMA_OK;
-  if (!A || !B || !sA || !sB) return BSMMA_ERR_INVALID_ARG;
-  if (!aligned16(A) || !aligned16(B) || !aligned16(sA) || !aligned16(sB))
-    return BSMMA_ERR_MISALIGNED;
-  if (layout != BSMMA_NT && N % 16 != 0) return BSMMA_ERR_MISALIGNED;
-  if (layout == BSMMA_TN && M % 16 != 0) return BSMMA_ERR_MISALIGNED;
-  if (M > kMaxTmaDim || N > kMaxTmaDim || K > kMaxTmaDim) return BSMMA_ERR_INVALID_ARG;
-  if (M > kMaxStride || N > kMaxStride || K > kMaxStride) return BSMMA_ERR_INVALID_ARG;
-  // tile ids are 32-bit
-  if ((M + 127) / 128 * ((N + 255) / 256) > INT32_MAX / 2) return BSMMA_ERR_INVALID_ARG;
-  return BSMMA_OK;
-}
-
 // Workspace of at least `bytes` for (current device, stream).
 bsmma_status get_workspace(int64_t bytes, cudaStream_t stream, void** out) {
   int dev = 0;
@@ -186,6 +160,33 @@ bsmma_status get_workspace(int64_t bytes, cudaStream_t stream, void** out) {
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
+
+bsmma_status validate_dense(const void* A, const void* sA, const void* B, const void* sB,
+                            const void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
+                            bsmma_fmt a_fmt, bsmma_fmt b_fmt) {
+  if (M < 0 || N < 0 || K < 0 || K % 32 != 0) return BSMMA_ERR_INVALID_ARG;
+  if (layout < BSMMA_NT || layout > BSMMA_TN) return BSMMA_ERR_INVALID_ARG;
+  if (a_fmt < BSMMA_E4M3 || a_fmt > BSMMA_E2M1 || b_fmt < BSMMA_E4M3 || b_fmt > BSMMA_E2M1)
+    return BSMMA_ERR_INVALID_ARG;
+  const bool fp4a = a_fmt == BSMMA_E2M1, fp4b = b_fmt == BSMMA_E2M1;
+  if (fp4a != fp4b) return BSMMA_ERR_UNSUPPORTED;
+  if (fp4a && layout != BSMMA_NT) return BSMMA_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return BSMMA_OK;
+  if (!D) return BSMMA_ERR_INVALID_ARG;
+  if (N % 8 != 0 || !aligned16(D)) return BSMMA_ERR_MISALIGNED;
+  if (K == 0) return BSMMA_OK;
+  if (!A || !B || !sA || !sB) return BSMMA_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(sA) || !aligned16(sB))
+    return BSMMA_ERR_MISALIGNED;
+  if (layout != BSMMA_NT && N % 16 != 0) return BSMMA_ERR_MISALIGNED;
+  if (layout == BSMMA_TN && M % 16 != 0) return BSMMA_ERR_MISALIGNED;
+  if (M > kMaxTmaDim || N > kMaxTmaDim || K > kMaxTmaDim) return BSMMA_ERR_INVALID_ARG;
+  if (M > kMaxStride || N > kMaxStride || K > kMaxStride) return BSMMA_ERR_INVALID_ARG;
+  // tile ids are 32-bit
+  if ((M + 127) / 128 * ((N + 255) / 256) > INT32_MAX / 2) return BSMMA_ERR_INVALID_ARG;
+  return BSMMA_OK;
+}
+
 }  // namespace bsmma
 
 using namespace bsmma;
@@ -292,6 +293,7 @@ bsmma_status bsmma_set_grouped_tile_width(int width) {
 
 const char* bsmma_status_string(bsmma_status s) {
   switch (s) {
+    case BSMMA_ERR_SCRATCH_LIMIT: return "BSMMA_ERR_SCRATCH_LIMIT";
     case BSMMA_OK: return "BSMMA_OK";
     case BSMMA_ERR_INVALID_ARG: return "BSMMA_ERR_INVALID_ARG";
     case BSMMA_ERR_UNSUPPORTED: return "BSMMA_ERR_UNSUPPORTED";

@@ -30,6 +30,11 @@ void count_launches(int n);
 bsmma_status encode_tmap_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                             uint64_t row_stride, uint32_t box_inner, uint32_t box_outer);
 
+// Host-side argument checks shared by the dense entry points.
+bsmma_status validate_dense(const void* A, const void* sA, const void* B, const void* sB,
+                            const void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
+                            bsmma_fmt a_fmt, bsmma_fmt b_fmt);
+
 // Launchers (arguments already validated by the entry points).
 bsmma_status launch_relayout(const uint8_t* s0, int64_t rows0, int64_t kb0, uint8_t* out0,
                              const uint8_t* s1, int64_t rows1, int64_t kb1, uint8_t* out1,

@@ -51,7 +51,8 @@ typedef enum {
   BSMMA_ERR_WORKSPACE = 4,     /* workspace would have to grow during stream capture */
   BSMMA_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed               */
   BSMMA_DEV_TIMEOUT = 6,       /* a device-side wait exceeded its limit           */
-  BSMMA_DEV_BAD_MSIZES = 7     /* m_sizes negative or not summing to total_M      */
+  BSMMA_DEV_BAD_MSIZES = 7,    /* m_sizes negative or not summing to total_M      */
+  BSMMA_ERR_SCRATCH_LIMIT = 8  /* problem too large for mx_gemm_noalloc's fixed scratch */
 } bsmma_status;
 
 /* Layout letters in row-major operator form: NT D = A . B^T, NN D = A . B,
@@ -97,6 +98,34 @@ bsmma_status mx_gemm_tiled(const void* A, const uint8_t* sA_tiled, const void* B
                            const uint8_t* sB_tiled, void* D, int64_t M, int64_t N, int64_t K,
                            bsmma_layout layout, bsmma_fmt a_fmt, bsmma_fmt b_fmt,
                            bsmma_stream stream);
+
+/*
+ * mx_gemm_noalloc -- mx_gemm for callers that cannot allocate device memory.
+ *
+ * (The source pages have no counterpart; this entry point exists for callers of
+ * this library.)  mx_gemm may call cudaMalloc the first time a stream needs a
+ * bigger scale workspace.  Some callers cannot allow that: code being captured
+ * into a CUDA graph, code that must stay within a framework's own memory pool or a
+ * fixed memory budget, and code on a path that must not synchronise (cudaMalloc
+ * and cudaFree can).  mx_gemm_noalloc computes exactly what mx_gemm computes, with
+ * the same arguments, preconditions and two launches, but rearranges the scales
+ * into a fixed array of BSMMA_NOALLOC_SCRATCH_BYTES (16 MiB) in device memory that
+ * belongs to the library; every GPU that loads the library holds that array until
+ * the process exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Limit: mx_scale_tiled_bytes(M, K/32) rounded up to 256, plus
+ * mx_scale_tiled_bytes(N, K/32), must not exceed BSMMA_NOALLOC_SCRATCH_BYTES;
+ * larger problems return BSMMA_ERR_SCRATCH_LIMIT before any launch.
+ * The first call on a device looks up the array's device address on that device
+ * (cudaGetSymbolAddress) and caches it; make that first call before any stream
+ * capture.  All calls on a device share the one array and overwrite it completely,
+ * so calls that can overlap on the GPU (different streams without ordering between
+ * them) race with each other; order them on one stream.
+ */
+#define BSMMA_NOALLOC_SCRATCH_BYTES (16ll << 20)
+bsmma_status mx_gemm_noalloc(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
+                             void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
+                             bsmma_fmt a_fmt, bsmma_fmt b_fmt, bsmma_stream stream);
 
 /*
  * grouped_fp8_gemm -- grouped groupwise FP8 GEMM, one launch.

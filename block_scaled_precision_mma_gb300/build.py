@@ -11,7 +11,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libbsmma.so")
-SOURCES = ["api.cu", "relayout.cu", "mx_gemm.cu", "grouped_gemm.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "relayout.cu", "mx_gemm.cu", "grouped_gemm.cu", "noalloc.cu",
+           "mx_gemm_2sm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 

@@ -105,6 +105,31 @@ bsmma_status encode_tmap_u8(CUtensorMap* map, const void* base, uint64_t inner, 
   return r == CUDA_SUCCESS ? BSMMA_OK : BSMMA_ERR_INVALID_ARG;
 }
 
+bsmma_status encode_tmap_words(CUtensorMap* map, const void* base, uint64_t inner,
+                               uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return BSMMA_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+  }
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 4};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BSMMA_OK : BSMMA_ERR_INVALID_ARG;
+}
+
 namespace {
 
 __global__ void wait_probe_kernel(int* status, uint64_t limit_ns) {
@@ -226,6 +251,17 @@ bsmma_status mx_gemm(const void* A, const uint8_t* sA, const void* B, const uint
   if (st != BSMMA_OK || M == 0 || N == 0) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (K == 0) return cuda_ok(cudaMemsetAsync(D, 0, static_cast<size_t>(M * N * 2), s));
+  if (dense_variant() >= 3) {
+    const int64_t wa = align_up(wide_scale_bytes(M, K / 32, 0), 256);
+    const int64_t wb = wide_scale_bytes(N, K / 32, 1);
+    void* w = nullptr;
+    st = get_workspace(wa + wb, s, &w);
+    if (st != BSMMA_OK) return st;
+    uint8_t* ta = static_cast<uint8_t*>(w);
+    st = launch_wide_relayout(sA, M, ta, sB, N, ta + wa, K / 32, s);
+    if (st != BSMMA_OK) return st;
+    return launch_mx_gemm_2sm(A, ta, B, ta + wa, D, M, N, K, layout, a_fmt, b_fmt, s);
+  }
   const int64_t bytes_a = align_up(mx_scale_tiled_bytes(M, K / 32), 256);
   const int64_t bytes_b = mx_scale_tiled_bytes(N, K / 32);
   void* ws = nullptr;
@@ -280,7 +316,7 @@ bsmma_status bsmma_set_wait_limit_ns(int64_t ns) {
 }
 
 bsmma_status bsmma_set_dense_variant(int variant) {
-  if (variant < 0 || variant > 2) return BSMMA_ERR_INVALID_ARG;
+  if (variant < 0 || variant > 4) return BSMMA_ERR_INVALID_ARG;
   g_dense_variant = variant;
   return BSMMA_OK;
 }

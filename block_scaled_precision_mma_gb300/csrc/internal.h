@@ -21,7 +21,7 @@ struct DeviceInfo {
 const DeviceInfo* current_device(bsmma_status* err);
 
 uint64_t wait_limit_ns();
-int dense_variant();   // 0 automatic, 1 single CTAs, 2 CTA pairs
+int dense_variant();   // 0 automatic, 1 single CTAs, 2 CTA pairs, 3 SM-pair MMAs
 int grouped_tile_width();   // 0 automatic, 128 or 256
 void count_launches(int n);
 
@@ -35,6 +35,17 @@ bsmma_status validate_dense(const void* A, const void* sA, const void* B, const 
                             const void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
                             bsmma_fmt a_fmt, bsmma_fmt b_fmt);
 
+// Encodes a 2-D tensor map of 32-bit words without swizzle: `inner` words per row,
+// `outer` rows, box of box_inner x box_outer words.
+bsmma_status encode_tmap_words(CUtensorMap* map, const void* base, uint64_t inner,
+                               uint64_t outer, uint32_t box_inner, uint32_t box_outer);
+
+// Wide scale layouts of the SM-pair kernel (role 0 row scales, role 1 column scales).
+int64_t wide_scale_bytes(int64_t rows, int64_t kblocks, int role);
+bsmma_status launch_wide_relayout(const uint8_t* sa, int64_t rows_a, uint8_t* out_a,
+                                  const uint8_t* sb, int64_t rows_b, uint8_t* out_b,
+                                  int64_t kblocks, cudaStream_t stream);
+
 // Launchers (arguments already validated by the entry points).
 bsmma_status launch_relayout(const uint8_t* s0, int64_t rows0, int64_t kb0, uint8_t* out0,
                              const uint8_t* s1, int64_t rows1, int64_t kb1, uint8_t* out1,
@@ -42,6 +53,10 @@ bsmma_status launch_relayout(const uint8_t* s0, int64_t rows0, int64_t kb0, uint
 bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, const uint8_t* sfb,
                             void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
                             bsmma_fmt a_fmt, bsmma_fmt b_fmt, cudaStream_t stream);
+bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B,
+                                const uint8_t* sfb, void* D, int64_t M, int64_t N, int64_t K,
+                                bsmma_layout layout, bsmma_fmt a_fmt, bsmma_fmt b_fmt,
+                                cudaStream_t stream);
 bsmma_status launch_grouped(const uint8_t* X, const float* sX, const uint8_t* W, const float* sW,
                             void* D, const int64_t* m_sizes, int64_t total_M, int G, int64_t N,
                             int64_t K, cudaStream_t stream);

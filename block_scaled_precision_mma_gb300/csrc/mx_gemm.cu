@@ -380,6 +380,7 @@ bool use_pair(int num_m_tiles) {
 bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, const uint8_t* sfb,
                             void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
                             bsmma_fmt a_fmt, bsmma_fmt b_fmt, cudaStream_t stream) {
+  if (dense_variant() >= 3) return BSMMA_ERR_UNSUPPORTED;   // takes the wide scale layouts
   bsmma_status st;
   const DeviceInfo* dev = current_device(&st);
   if (!dev) return st;

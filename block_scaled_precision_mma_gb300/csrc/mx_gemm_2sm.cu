@@ -1,0 +1,472 @@
+// mx_gemm_2sm.cu -- dense block-scaled GEMM on SM pairs (tcgen05 cta_group::2).
+//
+// Same operation as mx_gemm.cu (D = op(A) . op(B)^T with E8M0 block scales; "PyTorch
+// on AMD GPUs gains a FlyDSL backend", Interpretation), computed by 2-CTA clusters:
+// one MMA instruction covers a 256 x 256 output tile spread over the two SMs of a
+// pair.  Each CTA holds its own 128 rows of A and its own 128 rows of B in shared
+// memory, so per SM the operand bytes per flop are two thirds of the single-CTA
+// 128 x 256 tile, and six stages fit where four did.
+//
+//   both CTAs, warp 0   TMA producer: its A half, its B half and the scale atoms of
+//                       its A rows and of all 256 B rows, completing bytes on the
+//                       leader CTA's stage barrier;
+//   leader,    warp 1   lane 0 copies the scales into both CTAs' tensor memory and
+//                       issues the pair MMAs; commits release the stage in both CTAs;
+//   both CTAs, warps 2-9  epilogue of the CTA's 128 accumulator rows, then an arrive on
+//                       the leader's accumulator barrier.
+// Every wait is bounded; on a timeout each role unwinds to the common teardown.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace bsmma {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfaCol = 256;   // 2 slots x 8 columns: row-scale chunks
+constexpr uint32_t kSfbCol = 288;   // 4 slots x 8 columns: column-scale blocks
+constexpr int kSmemLimit = 232448;
+constexpr int kBandUnits = 8;       // unit rows (256 output rows each) per raster band
+
+// REPL: copies of a column-scale block in the copy's source (4 = one per lane quarter).
+template <bool FP4, int REPL>
+struct Cfg2 {
+  static constexpr int kSfbRepl = REPL;
+  static constexpr int kKgPerStage = FP4 ? 2 : 1;        // 4-block K groups per 128-byte stage
+  static constexpr int kStagesPerChunk = 2 / kKgPerStage; // a row-scale chunk spans 2 K groups
+  static constexpr int kABytes = 128 * 128;
+  static constexpr int kBBytes = 128 * 128;
+  static constexpr int kSfbBytes = kKgPerStage * kSfbRepl * 1024;
+  static constexpr int kChunkBytes = 4096;                // row-scale chunk, in the stage that loads it
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfbBytes + kChunkBytes;
+  static constexpr int kStages0 = (kSmemLimit - 2048) / kStageBytes;
+  static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
+};
+
+struct Pair2Params {
+  __nv_bfloat16* D;
+  int64_t M, N;
+  int sfa_kq;           // row-scale chunks per 128-row block
+  int sfb_kg;           // column-scale blocks per 256-column block
+  int num_m_tiles;      // 128-row tiles of D
+  int num_unit_rows;    // 256-row pair units
+  int num_n_tiles;      // 256-column tiles
+  int num_k_stages;
+  uint32_t idesc;
+  int* status;
+  uint64_t limit_ns;
+};
+
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+// 2-D tensor load by a CTA of a pair, completing bytes on the barrier at shared::cluster
+// address `bar_cluster` (which may be in the peer CTA).
+__device__ __forceinline__ void tma_load_2d_pair(const void* tmap, uint32_t bar_cluster,
+                                                 void* dst, int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar_cluster)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+// 128 lanes x 32 bytes of shared memory into 8 tensor-memory columns, in both CTAs.
+__device__ __forceinline__ void tc_cp_wide_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+__device__ __forceinline__ void mma_mxf8f6f4_pair(uint32_t d, uint64_t a, uint64_t b,
+                                                  uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                                  uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+__device__ __forceinline__ void mma_mxf4_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+
+// Unit u -> (256-row unit row ur, 256-column tile nt), banded along N for L2 reuse.
+__device__ __forceinline__ void unit_tile2(const Pair2Params& p, int u, int& ur, int& nt) {
+  const int per_band = kBandUnits * p.num_n_tiles;
+  const int b = u / per_band;
+  const int r0 = b * kBandUnits;
+  const int h = p.num_unit_rows - r0 < kBandUnits ? p.num_unit_rows - r0 : kBandUnits;
+  const int v = u - b * per_band;
+  ur = r0 + v % h;
+  nt = v / h;
+}
+
+// 10 warps share an SM's four register-file quarters (16384 registers each) as
+// 3+3+2+2 warps, so a thread may hold at most 16384 / (3 * 32) = 170 registers.
+template <bool FP4, bool A_MN, bool B_MN, int REPL>
+__global__ void __maxnreg__(168)
+    mx_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmSFA,
+                       const __grid_constant__ CUtensorMap tmSFB, const Pair2Params p) {
+  using C = Cfg2<FP4, REPL>;
+  constexpr int kSfbRepl = C::kSfbRepl;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + C::kStages * C::kABytes;
+  uint8_t* sSFB = sB + C::kStages * C::kBBytes;
+  uint8_t* sSFA = sSFB + C::kStages * C::kSfbBytes;        // one chunk slot per stage
+  uint64_t* full = reinterpret_cast<uint64_t*>(sSFA + C::kStages * C::kChunkBytes);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* acc_full = empty + C::kStages;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  constexpr uint16_t kPairMask = 3;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);     // used in the leader: its producer's arrive + both CTAs' bytes
+      mbar_init(&empty[s], 1);    // released by the leader's commit in both CTAs
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 2 * kEpiWarps);   // used in the leader: epilogues of both CTAs
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmSFA);
+    prefetch_tmap(&tmSFB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // both CTAs' barriers initialised and tensor memory allocated
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int total_units = p.num_unit_rows * p.num_n_tiles;
+  const int first_unit = static_cast<int>(blockIdx.x >> 1);
+  const int unit_stride = static_cast<int>(gridDim.x >> 1);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_parity = 0;
+      bool ok = true;
+      for (int u = first_unit; ok && u < total_units; u += unit_stride) {
+        int ur, nt;
+        unit_tile2(p, u, ur, nt);
+        const int mt = ur * 2 + static_cast<int>(rank);          // this CTA's 128 rows of A
+        const int nb = nt * 2 + static_cast<int>(rank);          // this CTA's 128 rows of B
+        for (int ks = 0; ks < p.num_k_stages; ++ks) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.limit_ns, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = map_to_cta(smem_u32(&full[stage]), 0);
+          const int kq = ks / C::kStagesPerChunk;
+          const bool chunk_start = (ks % C::kStagesPerChunk) == 0;
+          if (leader) {
+            mbar_arrive_expect_tx(&full[stage], 2 * (C::kStageBytes - C::kChunkBytes +
+                                                     (chunk_start ? C::kChunkBytes : 0)));
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          }
+          uint8_t* a_dst = sA + stage * C::kABytes;
+          uint8_t* b_dst = sB + stage * C::kBBytes;
+          if (A_MN) tma_load_2d_pair(&tmA, bar, a_dst, mt * 128, ks * 128);
+          else      tma_load_2d_pair(&tmA, bar, a_dst, ks * 128, mt * 128);
+          if (B_MN) tma_load_2d_pair(&tmB, bar, b_dst, nb * 128, ks * 128);
+          else      tma_load_2d_pair(&tmB, bar, b_dst, ks * 128, nb * 128);
+          // column scales of all 256 B rows, one copy per lane quarter
+#pragma unroll
+          for (int g = 0; g < C::kKgPerStage; ++g)
+#pragma unroll
+            for (int r = 0; r < kSfbRepl; ++r)
+              tma_load_2d_pair(&tmSFB, bar, sSFB + stage * C::kSfbBytes + (g * kSfbRepl + r) * 1024,
+                               0, nt * p.sfb_kg + ks * C::kKgPerStage + g);
+          // row scales of this CTA's 128 A rows, one chunk per 4 K groups
+          if (chunk_start)
+            tma_load_2d_pair(&tmSFA, bar, sSFA + stage * C::kChunkBytes, 0,
+                             (mt * p.sfa_kq + kq) * 4);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      for (int s = 0; s < C::kStages; ++s)
+        if (armed & (1u << s)) {
+          volatile int no_abort = 0;
+          mbar_wait(&full[s], (armed_parity >> s) & 1u, p.limit_ns / 4 + 1, &no_abort, nullptr);
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------------------ MMA issuer (leader)
+      int stage = 0;
+      uint32_t phase = 0, kiter = 0, chunk = 0;
+      bool ok = true;
+      int local = 0;
+      for (int u = first_unit; ok && u < total_units; u += unit_stride, ++local) {
+        if (!mbar_wait(acc_empty, (local & 1) ^ 1, p.limit_ns, abort_flag, p.status)) break;
+        tc_fence_after();
+        for (int ks = 0; ks < p.num_k_stages; ++ks) {
+          if (!mbar_wait(&full[stage], phase, p.limit_ns, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int sub = ks % C::kStagesPerChunk;                  // stage within the chunk
+          const uint32_t sfa_t = tmem + kSfaCol + (chunk & 1) * 8;
+          if (sub == 0)
+            tc_cp_wide_pair(sfa_t, make_sdesc(smem_u32(sSFA + stage * C::kChunkBytes), 128, 256, 0));
+          uint32_t sfb_t[C::kKgPerStage];
+#pragma unroll
+          for (int g = 0; g < C::kKgPerStage; ++g) {
+            sfb_t[g] = tmem + kSfbCol + ((kiter * C::kKgPerStage + g) & 3) * 8;
+            tc_cp_wide_pair(sfb_t[g], make_sdesc(smem_u32(sSFB + stage * C::kSfbBytes +
+                                                           g * kSfbRepl * 1024),
+                                                 128, 256, 0));
+          }
+          const uint32_t a_base = smem_u32(sA + stage * C::kABytes);
+          const uint32_t b_base = smem_u32(sB + stage * C::kBBytes);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t ad = A_MN ? make_sdesc(a_base + j * 4096, 16384, 1024, kSwizzle128B)
+                                     : make_sdesc(a_base + j * 32, 16, 1024, kSwizzle128B);
+            const uint64_t bd = B_MN ? make_sdesc(b_base + j * 4096, 16384, 1024, kSwizzle128B)
+                                     : make_sdesc(b_base + j * 32, 16, 1024, kSwizzle128B);
+            const uint32_t acc = (ks | j) != 0;
+            if (FP4) {
+              const int g = j >> 1;                                   // K group within the stage
+              const uint32_t sfid = (j & 1) * 2;
+              mma_mxf4_pair(tmem, ad, bd, p.idesc | idesc_sf_id(sfid, sfid),
+                            sfa_t + 4 * (sub * C::kKgPerStage + g), sfb_t[g], acc);
+            } else {
+              mma_mxf8f6f4_pair(tmem, ad, bd, p.idesc | idesc_sf_id(j, j), sfa_t + 4 * sub,
+                                sfb_t[0], acc);
+            }
+          }
+          tc_commit_pair(&empty[stage], kPairMask);
+          ++kiter;
+          if (sub == C::kStagesPerChunk - 1 || ks == p.num_k_stages - 1) ++chunk;
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (ok) tc_commit_pair(acc_full, kPairMask);
+      }
+      // every MMA and scale copy must be finished before tensor memory is freed
+      tc_commit_pair(drain, 1);
+      volatile int no_abort = 0;
+      mbar_wait(drain, 0, p.limit_ns, &no_abort, nullptr);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue (both CTAs)
+    constexpr int kCols = 128;             // columns per epilogue warp
+    constexpr int kChunks = kCols / 32;
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const uint32_t acc_empty_leader = map_to_cta(smem_u32(acc_empty), 0);
+    int local = 0;
+    for (int u = first_unit; u < total_units; u += unit_stride, ++local) {
+      int ur, nt;
+      unit_tile2(p, u, ur, nt);
+      const int mt = ur * 2 + static_cast<int>(rank);
+      if (!mbar_wait(acc_full, local & 1, p.limit_ns, abort_flag, p.status)) break;
+      tc_fence_after();
+      uint32_t r[kChunks][32];
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * kCols;
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) tmem_ld32(tbase + c * 32, r[c]);
+      tmem_ld_wait(r[0]);
+#pragma unroll
+      for (int c = 1; c < kChunks; ++c) reg_fence(r[c]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+      const int64_t row = static_cast<int64_t>(mt) * 128 + q * 32 + lane;
+      const int64_t col0 = static_cast<int64_t>(nt) * 256 + h * kCols;
+      if (row < p.M) {
+        __nv_bfloat16* out = p.D + row * p.N + col0;
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int o = c * 32 + v * 8;
+            if (col0 + o < p.N)
+              st_global_v4_cs(out + o,
+                              pack_bf16x2(__uint_as_float(r[c][v * 8 + 0]), __uint_as_float(r[c][v * 8 + 1])),
+                              pack_bf16x2(__uint_as_float(r[c][v * 8 + 2]), __uint_as_float(r[c][v * 8 + 3])),
+                              pack_bf16x2(__uint_as_float(r[c][v * 8 + 4]), __uint_as_float(r[c][v * 8 + 5])),
+                              pack_bf16x2(__uint_as_float(r[c][v * 8 + 6]), __uint_as_float(r[c][v * 8 + 7])));
+          }
+      }
+    }
+  }
+  __syncthreads();
+  cluster_sync();   // both CTAs are done with tensor memory and with each other's barriers
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+  cluster_sync();
+}
+
+template <bool FP4, bool A_MN, bool B_MN, int REPL>
+bsmma_status launch_2sm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
+                        const CUtensorMap& tsb, const Pair2Params& p, cudaStream_t stream) {
+  using C = Cfg2<FP4, REPL>;
+  auto kern = mx_gemm_2sm_kernel<FP4, A_MN, B_MN, REPL>;
+  static int max_clusters = -1;   // benign race: every thread computes the same value
+  if (max_clusters < 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
+      return BSMMA_ERR_CUDA;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * sms, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1)
+      return BSMMA_ERR_CUDA;
+    max_clusters = n;
+  }
+  const int64_t units = static_cast<int64_t>(p.num_unit_rows) * p.num_n_tiles;
+  const int grid = static_cast<int>(2 * (units < max_clusters ? units : max_clusters));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, p);
+  count_launches(1);
+  return cuda_ok(e == cudaSuccess ? cudaGetLastError() : e);
+}
+
+}  // namespace
+
+bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B,
+                                const uint8_t* sfb, void* D, int64_t M, int64_t N, int64_t K,
+                                bsmma_layout layout, bsmma_fmt a_fmt, bsmma_fmt b_fmt,
+                                cudaStream_t stream) {
+  bsmma_status st;
+  const DeviceInfo* dev = current_device(&st);
+  if (!dev) return st;
+  const bool fp4 = (a_fmt == BSMMA_E2M1);
+  const uint64_t kbytes = fp4 ? static_cast<uint64_t>(K / 2) : static_cast<uint64_t>(K);
+  const int64_t kblocks = K / 32;
+  const int64_t kq = (kblocks + 7) / 8;                   // row-scale chunks per 128 rows
+  const int64_t kgp = 2 * ((kblocks + 7) / 8);            // column-scale blocks per 256 columns
+  CUtensorMap ta, tb, tsa, tsb;
+  if (layout == BSMMA_TN) st = encode_tmap_u8(&ta, A, M, K, M, 128, 128);
+  else st = encode_tmap_u8(&ta, A, kbytes, M, kbytes, 128, 128);
+  if (st != BSMMA_OK) return st;
+  if (layout == BSMMA_NT) st = encode_tmap_u8(&tb, B, kbytes, N, kbytes, 128, 128);
+  else st = encode_tmap_u8(&tb, B, N, K, N, 128, 128);
+  if (st != BSMMA_OK) return st;
+  // row-scale chunks as [chunks*4][256 words], column-scale blocks as [blocks][256 words]
+  st = encode_tmap_words(&tsa, sfa, 256, static_cast<uint64_t>(2 * ((M + 255) / 256) * kq * 4), 256, 4);
+  if (st != BSMMA_OK) return st;
+  st = encode_tmap_words(&tsb, sfb, 256, static_cast<uint64_t>(((N + 255) / 256) * kgp), 256, 1);
+  if (st != BSMMA_OK) return st;
+  Pair2Params p;
+  p.D = static_cast<__nv_bfloat16*>(D);
+  p.M = M;
+  p.N = N;
+  p.sfa_kq = static_cast<int>(kq);
+  p.sfb_kg = static_cast<int>(kgp);
+  p.num_m_tiles = static_cast<int>((M + 127) / 128);
+  p.num_unit_rows = static_cast<int>((M + 255) / 256);
+  p.num_n_tiles = static_cast<int>((N + 255) / 256);
+  p.num_k_stages = static_cast<int>((static_cast<int64_t>(kbytes) + 127) / 128);
+  const uint32_t af = fp4 ? 1u : static_cast<uint32_t>(a_fmt);
+  const uint32_t bf = fp4 ? 1u : static_cast<uint32_t>(b_fmt);
+  p.idesc = idesc_block_scaled(af, bf, layout == BSMMA_TN, layout != BSMMA_NT, 256, 256);
+  p.status = dev->status;
+  p.limit_ns = wait_limit_ns();
+  if (dense_variant() == 4) {   // column scales only in lanes 0-31 (probe of the read rule)
+    if (fp4) return launch_2sm<true, false, false, 1>(ta, tb, tsa, tsb, p, stream);
+    if (layout == BSMMA_NT) return launch_2sm<false, false, false, 1>(ta, tb, tsa, tsb, p, stream);
+    return BSMMA_ERR_UNSUPPORTED;
+  }
+  if (fp4) return launch_2sm<true, false, false, 4>(ta, tb, tsa, tsb, p, stream);
+  switch (layout) {
+    case BSMMA_NT: return launch_2sm<false, false, false, 4>(ta, tb, tsa, tsb, p, stream);
+    case BSMMA_NN: return launch_2sm<false, false, true, 4>(ta, tb, tsa, tsb, p, stream);
+    default:       return launch_2sm<false, true, true, 4>(ta, tb, tsa, tsb, p, stream);
+  }
+}
+
+}  // namespace bsmma

@@ -108,3 +108,114 @@ bsmma_status launch_relayout(const uint8_t* s0, int64_t rows0, int64_t kb0, uint
 }
 
 }  // namespace bsmma
+
+// ---------------------------------------------------------------------------
+// Wide scale layouts for the SM-pair kernel, read by tcgen05.cp 128x256b copies.
+//
+// Row scales (the A side): one 4 KB chunk per 128 rows and 8 K-blocks (two K groups),
+// holding for TMEM lane l (row l of the block, lane quarter q = l/32) in column
+// c = 4g + q the four scales of row l for K group g of the chunk (other columns are
+// padding).  An MMA for K group g names column base + 4g (scale addresses are
+// 4-column aligned) and lane quarter q reads its own column base + 4g + q.  Chunk
+// (rb, kq) sits at (rb*KQ + kq)*4096 and its bytes are in the order the copy's
+// source descriptor walks (8-row groups of 256 bytes, two 16-byte column halves of
+// 128 bytes each):
+//   byte(l, c, b) = (l/8)*256 + (c/4)*128 + (l%8)*16 + (c%4)*4 + b.
+// Column scales (the B side): one 1 KB block per 256 columns and one K-group,
+// 32 lanes x 8 columns: lane i, column c holds the four scales of column 32c+i.
+// Block (nb, kg) sits at (nb*KGp + kg)*1024, bytes ordered like lanes 0-31 above.
+// Padding holds 127 (scale 1.0).
+namespace bsmma {
+namespace {
+
+__device__ __forceinline__ uint32_t gather4(const uint8_t* s, int64_t rows, int64_t kblocks,
+                                            int64_t r, int64_t kb0) {
+  uint32_t v = 0;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const int64_t kb = kb0 + b;
+    const uint32_t x = (r < rows && kb < kblocks) ? s[r * kblocks + kb] : 127u;
+    v |= x << (8 * b);
+  }
+  return v;
+}
+
+struct WideJob {
+  const uint8_t* src;
+  uint8_t* dst;
+  int64_t rows, kblocks;
+  int64_t per_block;   // chunks (row role: KQ) or blocks (column role: KGp) per row block
+  int64_t words;       // output words
+  int role;            // 0 row scales, 1 column scales
+};
+
+__device__ __forceinline__ void wide_word(const WideJob& j, int64_t w) {
+  uint32_t v;
+  if (j.role == 0) {
+    const int64_t chunk = w >> 10;                 // 1024 words per 4 KB chunk
+    const int wi = static_cast<int>(w & 1023);
+    const int64_t rb = chunk / j.per_block, kq = chunk - rb * j.per_block;
+    const int byte = wi * 4;
+    const int lg = byte >> 8, ch = (byte >> 7) & 1, l8 = (byte >> 4) & 7, c4 = (byte >> 2) & 3;
+    const int l = lg * 8 + l8, c = ch * 4 + c4, q = l >> 5;
+    v = (c4 == q) ? gather4(j.src, j.rows, j.kblocks, rb * 128 + l, (kq * 2 + ch) * 4)
+                  : 0x7f7f7f7fu;
+  } else {
+    const int64_t blk = w >> 8;                    // 256 words per 1 KB block
+    const int wi = static_cast<int>(w & 255);
+    const int64_t nb = blk / j.per_block, kg = blk - nb * j.per_block;
+    const int byte = wi * 4;
+    const int lg = byte >> 8, ch = (byte >> 7) & 1, l8 = (byte >> 4) & 7, c4 = (byte >> 2) & 3;
+    const int i = lg * 8 + l8, c = ch * 4 + c4;
+    v = gather4(j.src, j.rows, j.kblocks, nb * 256 + 32 * c + i, kg * 4);
+  }
+  reinterpret_cast<uint32_t*>(j.dst)[w] = v;
+}
+
+__global__ void __launch_bounds__(256) wide_relayout_kernel(WideJob j0, WideJob j1) {
+  const int64_t total = j0.words + j1.words;
+  for (int64_t w = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; w < total;
+       w += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    if (w < j0.words) wide_word(j0, w);
+    else wide_word(j1, w - j0.words);
+  }
+}
+
+WideJob make_wide(const uint8_t* s, int64_t rows, int64_t kb, uint8_t* out, int role) {
+  WideJob j;
+  j.src = s;
+  j.dst = out;
+  j.rows = rows;
+  j.kblocks = kb;
+  j.role = role;
+  j.per_block = role == 0 ? (kb + 7) / 8 : 2 * ((kb + 7) / 8);
+  j.words = (s && out && rows > 0 && kb > 0) ? wide_scale_bytes(rows, kb, role) / 4 : 0;
+  return j;
+}
+
+}  // namespace
+
+int64_t wide_scale_bytes(int64_t rows, int64_t kblocks, int role) {
+  if (rows <= 0 || kblocks <= 0) return 0;
+  if (role == 0) return 2 * ((rows + 255) / 256) * ((kblocks + 7) / 8) * 4096;
+  return ((rows + 255) / 256) * 2 * ((kblocks + 7) / 8) * 1024;
+}
+
+bsmma_status launch_wide_relayout(const uint8_t* sa, int64_t rows_a, uint8_t* out_a,
+                                  const uint8_t* sb, int64_t rows_b, uint8_t* out_b,
+                                  int64_t kblocks, cudaStream_t stream) {
+  bsmma_status st;
+  const DeviceInfo* dev = current_device(&st);
+  if (!dev) return st;
+  WideJob j0 = make_wide(sa, rows_a, kblocks, out_a, 0), j1 = make_wide(sb, rows_b, kblocks, out_b, 1);
+  const int64_t total = j0.words + j1.words;
+  if (total == 0) return BSMMA_OK;
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(dev->sm_count) * 8;
+  if (blocks > cap) blocks = cap;
+  wide_relayout_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(j0, j1);
+  count_launches(1);
+  return cuda_ok(cudaGetLastError());
+}
+
+}  // namespace bsmma

@@ -175,8 +175,9 @@ bsmma_status bsmma_set_wait_limit_ns(int64_t ns);
 
 /* Selects the dense kernel variant for later mx_gemm / mx_gemm_tiled calls:
  * 0 automatic (default), 1 one CTA per 128x256 tile, 2 CTA pairs (2-CTA clusters
- * computing two vertically adjacent tiles that share one multicast B tile).  All
- * variants compute the same result; this is a tuning and testing control. */
+ * computing two vertically adjacent tiles that share one multicast B tile), 3 SM-pair
+ * MMAs (2-CTA clusters issuing one 256x256 MMA over both SMs).  All variants compute
+ * the same result; this is a tuning and testing control. */
 bsmma_status bsmma_set_dense_variant(int variant);
 
 /* Selects the grouped kernel's tile width for later grouped_fp8_gemm calls: 0

@@ -71,6 +71,10 @@ def bind(path: str):
     lib.oracle_scale_tiled_bytes.restype = i64
     lib.oracle_scale_relayout.argtypes = [p, i64, i64, p]
     lib.oracle_scale_relayout.restype = None
+    lib.oracle_wide_scale_bytes.argtypes = [i64, i64, i32]
+    lib.oracle_wide_scale_bytes.restype = i64
+    lib.oracle_wide_scale_relayout.argtypes = [p, i64, i64, i32, p]
+    lib.oracle_wide_scale_relayout.restype = None
     return lib
 
 
@@ -162,4 +166,18 @@ def scale_relayout(s_plain: np.ndarray, lib=None) -> np.ndarray:
     rows, kblocks = s.shape
     out = np.empty(scale_tiled_bytes(rows, kblocks, lib), dtype=np.uint8)
     _load(lib).oracle_scale_relayout(_ptr(s), rows, kblocks, _ptr(out))
+    return out
+
+
+def wide_scale_bytes(rows: int, kblocks: int, role: int, lib=None) -> int:
+    return int(_load(lib).oracle_wide_scale_bytes(rows, kblocks, role))
+
+
+def wide_scale_relayout(s_plain: np.ndarray, role: int, lib=None) -> np.ndarray:
+    """Plain E8M0 scales [rows, kblocks] -> wide layout (role 0 rows of op(A),
+    role 1 rows of op(B)), flat uint8."""
+    s = np.ascontiguousarray(s_plain, dtype=np.uint8)
+    rows, kblocks = s.shape
+    out = np.empty(wide_scale_bytes(rows, kblocks, role, lib), dtype=np.uint8)
+    _load(lib).oracle_wide_scale_relayout(_ptr(s), rows, kblocks, role, _ptr(out))
     return out

@@ -303,3 +303,54 @@ void oracle_scale_relayout(const uint8_t* s, int64_t rows, int64_t kblocks, uint
       out[(rb * KG + kg) * 512 + (rr % 32) * 16 + (rr / 32) * 4 + kk] = s[r * kblocks + kb];
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Wide scale layouts (integer permutations with padding), read by the      */
+/* tensor core's 128-lane x 32-byte copies.                                 */
+/*                                                                          */
+/* Byte position of (lane l, column c, byte b) inside a block, in the order */
+/* the copy walks its source: 8-lane groups of 256 bytes, each holding two  */
+/* 128-byte halves (columns 0-3, 4-7) of 8 lanes x 16 bytes.               */
+/*                                                                          */
+/* Row role (op(A) rows): 4096-byte chunk per 128 rows and 8 K-blocks.      */
+/*   Lane l is row l of the block, in lane quarter q = l/32.  Column c holds */
+/*   row l's 4 scales of K group c/4 of the chunk when c%4 == q; every other */
+/*   column is padding.  Chunk (rb, kq) at (rb*KQ + kq)*4096,               */
+/*   RB = 2*ceil(rows/256), KQ = ceil(kblocks/8).                           */
+/* Column role (op(B) rows): 1024-byte block per 256 rows and one K group.  */
+/*   Lane i (0..31), column c holds the 4 scales of row 32c + i.            */
+/*   Block (nb, kg) at (nb*KG + kg)*1024, NB = ceil(rows/256),              */
+/*   KG = 2*ceil(kblocks/8).                                                */
+/* Padding holds 127 (the E8M0 code of 1.0).                                */
+/* ------------------------------------------------------------------------ */
+static int64_t lane_col_byte(int64_t l, int64_t c, int64_t b) {
+  return (l / 8) * 256 + (c / 4) * 128 + (l % 8) * 16 + (c % 4) * 4 + b;
+}
+
+int64_t oracle_wide_scale_bytes(int64_t rows, int64_t kblocks, int role) {
+  if (rows <= 0 || kblocks <= 0) return 0;
+  if (role == 0) return 2 * ((rows + 255) / 256) * ((kblocks + 7) / 8) * 4096;
+  return ((rows + 255) / 256) * 2 * ((kblocks + 7) / 8) * 1024;
+}
+
+void oracle_wide_scale_relayout(const uint8_t* s, int64_t rows, int64_t kblocks, int role,
+                                uint8_t* out) {
+  int64_t total = oracle_wide_scale_bytes(rows, kblocks, role);
+  for (int64_t i = 0; i < total; ++i) out[i] = 127;
+  if (role == 0) {
+    int64_t KQ = (kblocks + 7) / 8;
+    for (int64_t r = 0; r < rows; ++r)
+      for (int64_t kb = 0; kb < kblocks; ++kb) {
+        int64_t rb = r / 128, l = r % 128, kg = kb / 4, kq = kg / 2, g = kg % 2;
+        int64_t c = 4 * g + l / 32;
+        out[(rb * KQ + kq) * 4096 + lane_col_byte(l, c, kb % 4)] = s[r * kblocks + kb];
+      }
+  } else {
+    int64_t KG = 2 * ((kblocks + 7) / 8);
+    for (int64_t n = 0; n < rows; ++n)
+      for (int64_t kb = 0; kb < kblocks; ++kb) {
+        int64_t nb = n / 256, nn = n % 256, kg = kb / 4;
+        out[(nb * KG + kg) * 1024 + lane_col_byte(nn % 32, nn / 32, kb % 4)] = s[n * kblocks + kb];
+      }
+  }
+}

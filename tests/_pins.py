@@ -329,6 +329,49 @@ def pin_relayout(lib=None):
         assert pos[(r, k)] == (rb * KG + kg) * 512 + off, (r, k)
 
 
+def load_wide_positions():
+    out = []
+    with open(os.path.join(GOLDEN, "wide_scale_positions.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                out.append(tuple(int(t) for t in line.split()))
+    return out
+
+
+def pin_wide_relayout(lib=None):
+    """The wide layouts: sizes, every input byte exactly once, padding 127, and the
+    hand-derived positions of the golden fixture."""
+    assert oracle.wide_scale_bytes(1, 1, 0, lib) == 2 * 1 * 4096
+    assert oracle.wide_scale_bytes(257, 9, 0, lib) == 4 * 2 * 4096
+    assert oracle.wide_scale_bytes(1, 1, 1, lib) == 1 * 2 * 1024
+    assert oracle.wide_scale_bytes(257, 9, 1, lib) == 2 * 4 * 1024
+    rows, kblocks = 300, 14
+    per = {0: (kblocks + 7) // 8, 1: 2 * ((kblocks + 7) // 8)}
+    size = {0: 4096, 1: 1024}
+    for role in (0, 1):
+        r_ids = np.repeat((np.arange(rows) % 251)[:, None], kblocks, axis=1).astype(np.uint8)
+        hi = np.repeat((np.arange(rows) // 251)[:, None], kblocks, axis=1).astype(np.uint8)
+        k_ids = np.repeat(np.arange(kblocks)[None, :], rows, axis=0).astype(np.uint8)
+        out_r = oracle.wide_scale_relayout(r_ids, role, lib)
+        out_h = oracle.wide_scale_relayout(hi, role, lib)
+        out_k = oracle.wide_scale_relayout(k_ids, role, lib)
+        ones = oracle.wide_scale_relayout(np.zeros((rows, kblocks), dtype=np.uint8), role, lib)
+        assert out_r.size == oracle.wide_scale_bytes(rows, kblocks, role, lib)
+        is_data = ones == 0
+        assert is_data.sum() == rows * kblocks
+        assert np.all(ones[~is_data] == 127)
+        src = list(zip((out_h[is_data].astype(int) * 251 + out_r[is_data].astype(int)).tolist(),
+                       out_k[is_data].astype(int).tolist()))
+        assert len(set(src)) == rows * kblocks
+        pos = dict(zip(src, np.nonzero(is_data)[0].tolist()))
+        for rl, r, k, off in load_wide_positions():
+            if rl != role or r >= rows or k >= kblocks:
+                continue
+            blk = (r // 128, k // 8) if role == 0 else (r // 256, k // 4)
+            assert pos[(r, k)] == (blk[0] * per[role] + blk[1]) * size[role] + off, (role, r, k)
+
+
 ALL_PINS = [pin_decode_points, pin_decode_vs_torch, pin_dense_bruteforce, pin_dense_unit_scales,
             pin_dense_pow2, pin_dense_layouts, pin_grouped_concat, pin_grouped_g1_transpose,
-            pin_grouped_probes, pin_relayout]
+            pin_grouped_probes, pin_relayout, pin_wide_relayout]

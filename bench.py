@@ -234,6 +234,7 @@ def run_ours(args):
     bs.build()
     bs.load()
     bs.set_dense_variant(args.dense_variant)
+    bs.set_grouped_tile_width(args.grouped_width)
     dev = torch.device("cuda", local)
     spec = workload_spec(args.workload)
 
@@ -249,8 +250,10 @@ def run_ours(args):
         else:
             t = {k: torch.from_numpy(np.ascontiguousarray(c[k])).to(dev) for k in ("A", "sA", "B", "sB")}
             t["D"] = torch.empty((g["M"], g["N"]), dtype=torch.bfloat16, device=dev)
-            t["tA"] = torch.empty(bs.mx_scale_tiled_bytes(g["M"], g["K"] // 32), dtype=torch.uint8, device=dev)
-            t["tB"] = torch.empty(bs.mx_scale_tiled_bytes(g["N"], g["K"] // 32), dtype=torch.uint8, device=dev)
+            t["tA"] = torch.empty(bs.mx_scale_tiled_bytes(g["M"], g["K"] // 32, "A"), dtype=torch.uint8,
+                                  device=dev)
+            t["tB"] = torch.empty(bs.mx_scale_tiled_bytes(g["N"], g["K"] // 32, "B"), dtype=torch.uint8,
+                                  device=dev)
             host = {k: torch.from_numpy(np.ascontiguousarray(c[k])).pin_memory()
                     for k in ("A", "sA", "B", "sB")}
             g.setdefault("layout", c["layout"])
@@ -269,8 +272,8 @@ def run_ours(args):
             ev[1].record(stream)
             bs.grouped_fp8_gemm(t["X"], t["sX"], t["W"], t["sW"], t["m_sizes"], out=t["D"])
         else:
-            bs.mx_scale_relayout(t["sA"], out=t["tA"])
-            bs.mx_scale_relayout(t["sB"], out=t["tB"])
+            bs.mx_scale_relayout(t["sA"], "A", out=t["tA"])
+            bs.mx_scale_relayout(t["sB"], "B", out=t["tB"])
             ev[1].record(stream)
             bs.mx_gemm_tiled(t["A"], t["tA"], t["B"], t["tB"], g["layout"], g["a"], g["b"],
                              out=t["D"], M=g["M"], N=g["N"], K=g["K"])
@@ -374,6 +377,7 @@ def run_ours(args):
                    "l2": "flushed before every GEMM by a 256 MiB write outside the timed events",
                    "parallelism": f"replicas x{ws}",
                    "dense_variant": args.dense_variant,
+                   "grouped_width": args.grouped_width,
                    "per_gemm_kernel_ms": [round(x, 4) for x in per_gemm_ms]},
         "roofline": {"bound": "tensor", "kernel": kernel,
                      "launch": describe(dom_g),
@@ -485,8 +489,10 @@ def main():
                     choices=["mxfp8_dense", "mxfp8_256", "mxfp4_dense", "linear_triple", "grouped_fp8"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
-    ap.add_argument("--dense-variant", type=int, default=0, choices=[0, 1, 2],
-                    help="0 automatic, 1 single-CTA tiles, 2 CTA pairs (tuning only)")
+    ap.add_argument("--grouped-width", type=int, default=0, choices=[0, 128, 256],
+                    help="grouped tile width: 0 automatic, 128 or 256 (tuning only)")
+    ap.add_argument("--dense-variant", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="0 automatic, 1 single-CTA tiles, 2 CTA pairs, 3 SM-pair MMAs (tuning only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     args = ap.parse_args()

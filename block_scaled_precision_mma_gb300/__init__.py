@@ -27,9 +27,10 @@ __all__ = ["mx_gemm", "mx_gemm_tiled", "mx_gemm_noalloc", "grouped_fp8_gemm", "m
            "mx_scale_tiled_bytes", "device_status", "reserve_workspace", "set_wait_limit_ns",
            "set_dense_variant", "set_grouped_tile_width",
            "launch_count", "probe_wait_timeout", "status_string", "BsmmaError", "load",
-           "LAYOUTS", "FORMATS", "build", "LIB_PATH"]
+           "LAYOUTS", "FORMATS", "ROLES", "build", "LIB_PATH"]
 
 LAYOUTS = {"NT": 0, "NN": 1, "TN": 2}
+ROLES = {"A": 0, "B": 1}      # scales of op(A) rows / of op(B) rows
 FORMATS = {"e4m3": 0, "e5m2": 1, "e2m1": 2}
 STATUS = ["BSMMA_OK", "BSMMA_ERR_INVALID_ARG", "BSMMA_ERR_UNSUPPORTED", "BSMMA_ERR_MISALIGNED",
           "BSMMA_ERR_WORKSPACE", "BSMMA_ERR_CUDA", "BSMMA_DEV_TIMEOUT", "BSMMA_DEV_BAD_MSIZES",
@@ -61,8 +62,8 @@ def load(path: str | None = None):
         lib.mx_gemm_tiled.argtypes = [p, p, p, p, p, i64, i64, i64, i32, i32, i32, p]
         lib.mx_gemm_noalloc.argtypes = [p, p, p, p, p, i64, i64, i64, i32, i32, i32, p]
         lib.grouped_fp8_gemm.argtypes = [p, p, p, p, p, p, i64, i32, i64, i64, p]
-        lib.mx_scale_relayout.argtypes = [p, i64, i64, p, p]
-        lib.mx_scale_tiled_bytes.argtypes = [i64, i64]
+        lib.mx_scale_relayout.argtypes = [p, i64, i64, i32, p, p]
+        lib.mx_scale_tiled_bytes.argtypes = [i64, i64, i32]
         lib.mx_scale_tiled_bytes.restype = i64
         lib.bsmma_reserve_workspace.argtypes = [i64, p]
         lib.bsmma_device_status.argtypes = [p]
@@ -173,18 +174,19 @@ def grouped_fp8_gemm(X, sX, W, sW, m_sizes, out=None, stream=None):
     return out
 
 
-def mx_scale_tiled_bytes(rows: int, kblocks: int) -> int:
-    return int(load().mx_scale_tiled_bytes(rows, kblocks))
+def mx_scale_tiled_bytes(rows: int, kblocks: int, role="A") -> int:
+    return int(load().mx_scale_tiled_bytes(rows, kblocks, ROLES[role]))
 
 
-def mx_scale_relayout(s_plain, out=None, stream=None):
-    """Plain E8M0 scales [rows, kblocks] -> tensor-core atom layout (flat uint8)."""
+def mx_scale_relayout(s_plain, role="A", out=None, stream=None):
+    """Plain E8M0 scales [rows, kblocks] -> the tiled layout of `role` ('A': scales
+    of op(A) rows, 'B': scales of op(B) rows), as a flat uint8 tensor."""
     rows, kblocks = s_plain.shape
     if out is None:
-        out = torch.empty(mx_scale_tiled_bytes(rows, kblocks), dtype=torch.uint8,
+        out = torch.empty(mx_scale_tiled_bytes(rows, kblocks, role), dtype=torch.uint8,
                           device=s_plain.device)
-    _check(load().mx_scale_relayout(_ptr(s_plain), rows, kblocks, _ptr(out), _stream(stream)),
-           "mx_scale_relayout")
+    _check(load().mx_scale_relayout(_ptr(s_plain), rows, kblocks, ROLES[role], _ptr(out),
+                                    _stream(stream)), "mx_scale_relayout")
     return out
 
 

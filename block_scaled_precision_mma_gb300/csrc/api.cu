@@ -218,19 +218,22 @@ using namespace bsmma;
 
 extern "C" {
 
-int64_t mx_scale_tiled_bytes(int64_t rows, int64_t kblocks) {
-  if (rows <= 0 || kblocks <= 0) return 0;
-  return 2 * ((rows + 255) / 256) * 2 * ((kblocks + 7) / 8) * 512;
+int64_t mx_scale_tiled_bytes(int64_t rows, int64_t kblocks, bsmma_scale_role role) {
+  if (role != BSMMA_SCALES_A && role != BSMMA_SCALES_B) return 0;
+  return wide_scale_bytes(rows, kblocks, static_cast<int>(role));
 }
 
 bsmma_status mx_scale_relayout(const uint8_t* s_plain, int64_t rows, int64_t kblocks,
-                               uint8_t* s_tiled, bsmma_stream stream) {
+                               bsmma_scale_role role, uint8_t* s_tiled, bsmma_stream stream) {
   if (rows < 0 || kblocks < 0) return BSMMA_ERR_INVALID_ARG;
+  if (role != BSMMA_SCALES_A && role != BSMMA_SCALES_B) return BSMMA_ERR_INVALID_ARG;
   if (rows == 0 || kblocks == 0) return BSMMA_OK;
   if (!s_plain || !s_tiled) return BSMMA_ERR_INVALID_ARG;
   if (!aligned16(s_tiled)) return BSMMA_ERR_MISALIGNED;
-  return launch_relayout(s_plain, rows, kblocks, s_tiled, nullptr, 0, 0, nullptr,
-                         reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (role == BSMMA_SCALES_A)
+    return launch_wide_relayout(s_plain, rows, s_tiled, nullptr, 0, nullptr, kblocks, s);
+  return launch_wide_relayout(nullptr, 0, nullptr, s_plain, rows, s_tiled, kblocks, s);
 }
 
 bsmma_status mx_gemm_tiled(const void* A, const uint8_t* sA_tiled, const void* B,
@@ -251,25 +254,14 @@ bsmma_status mx_gemm(const void* A, const uint8_t* sA, const void* B, const uint
   if (st != BSMMA_OK || M == 0 || N == 0) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (K == 0) return cuda_ok(cudaMemsetAsync(D, 0, static_cast<size_t>(M * N * 2), s));
-  if (dense_variant() >= 3) {
-    const int64_t wa = align_up(wide_scale_bytes(M, K / 32, 0), 256);
-    const int64_t wb = wide_scale_bytes(N, K / 32, 1);
-    void* w = nullptr;
-    st = get_workspace(wa + wb, s, &w);
-    if (st != BSMMA_OK) return st;
-    uint8_t* ta = static_cast<uint8_t*>(w);
-    st = launch_wide_relayout(sA, M, ta, sB, N, ta + wa, K / 32, s);
-    if (st != BSMMA_OK) return st;
-    return launch_mx_gemm_2sm(A, ta, B, ta + wa, D, M, N, K, layout, a_fmt, b_fmt, s);
-  }
-  const int64_t bytes_a = align_up(mx_scale_tiled_bytes(M, K / 32), 256);
-  const int64_t bytes_b = mx_scale_tiled_bytes(N, K / 32);
+  const int64_t bytes_a = align_up(wide_scale_bytes(M, K / 32, 0), 256);
+  const int64_t bytes_b = wide_scale_bytes(N, K / 32, 1);
   void* ws = nullptr;
   st = get_workspace(bytes_a + bytes_b, s, &ws);
   if (st != BSMMA_OK) return st;
   uint8_t* ta = static_cast<uint8_t*>(ws);
   uint8_t* tb = ta + bytes_a;
-  st = launch_relayout(sA, M, K / 32, ta, sB, N, K / 32, tb, s);
+  st = launch_wide_relayout(sA, M, ta, sB, N, tb, K / 32, s);
   if (st != BSMMA_OK) return st;
   return launch_mx_gemm(A, ta, B, tb, D, M, N, K, layout, a_fmt, b_fmt, s);
 }
@@ -316,7 +308,7 @@ bsmma_status bsmma_set_wait_limit_ns(int64_t ns) {
 }
 
 bsmma_status bsmma_set_dense_variant(int variant) {
-  if (variant < 0 || variant > 4) return BSMMA_ERR_INVALID_ARG;
+  if (variant < 0 || variant > 3) return BSMMA_ERR_INVALID_ARG;
   g_dense_variant = variant;
   return BSMMA_OK;
 }

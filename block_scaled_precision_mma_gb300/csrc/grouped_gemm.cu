@@ -42,7 +42,8 @@ struct GCfg {
   static constexpr int kBTileBytes = BN * kBK;
   static constexpr int kStageBytes = kATileBytes + kBTileBytes;
   static constexpr int kStages = BN == 128 ? 6 : 4;
-  static constexpr uint32_t kTmemCols = 2 * BN;   // two partial slots
+  static constexpr int kSlots = 512 / BN;         // partial slots in tensor memory (4 or 2)
+  static constexpr uint32_t kTmemCols = 512;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 2048;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -89,9 +90,10 @@ __global__ void __maxnreg__(168)
   uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + kStages * kStageBytes);
   uint64_t* empty = full + kStages;
-  uint64_t* p_full = empty + kStages;      // [2]
-  uint64_t* p_empty = p_full + 2;          // [2]
-  uint64_t* drain = p_empty + 2;
+  constexpr int kSlots = C::kSlots;
+  uint64_t* p_full = empty + kStages;      // [kSlots]
+  uint64_t* p_empty = p_full + kSlots;     // [kSlots]
+  uint64_t* drain = p_empty + kSlots;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   GroupTable& gt = *reinterpret_cast<GroupTable*>(
@@ -123,7 +125,7 @@ __global__ void __maxnreg__(168)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kSlots; ++s) {
       mbar_init(&p_full[s], 1);
       mbar_init(&p_empty[s], kEpiWarps);
     }
@@ -189,9 +191,9 @@ __global__ void __maxnreg__(168)
       bool ok = true;
       for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
         for (int kb = 0; kb < KB; ++kb) {
-          const uint32_t slot = pcount & 1;
+          const uint32_t slot = pcount % kSlots;
           if (!mbar_wait(&full[stage], phase, p.limit_ns, abort_flag, p.status) ||
-              !mbar_wait(&p_empty[slot], ((pcount >> 1) & 1) ^ 1, p.limit_ns, abort_flag,
+              !mbar_wait(&p_empty[slot], ((pcount / kSlots) & 1) ^ 1, p.limit_ns, abort_flag,
                          p.status)) {
             ok = false;
             break;
@@ -229,6 +231,9 @@ __global__ void __maxnreg__(168)
       const int64_t m_g = gt.size[g];
       const int64_t l = static_cast<int64_t>(mt - gt.tile_start[g]) * kBM + q * 32 + lane;
       const bool valid = l < m_g;
+      // a warp whose 32 rows all lie past the group's end folds nothing (it still
+      // takes part in the partial-slot handshake)
+      const bool warp_rows = static_cast<int64_t>(mt - gt.tile_start[g]) * kBM + q * 32 < m_g;
       const float* sx = p.sX + gt.start[g] * KB + l;   // + kb * m_g
       // weight scales of the 128-column block(s) of this warp's columns
       const float* sw = p.sW + (static_cast<int64_t>(g) * (p.N / 128) +
@@ -253,14 +258,39 @@ __global__ void __maxnreg__(168)
 #pragma unroll
           for (int b = 0; b < kSwPerWarp; ++b) sw_next[b] = __ldg(sw + (sw_blk0 + b) * KB + kb + 1);
         }
-        const uint32_t slot = pcount & 1;
-        if (!mbar_wait(&p_full[slot], (pcount >> 1) & 1, p.limit_ns, abort_flag, p.status)) {
+        const uint32_t slot = pcount % kSlots;
+        if (!mbar_wait(&p_full[slot], (pcount / kSlots) & 1, p.limit_ns, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t taddr =
             tmem + (static_cast<uint32_t>(q * 32) << 16) + slot * BN + h * kCols;
+        if (!warp_rows) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&p_empty[slot]);
+          ++pcount;
+          continue;
+        }
+        if (kCols == 64) {
+          // the whole 64-column slice in one round trip
+          uint32_t r0[32], r1[32];
+          tmem_ld32(taddr, r0);
+          tmem_ld32(taddr + 32, r1);
+          tmem_ld_wait(r0);
+          reg_fence(r1);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&p_empty[slot]);
+          const float s = sx_cur * sw_cur[0];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] = fmaf(s, __uint_as_float(r0[i]), acc[i]);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[32 + i] = fmaf(s, __uint_as_float(r1[i]), acc[32 + i]);
+          ++pcount;
+          continue;
+        }
 #pragma unroll
         for (int c = 0; c < kCols / 16; ++c) {
           uint32_t r[16];
@@ -281,7 +311,7 @@ __global__ void __maxnreg__(168)
         __nv_bfloat16* out = p.D + row * p.N + static_cast<int64_t>(nt) * BN + h * kCols;
 #pragma unroll
         for (int v = 0; v < kCols / 8; ++v)
-          st_global_v4(out + v * 8, pack_bf16x2(acc[v * 8 + 0], acc[v * 8 + 1]),
+          st_global_v4_cs(out + v * 8, pack_bf16x2(acc[v * 8 + 0], acc[v * 8 + 1]),
                        pack_bf16x2(acc[v * 8 + 2], acc[v * 8 + 3]),
                        pack_bf16x2(acc[v * 8 + 4], acc[v * 8 + 5]),
                        pack_bf16x2(acc[v * 8 + 6], acc[v * 8 + 7]));

@@ -40,16 +40,14 @@ bsmma_status validate_dense(const void* A, const void* sA, const void* B, const 
 bsmma_status encode_tmap_words(CUtensorMap* map, const void* base, uint64_t inner,
                                uint64_t outer, uint32_t box_inner, uint32_t box_outer);
 
-// Wide scale layouts of the SM-pair kernel (role 0 row scales, role 1 column scales).
+// Tiled scale layouts (role 0 scales of op(A) rows, role 1 scales of op(B) rows); a
+// null source or destination skips that operand.
 int64_t wide_scale_bytes(int64_t rows, int64_t kblocks, int role);
 bsmma_status launch_wide_relayout(const uint8_t* sa, int64_t rows_a, uint8_t* out_a,
                                   const uint8_t* sb, int64_t rows_b, uint8_t* out_b,
                                   int64_t kblocks, cudaStream_t stream);
 
 // Launchers (arguments already validated by the entry points).
-bsmma_status launch_relayout(const uint8_t* s0, int64_t rows0, int64_t kb0, uint8_t* out0,
-                             const uint8_t* s1, int64_t rows1, int64_t kb1, uint8_t* out1,
-                             cudaStream_t stream);
 bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, const uint8_t* sfb,
                             void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
                             bsmma_fmt a_fmt, bsmma_fmt b_fmt, cudaStream_t stream);

@@ -1,21 +1,24 @@
-// mx_gemm.cu -- dense block-scaled GEMM (MXFP8 / MXFP4) for sm_103a.
+// mx_gemm.cu -- dense block-scaled GEMM (MXFP8 / MXFP4) for sm_103a, one CTA per MMA.
 //
 // D[M][N] (BF16) = op(A) . op(B)^T with one E8M0 scale per 32 values along K
 // ("PyTorch on AMD GPUs gains a FlyDSL backend", Interpretation; "Experimental
 // FlyDSL GEMM backend for TE PyTorch", Supported Data Types / Validation).
 //
 // One persistent, warp-specialised kernel per (format, layout):
-//   warp 0      TMA producer: A/B tiles (128-byte swizzle) and the tile's scale
-//               atoms (bulk copies) into a multi-stage shared-memory ring;
-//   warp 1      allocates tensor memory; lane 0 copies the stage's scale atoms into
-//               tensor memory (tcgen05.cp) and issues the block-scaled MMAs
+//   warp 0      TMA producer: A/B tiles (128-byte swizzle) into a 4-stage ring; the
+//               wide scale layouts into two small rings of their own (row-scale
+//               chunks of 2 K groups, column-scale blocks of 1 or 2 K groups);
+//   warp 1      allocates tensor memory; lane 0 copies scales into tensor memory with
+//               128-lane x 32-byte tcgen05.cp copies and issues the block-scaled MMAs
 //               (kind::mxf8f6f4 scale_vec::1X for FP8, kind::mxf4 scale_vec::2X for
 //               packed FP4) into an FP32 accumulator in tensor memory;
 //   warps 2-9   epilogue: tcgen05.ld of the accumulator, release of tensor memory to
-//               the next tile, BF16 round-to-nearest-even, 16-byte global stores.
-// Tile 128 x BN, 128 bytes of K per stage (128 FP8 / 256 FP4 values), four MMAs
-// per stage.  Every wait is bounded; a timed-out wait latches a status and every
-// role unwinds to the common teardown, which frees tensor memory.
+//               the next tile, BF16 round-to-nearest-even, streaming 16-byte stores.
+// Tile 128 x 256, 128 bytes of K per stage (128 FP8 / 256 FP4 values), four MMAs per
+// stage.  As a CTA pair (2-CTA cluster) two vertically adjacent tiles share their B
+// tile: each CTA loads half of it and multicasts it to both.  Every wait is bounded;
+// a timed-out wait latches a status and every role unwinds to the common teardown,
+// which frees tensor memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -26,38 +29,34 @@
 namespace bsmma {
 namespace {
 
-constexpr int kBM = 128;
+constexpr int kBM = 128, kBN = 256;
 constexpr int kThreads = 320;       // 10 warps
 constexpr int kEpiWarps = 8;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfaCol = 256;   // 4 slots x 8 columns
-constexpr uint32_t kSfbCol = 288;   // 4 slots x 16 columns
-constexpr uint32_t kSfSlots = 4;
+constexpr uint32_t kSfaCol = 256;   // 2 slots x 8 columns: row-scale chunks
+constexpr uint32_t kSfbCol = 288;   // 4 slots x 8 columns: column-scale blocks
 constexpr int kSmemLimit = 232448;  // 227 KB of dynamic shared memory per block
 constexpr bool kPairDefault = true;
 
-template <int BN, bool FP4>
+template <bool FP4>
 struct Cfg {
-  static constexpr int kAP = FP4 ? 2 : 1;                  // scale atoms per stage per 128 rows
+  static constexpr int kKgPerStage = FP4 ? 2 : 1;         // 4-block K groups per stage
+  static constexpr int kStagesPerChunk = 2 / kKgPerStage;  // a row-scale chunk spans 2 K groups
   static constexpr int kABytes = kBM * 128;
-  static constexpr int kBBytes = BN * 128;
-  static constexpr int kSfaBytes = kAP * 512;
-  static constexpr int kSfbBytes = (BN / 128) * kAP * 512;
-  static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-  static constexpr int kStages0 = (kSmemLimit - 2048) / kStageBytes;
-  static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
-  static constexpr int kBarBytes = 256;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  static constexpr int kBBytes = kBN * 128;
+  static constexpr int kStages = 4;
+  static constexpr int kSfaSlots = 2, kSfaSlotBytes = 4096;
+  static constexpr int kSfbSlots = 3, kSfbSlotBytes = kKgPerStage * 4096;
+  static constexpr int kSmemBytes = 1024 + kStages * (kABytes + kBBytes) +
+                                    kSfaSlots * kSfaSlotBytes + kSfbSlots * kSfbSlotBytes + 256;
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
-  static_assert(BN == 128 || BN == 256, "tile width");
 };
 
 struct DenseParams {
-  const uint8_t* sfa;   // tiled scales of op(A)
-  const uint8_t* sfb;   // tiled scales of op(B)
   __nv_bfloat16* D;
   int64_t M, N;
-  int64_t sfa_kg, sfb_kg;   // 512-byte atoms per 128-row block of each scale buffer
+  int sfa_kq;               // row-scale chunks per 128-row block
+  int sfb_kg;               // column-scale blocks per 256-column block
   int num_m_tiles, num_n_tiles, num_k_stages;
   uint32_t idesc;
   int* status;
@@ -65,10 +64,9 @@ struct DenseParams {
 };
 
 // Scheduling unit u -> output tile (mt, nt).  Single CTAs take one tile per unit;
-// a CTA pair (2-CTA cluster) takes two vertically adjacent tiles that share their
-// B tile, which each CTA loads half of and multicasts to both.  Units walk the
-// output in bands of kBandRows tile rows, along N inside a band, so that the CTAs
-// running at the same time touch a compact block of A and B that stays in L2.
+// a CTA pair takes two vertically adjacent tiles that share their B tile.  Units
+// walk the output in bands of kBandRows tile rows, along N inside a band, so that
+// the CTAs running at the same time touch a compact block of A and B that stays in L2.
 constexpr int kBandRows = 16;
 
 template <bool PAIR>
@@ -86,24 +84,45 @@ __device__ __forceinline__ void unit_tile(const DenseParams& p, int u, uint32_t 
   mt = PAIR ? ur * 2 + static_cast<int>(rank) : ur;
 }
 
+// A ring position: slot index and the parity of its current phase.
+struct Ring {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void advance(int slots) {
+    if (++slot == slots) {
+      slot = 0;
+      phase ^= 1;
+    }
+  }
+};
+
+// Copies 128 lanes x 32 bytes of shared memory into 8 tensor-memory columns.
+__device__ __forceinline__ void tc_cp_wide(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // 10 warps share an SM's four register-file quarters (16384 registers each) as
 // 3+3+2+2 warps, so a thread may hold at most 16384 / (3 * 32) = 170 registers.
-template <int BN, bool FP4, bool A_MN, bool B_MN, bool PAIR>
+template <bool FP4, bool A_MN, bool B_MN, bool PAIR>
 __global__ void __maxnreg__(168)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const DenseParams p) {
-  using C = Cfg<BN, FP4>;
-  static_assert(!PAIR || BN == 256, "a CTA pair splits a 256-wide B tile");
+                   const __grid_constant__ CUtensorMap tmSFA,
+                   const __grid_constant__ CUtensorMap tmSFB, const DenseParams p) {
+  using C = Cfg<FP4>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + C::kStages * C::kABytes;
   uint8_t* sSFA = sB + C::kStages * C::kBBytes;
-  uint8_t* sSFB = sSFA + C::kStages * C::kSfaBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + C::kStages * C::kSfbBytes);
+  uint8_t* sSFB = sSFA + C::kSfaSlots * C::kSfaSlotBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + C::kSfbSlots * C::kSfbSlotBytes);
   uint64_t* empty = full + C::kStages;
-  uint64_t* acc_full = empty + C::kStages;
+  uint64_t* sfa_full = empty + C::kStages;
+  uint64_t* sfa_empty = sfa_full + C::kSfaSlots;
+  uint64_t* sfb_full = sfa_empty + C::kSfaSlots;
+  uint64_t* sfb_empty = sfb_full + C::kSfbSlots;
+  uint64_t* acc_full = sfb_empty + C::kSfbSlots;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -117,6 +136,14 @@ __global__ void __maxnreg__(168)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], PAIR ? 2 : 1);   // a pair frees a stage only when both MMAs are done
     }
+    for (int s = 0; s < C::kSfaSlots; ++s) {
+      mbar_init(&sfa_full[s], 1);
+      mbar_init(&sfa_empty[s], 1);
+    }
+    for (int s = 0; s < C::kSfbSlots; ++s) {
+      mbar_init(&sfb_full[s], 1);
+      mbar_init(&sfb_empty[s], 1);
+    }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, kEpiWarps);
     mbar_init(drain, 1);
@@ -124,6 +151,8 @@ __global__ void __maxnreg__(168)
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    prefetch_tmap(&tmSFA);
+    prefetch_tmap(&tmSFB);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -142,57 +171,59 @@ __global__ void __maxnreg__(168)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
-      int stage = 0;
-      uint32_t phase = 0, armed = 0, armed_parity = 0;
+      Ring st, sa, sb;
+      uint32_t armed = 0, armed_parity = 0;   // data stages armed, for the drain at exit
       bool ok = true;
       for (int u = first_unit; ok && u < total_units; u += unit_stride) {
         int mt, nt;
         unit_tile<PAIR>(p, u, rank, mt, nt);
         for (int ks = 0; ks < p.num_k_stages; ++ks) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, p.limit_ns, abort_flag, p.status)) {
+          if (!mbar_wait(&empty[st.slot], st.phase ^ 1, p.limit_ns, abort_flag, p.status)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-          armed |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          uint8_t* a_dst = sA + stage * C::kABytes;
-          uint8_t* b_dst = sB + stage * C::kBBytes;
-          if (A_MN) tma_load_2d(&tmA, &full[stage], a_dst, mt * kBM, ks * 128);
-          else      tma_load_2d(&tmA, &full[stage], a_dst, ks * 128, mt * kBM);
-          bulk_load(sSFA + stage * C::kSfaBytes,
-                    p.sfa + (static_cast<int64_t>(mt) * p.sfa_kg + ks * C::kAP) * 512,
-                    C::kSfaBytes, &full[stage]);
+          mbar_arrive_expect_tx(&full[st.slot], C::kABytes + C::kBBytes);
+          armed |= 1u << st.slot;
+          armed_parity = (armed_parity & ~(1u << st.slot)) | (st.phase << st.slot);
+          uint8_t* a_dst = sA + st.slot * C::kABytes;
+          uint8_t* b_dst = sB + st.slot * C::kBBytes;
+          if (A_MN) tma_load_2d(&tmA, &full[st.slot], a_dst, mt * kBM, ks * 128);
+          else      tma_load_2d(&tmA, &full[st.slot], a_dst, ks * 128, mt * kBM);
           if (PAIR) {
-            // this CTA's 128-row half of the B tile and of its scales, to both CTAs
+            // this CTA's 128-row half of the B tile, to both CTAs
             const int r = static_cast<int>(rank);
             if (B_MN)
-              tma_load_2d_mc(&tmB, &full[stage], b_dst + r * 16384, nt * BN + r * 128, ks * 128,
-                             kPairMask);
+              tma_load_2d_mc(&tmB, &full[st.slot], b_dst + r * 16384, nt * kBN + r * 128,
+                             ks * 128, kPairMask);
             else
-              tma_load_2d_mc(&tmB, &full[stage], b_dst + r * 16384, ks * 128, nt * BN + r * 128,
-                             kPairMask);
-            bulk_load_mc(sSFB + stage * C::kSfbBytes + r * C::kAP * 512,
-                         p.sfb + ((static_cast<int64_t>(nt) * 2 + r) * p.sfb_kg + ks * C::kAP) * 512,
-                         C::kAP * 512, &full[stage], kPairMask);
+              tma_load_2d_mc(&tmB, &full[st.slot], b_dst + r * 16384, ks * 128,
+                             nt * kBN + r * 128, kPairMask);
+          } else if (B_MN) {
+            tma_load_2d(&tmB, &full[st.slot], b_dst, nt * kBN, ks * 128);
+            tma_load_2d(&tmB, &full[st.slot], b_dst + 16384, nt * kBN + 128, ks * 128);
           } else {
-            if (B_MN) {
-#pragma unroll
-              for (int j = 0; j < BN / 128; ++j)
-                tma_load_2d(&tmB, &full[stage], b_dst + j * 16384, nt * BN + j * 128, ks * 128);
-            } else {
-              tma_load_2d(&tmB, &full[stage], b_dst, ks * 128, nt * BN);
-            }
-#pragma unroll
-            for (int rb = 0; rb < BN / 128; ++rb)
-              bulk_load(sSFB + stage * C::kSfbBytes + rb * C::kAP * 512,
-                        p.sfb + ((static_cast<int64_t>(nt) * (BN / 128) + rb) * p.sfb_kg +
-                                 ks * C::kAP) * 512,
-                        C::kAP * 512, &full[stage]);
+            tma_load_2d(&tmB, &full[st.slot], b_dst, ks * 128, nt * kBN);
           }
-          if (++stage == C::kStages) {
-            stage = 0;
-            phase ^= 1;
+          st.advance(C::kStages);
+          // column scales of the stage's K groups (each block: one copy per lane quarter)
+          if (!mbar_wait(&sfb_empty[sb.slot], sb.phase ^ 1, p.limit_ns, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sfb_full[sb.slot], C::kSfbSlotBytes);
+          tma_load_2d(&tmSFB, &sfb_full[sb.slot], sSFB + sb.slot * C::kSfbSlotBytes, 0,
+                      (nt * p.sfb_kg + ks * C::kKgPerStage) * 4);
+          sb.advance(C::kSfbSlots);
+          // row scales of this CTA's 128 A rows, one chunk per two K groups
+          if (ks % C::kStagesPerChunk == 0) {
+            if (!mbar_wait(&sfa_empty[sa.slot], sa.phase ^ 1, p.limit_ns, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&sfa_full[sa.slot], C::kSfaSlotBytes);
+            tma_load_2d(&tmSFA, &sfa_full[sa.slot], sSFA + sa.slot * C::kSfaSlotBytes, 0,
+                        (mt * p.sfa_kq + ks / C::kStagesPerChunk) * 4);
+            sa.advance(C::kSfaSlots);
           }
         }
       }
@@ -202,38 +233,53 @@ __global__ void __maxnreg__(168)
           volatile int no_abort = 0;
           mbar_wait(&full[s], (armed_parity >> s) & 1u, p.limit_ns / 4 + 1, &no_abort, nullptr);
         }
+      if (!ok) {   // scale copies may still be landing after an abort: give them time
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000000ull) {
+        }
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      int stage = 0;
-      uint32_t phase = 0, kiter = 0;
+      Ring st, sa, sb;
+      uint32_t chunk = 0, kgs = 0;   // row-scale chunks and column-scale K groups consumed
       bool ok = true;
       int local = 0;
       for (int u = first_unit; ok && u < total_units; u += unit_stride, ++local) {
         if (!mbar_wait(acc_empty, (local & 1) ^ 1, p.limit_ns, abort_flag, p.status)) break;
         tc_fence_after();
         for (int ks = 0; ks < p.num_k_stages; ++ks) {
-          if (!mbar_wait(&full[stage], phase, p.limit_ns, abort_flag, p.status)) {
+          const int sub = ks % C::kStagesPerChunk;
+          const uint32_t sfa_t = tmem + kSfaCol + (chunk & 1) * 8;
+          if (sub == 0) {
+            if (!mbar_wait(&sfa_full[sa.slot], sa.phase, p.limit_ns, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            tc_cp_wide(sfa_t, make_sdesc(smem_u32(sSFA + sa.slot * C::kSfaSlotBytes), 128, 256, 0));
+            tc_commit(&sfa_empty[sa.slot]);
+            sa.advance(C::kSfaSlots);
+          }
+          if (!mbar_wait(&sfb_full[sb.slot], sb.phase, p.limit_ns, abort_flag, p.status) ||
+              !mbar_wait(&full[st.slot], st.phase, p.limit_ns, abort_flag, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t slot = kiter % kSfSlots;
-          const uint32_t sfa_t = tmem + kSfaCol + slot * 8;
-          const uint32_t sfb_t = tmem + kSfbCol + slot * 16;
-          const uint32_t sfa_s = smem_u32(sSFA + stage * C::kSfaBytes);
-          const uint32_t sfb_s = smem_u32(sSFB + stage * C::kSfbBytes);
+          uint32_t sfb_t[C::kKgPerStage];
 #pragma unroll
-          for (int a = 0; a < C::kAP; ++a) tc_cp_sf(sfa_t + a * 4, make_sdesc(sfa_s + a * 512, 0, 128, 0));
-#pragma unroll
-          for (int rb = 0; rb < BN / 128; ++rb)
-#pragma unroll
-            for (int a = 0; a < C::kAP; ++a)
-              tc_cp_sf(sfb_t + a * 8 + rb * 4,
-                       make_sdesc(sfb_s + (rb * C::kAP + a) * 512, 0, 128, 0));
-          const uint32_t a_base = smem_u32(sA + stage * C::kABytes);
-          const uint32_t b_base = smem_u32(sB + stage * C::kBBytes);
+          for (int g = 0; g < C::kKgPerStage; ++g) {
+            sfb_t[g] = tmem + kSfbCol + ((kgs + g) & 3) * 8;
+            tc_cp_wide(sfb_t[g], make_sdesc(smem_u32(sSFB + sb.slot * C::kSfbSlotBytes + g * 4096),
+                                            128, 256, 0));
+          }
+          tc_commit(&sfb_empty[sb.slot]);
+          sb.advance(C::kSfbSlots);
+          kgs += C::kKgPerStage;
+          const uint32_t a_base = smem_u32(sA + st.slot * C::kABytes);
+          const uint32_t b_base = smem_u32(sB + st.slot * C::kBBytes);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint64_t ad = A_MN ? make_sdesc(a_base + j * 4096, 16384, 1024, kSwizzle128B)
@@ -242,20 +288,18 @@ __global__ void __maxnreg__(168)
                                      : make_sdesc(b_base + j * 32, 16, 1024, kSwizzle128B);
             const uint32_t acc = (ks | j) != 0;
             if (FP4) {
-              const uint32_t atom = j >> 1, sfid = (j & 1) * 2;
-              mma_mxf4(tmem, ad, bd, p.idesc | idesc_sf_id(sfid, sfid), sfa_t + atom * 4,
-                       sfb_t + atom * 8, acc);
+              const int g = j >> 1;                      // K group within the stage
+              const uint32_t sfid = (j & 1) * 2;
+              mma_mxf4(tmem, ad, bd, p.idesc | idesc_sf_id(sfid, sfid),
+                       sfa_t + 4 * (sub * C::kKgPerStage + g), sfb_t[g], acc);
             } else {
-              mma_mxf8f6f4(tmem, ad, bd, p.idesc | idesc_sf_id(j, j), sfa_t, sfb_t, acc);
+              mma_mxf8f6f4(tmem, ad, bd, p.idesc | idesc_sf_id(j, j), sfa_t + 4 * sub, sfb_t[0], acc);
             }
           }
-          if (PAIR) tc_commit_mc(&empty[stage], kPairMask);
-          else tc_commit(&empty[stage]);
-          ++kiter;
-          if (++stage == C::kStages) {
-            stage = 0;
-            phase ^= 1;
-          }
+          if (PAIR) tc_commit_mc(&empty[st.slot], kPairMask);
+          else tc_commit(&empty[st.slot]);
+          st.advance(C::kStages);
+          if (sub == C::kStagesPerChunk - 1 || ks == p.num_k_stages - 1) ++chunk;
         }
         if (ok) tc_commit(acc_full);
       }
@@ -266,7 +310,7 @@ __global__ void __maxnreg__(168)
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    constexpr int kCols = BN / 2;          // columns per epilogue warp
+    constexpr int kCols = kBN / 2;         // columns per epilogue warp
     constexpr int kChunks = kCols / 32;
     const int q = warp & 3;                // tensor-memory lane quarter of this warp
     const int h = (warp - 2) >> 2;         // which half of the tile's columns
@@ -287,7 +331,7 @@ __global__ void __maxnreg__(168)
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty);
       const int64_t row = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
-      const int64_t col0 = static_cast<int64_t>(nt) * BN + h * kCols;
+      const int64_t col0 = static_cast<int64_t>(nt) * kBN + h * kCols;
       if (row < p.M) {
         __nv_bfloat16* out = p.D + row * p.N + col0;
 #pragma unroll
@@ -297,10 +341,10 @@ __global__ void __maxnreg__(168)
             const int o = c * 32 + v * 8;
             if (col0 + o < p.N)
               st_global_v4_cs(out + o,
-                           pack_bf16x2(__uint_as_float(r[c][v * 8 + 0]), __uint_as_float(r[c][v * 8 + 1])),
-                           pack_bf16x2(__uint_as_float(r[c][v * 8 + 2]), __uint_as_float(r[c][v * 8 + 3])),
-                           pack_bf16x2(__uint_as_float(r[c][v * 8 + 4]), __uint_as_float(r[c][v * 8 + 5])),
-                           pack_bf16x2(__uint_as_float(r[c][v * 8 + 6]), __uint_as_float(r[c][v * 8 + 7])));
+                              pack_bf16x2(__uint_as_float(r[c][v * 8 + 0]), __uint_as_float(r[c][v * 8 + 1])),
+                              pack_bf16x2(__uint_as_float(r[c][v * 8 + 2]), __uint_as_float(r[c][v * 8 + 3])),
+                              pack_bf16x2(__uint_as_float(r[c][v * 8 + 4]), __uint_as_float(r[c][v * 8 + 5])),
+                              pack_bf16x2(__uint_as_float(r[c][v * 8 + 6]), __uint_as_float(r[c][v * 8 + 7])));
           }
       }
     }
@@ -315,11 +359,12 @@ __global__ void __maxnreg__(168)
   if (PAIR) cluster_sync();
 }
 
-template <int BN, bool FP4, bool A_MN, bool B_MN, bool PAIR>
-bsmma_status launch_dense(const CUtensorMap& ta, const CUtensorMap& tb, const DenseParams& p,
-                          int sm_count, cudaStream_t stream) {
-  using C = Cfg<BN, FP4>;
-  auto kern = mx_gemm_kernel<BN, FP4, A_MN, B_MN, PAIR>;
+template <bool FP4, bool A_MN, bool B_MN, bool PAIR>
+bsmma_status launch_dense(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
+                          const CUtensorMap& tsb, const DenseParams& p, int sm_count,
+                          cudaStream_t stream) {
+  using C = Cfg<FP4>;
+  auto kern = mx_gemm_kernel<FP4, A_MN, B_MN, PAIR>;
   static int max_clusters = -1;   // benign race: every thread computes the same value
   if (max_clusters < 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
@@ -327,9 +372,6 @@ bsmma_status launch_dense(const CUtensorMap& ta, const CUtensorMap& tb, const De
       return BSMMA_ERR_CUDA;
     int n = sm_count;
     if (PAIR) {
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) !=
-          cudaSuccess)
-        return BSMMA_ERR_CUDA;
       cudaLaunchConfig_t cfg = {};
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -362,17 +404,16 @@ bsmma_status launch_dense(const CUtensorMap& ta, const CUtensorMap& tb, const De
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = PAIR ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, p);
   count_launches(1);
   return cuda_ok(e == cudaSuccess ? cudaGetLastError() : e);
 }
 
-// Which dense variant runs (see bsmma_set_dense_variant): CTA pairs or single CTAs.
+// One CTA per 128x256 tile (variant 1) or CTA pairs sharing a multicast B tile (2).
 bool use_pair(int num_m_tiles) {
   const int v = dense_variant();
   if (v == 1) return false;
-  if (v == 2) return num_m_tiles >= 1;
-  return kPairDefault && num_m_tiles >= 2;
+  return kPairDefault && num_m_tiles >= 1;
 }
 
 }  // namespace
@@ -380,57 +421,63 @@ bool use_pair(int num_m_tiles) {
 bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, const uint8_t* sfb,
                             void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
                             bsmma_fmt a_fmt, bsmma_fmt b_fmt, cudaStream_t stream) {
-  if (dense_variant() >= 3) return BSMMA_ERR_UNSUPPORTED;   // takes the wide scale layouts
+  // SM-pair MMAs unless a one-CTA variant is asked for
+  const int variant = dense_variant();
+  if (variant == 0 || variant == 3)
+    return launch_mx_gemm_2sm(A, sfa, B, sfb, D, M, N, K, layout, a_fmt, b_fmt, stream);
   bsmma_status st;
   const DeviceInfo* dev = current_device(&st);
   if (!dev) return st;
-  constexpr int BN = 256;
   const bool fp4 = (a_fmt == BSMMA_E2M1);
   const uint64_t kbytes = fp4 ? static_cast<uint64_t>(K / 2) : static_cast<uint64_t>(K);
-  CUtensorMap ta, tb;
-  if (layout == BSMMA_TN)
-    st = encode_tmap_u8(&ta, A, M, K, M, 128, 128);
-  else
-    st = encode_tmap_u8(&ta, A, kbytes, M, kbytes, 128, 128);
-  if (st != BSMMA_OK) return st;
+  const int64_t kblocks = K / 32;
+  const int64_t kq = (kblocks + 7) / 8;          // row-scale chunks per 128 rows
+  const int64_t kgp = 2 * ((kblocks + 7) / 8);   // column-scale blocks per 256 columns
   const int num_m_tiles = static_cast<int>((M + kBM - 1) / kBM);
   const bool pair = use_pair(num_m_tiles);
-  if (layout == BSMMA_NT)
-    st = encode_tmap_u8(&tb, B, kbytes, N, kbytes, 128, pair ? 128 : BN);
-  else
-    st = encode_tmap_u8(&tb, B, N, K, N, 128, 128);
+  CUtensorMap ta, tb, tsa, tsb;
+  if (layout == BSMMA_TN) st = encode_tmap_u8(&ta, A, M, K, M, 128, 128);
+  else st = encode_tmap_u8(&ta, A, kbytes, M, kbytes, 128, 128);
+  if (st != BSMMA_OK) return st;
+  if (layout == BSMMA_NT) st = encode_tmap_u8(&tb, B, kbytes, N, kbytes, 128, pair ? 128 : kBN);
+  else st = encode_tmap_u8(&tb, B, N, K, N, 128, 128);
+  if (st != BSMMA_OK) return st;
+  // both scale layouts viewed as rows of 1 KB ([*][256 words]): a row-scale chunk is 4
+  // rows, a column-scale block 4 rows (its lane-quarter copies)
+  st = encode_tmap_words(&tsa, sfa, 256, static_cast<uint64_t>(2 * ((M + 255) / 256) * kq * 4), 256, 4);
+  if (st != BSMMA_OK) return st;
+  st = encode_tmap_words(&tsb, sfb, 256, static_cast<uint64_t>(((N + 255) / 256) * kgp * 4), 256,
+                         fp4 ? 8 : 4);
   if (st != BSMMA_OK) return st;
 
   DenseParams p;
-  p.sfa = sfa;
-  p.sfb = sfb;
   p.D = static_cast<__nv_bfloat16*>(D);
   p.M = M;
   p.N = N;
-  p.sfa_kg = 2 * ((K / 32 + 7) / 8);   // block groups per row block of the tiled layout
-  p.sfb_kg = p.sfa_kg;
+  p.sfa_kq = static_cast<int>(kq);
+  p.sfb_kg = static_cast<int>(kgp);
   p.num_m_tiles = num_m_tiles;
-  p.num_n_tiles = static_cast<int>((N + BN - 1) / BN);
+  p.num_n_tiles = static_cast<int>((N + kBN - 1) / kBN);
   p.num_k_stages = static_cast<int>((static_cast<int64_t>(kbytes) + 127) / 128);
   const uint32_t af = fp4 ? 1u : static_cast<uint32_t>(a_fmt);   // kind::mxf4 codes E2M1 as 1
   const uint32_t bf = fp4 ? 1u : static_cast<uint32_t>(b_fmt);
-  p.idesc = idesc_block_scaled(af, bf, layout == BSMMA_TN, layout != BSMMA_NT, kBM, BN);
+  p.idesc = idesc_block_scaled(af, bf, layout == BSMMA_TN, layout != BSMMA_NT, kBM, kBN);
   p.status = dev->status;
   p.limit_ns = wait_limit_ns();
   const int sms = dev->sm_count;
   if (pair) {
-    if (fp4) return launch_dense<BN, true, false, false, true>(ta, tb, p, sms, stream);
+    if (fp4) return launch_dense<true, false, false, true>(ta, tb, tsa, tsb, p, sms, stream);
     switch (layout) {
-      case BSMMA_NT: return launch_dense<BN, false, false, false, true>(ta, tb, p, sms, stream);
-      case BSMMA_NN: return launch_dense<BN, false, false, true, true>(ta, tb, p, sms, stream);
-      default:       return launch_dense<BN, false, true, true, true>(ta, tb, p, sms, stream);
+      case BSMMA_NT: return launch_dense<false, false, false, true>(ta, tb, tsa, tsb, p, sms, stream);
+      case BSMMA_NN: return launch_dense<false, false, true, true>(ta, tb, tsa, tsb, p, sms, stream);
+      default:       return launch_dense<false, true, true, true>(ta, tb, tsa, tsb, p, sms, stream);
     }
   }
-  if (fp4) return launch_dense<BN, true, false, false, false>(ta, tb, p, sms, stream);
+  if (fp4) return launch_dense<true, false, false, false>(ta, tb, tsa, tsb, p, sms, stream);
   switch (layout) {
-    case BSMMA_NT: return launch_dense<BN, false, false, false, false>(ta, tb, p, sms, stream);
-    case BSMMA_NN: return launch_dense<BN, false, false, true, false>(ta, tb, p, sms, stream);
-    default:       return launch_dense<BN, false, true, true, false>(ta, tb, p, sms, stream);
+    case BSMMA_NT: return launch_dense<false, false, false, false>(ta, tb, tsa, tsb, p, sms, stream);
+    case BSMMA_NN: return launch_dense<false, false, true, false>(ta, tb, tsa, tsb, p, sms, stream);
+    default:       return launch_dense<false, true, true, false>(ta, tb, tsa, tsb, p, sms, stream);
   }
 }
 

@@ -33,10 +33,9 @@ constexpr uint32_t kSfbCol = 288;   // 4 slots x 8 columns: column-scale blocks
 constexpr int kSmemLimit = 232448;
 constexpr int kBandUnits = 8;       // unit rows (256 output rows each) per raster band
 
-// REPL: copies of a column-scale block in the copy's source (4 = one per lane quarter).
-template <bool FP4, int REPL>
+template <bool FP4>
 struct Cfg2 {
-  static constexpr int kSfbRepl = REPL;
+  static constexpr int kSfbRepl = 4;                      // one column-scale copy per lane quarter
   static constexpr int kKgPerStage = FP4 ? 2 : 1;        // 4-block K groups per 128-byte stage
   static constexpr int kStagesPerChunk = 2 / kKgPerStage; // a row-scale chunk spans 2 K groups
   static constexpr int kABytes = 128 * 128;
@@ -144,12 +143,12 @@ __device__ __forceinline__ void unit_tile2(const Pair2Params& p, int u, int& ur,
 
 // 10 warps share an SM's four register-file quarters (16384 registers each) as
 // 3+3+2+2 warps, so a thread may hold at most 16384 / (3 * 32) = 170 registers.
-template <bool FP4, bool A_MN, bool B_MN, int REPL>
+template <bool FP4, bool A_MN, bool B_MN>
 __global__ void __maxnreg__(168)
     mx_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmSFA,
                        const __grid_constant__ CUtensorMap tmSFB, const Pair2Params p) {
-  using C = Cfg2<FP4, REPL>;
+  using C = Cfg2<FP4>;
   constexpr int kSfbRepl = C::kSfbRepl;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -229,13 +228,9 @@ __global__ void __maxnreg__(168)
           else      tma_load_2d_pair(&tmA, bar, a_dst, ks * 128, mt * 128);
           if (B_MN) tma_load_2d_pair(&tmB, bar, b_dst, nb * 128, ks * 128);
           else      tma_load_2d_pair(&tmB, bar, b_dst, ks * 128, nb * 128);
-          // column scales of all 256 B rows, one copy per lane quarter
-#pragma unroll
-          for (int g = 0; g < C::kKgPerStage; ++g)
-#pragma unroll
-            for (int r = 0; r < kSfbRepl; ++r)
-              tma_load_2d_pair(&tmSFB, bar, sSFB + stage * C::kSfbBytes + (g * kSfbRepl + r) * 1024,
-                               0, nt * p.sfb_kg + ks * C::kKgPerStage + g);
+          // column scales of all 256 B rows (blocks already hold one copy per lane quarter)
+          tma_load_2d_pair(&tmSFB, bar, sSFB + stage * C::kSfbBytes, 0,
+                           (nt * p.sfb_kg + ks * C::kKgPerStage) * kSfbRepl);
           // row scales of this CTA's 128 A rows, one chunk per 4 K groups
           if (chunk_start)
             tma_load_2d_pair(&tmSFA, bar, sSFA + stage * C::kChunkBytes, 0,
@@ -367,11 +362,11 @@ __global__ void __maxnreg__(168)
   cluster_sync();
 }
 
-template <bool FP4, bool A_MN, bool B_MN, int REPL>
+template <bool FP4, bool A_MN, bool B_MN>
 bsmma_status launch_2sm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                         const CUtensorMap& tsb, const Pair2Params& p, cudaStream_t stream) {
-  using C = Cfg2<FP4, REPL>;
-  auto kern = mx_gemm_2sm_kernel<FP4, A_MN, B_MN, REPL>;
+  using C = Cfg2<FP4>;
+  auto kern = mx_gemm_2sm_kernel<FP4, A_MN, B_MN>;
   static int max_clusters = -1;   // benign race: every thread computes the same value
   if (max_clusters < 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
@@ -436,10 +431,12 @@ bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B
   if (layout == BSMMA_NT) st = encode_tmap_u8(&tb, B, kbytes, N, kbytes, 128, 128);
   else st = encode_tmap_u8(&tb, B, N, K, N, 128, 128);
   if (st != BSMMA_OK) return st;
-  // row-scale chunks as [chunks*4][256 words], column-scale blocks as [blocks][256 words]
+  // both scale layouts viewed as rows of 1 KB ([*][256 words]): a row-scale chunk is 4
+  // rows, a column-scale block 4 rows (its lane-quarter copies)
   st = encode_tmap_words(&tsa, sfa, 256, static_cast<uint64_t>(2 * ((M + 255) / 256) * kq * 4), 256, 4);
   if (st != BSMMA_OK) return st;
-  st = encode_tmap_words(&tsb, sfb, 256, static_cast<uint64_t>(((N + 255) / 256) * kgp), 256, 1);
+  st = encode_tmap_words(&tsb, sfb, 256, static_cast<uint64_t>(((N + 255) / 256) * kgp * 4), 256,
+                         fp4 ? 8 : 4);
   if (st != BSMMA_OK) return st;
   Pair2Params p;
   p.D = static_cast<__nv_bfloat16*>(D);
@@ -456,16 +453,11 @@ bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B
   p.idesc = idesc_block_scaled(af, bf, layout == BSMMA_TN, layout != BSMMA_NT, 256, 256);
   p.status = dev->status;
   p.limit_ns = wait_limit_ns();
-  if (dense_variant() == 4) {   // column scales only in lanes 0-31 (probe of the read rule)
-    if (fp4) return launch_2sm<true, false, false, 1>(ta, tb, tsa, tsb, p, stream);
-    if (layout == BSMMA_NT) return launch_2sm<false, false, false, 1>(ta, tb, tsa, tsb, p, stream);
-    return BSMMA_ERR_UNSUPPORTED;
-  }
-  if (fp4) return launch_2sm<true, false, false, 4>(ta, tb, tsa, tsb, p, stream);
+  if (fp4) return launch_2sm<true, false, false>(ta, tb, tsa, tsb, p, stream);
   switch (layout) {
-    case BSMMA_NT: return launch_2sm<false, false, false, 4>(ta, tb, tsa, tsb, p, stream);
-    case BSMMA_NN: return launch_2sm<false, false, true, 4>(ta, tb, tsa, tsb, p, stream);
-    default:       return launch_2sm<false, true, true, 4>(ta, tb, tsa, tsb, p, stream);
+    case BSMMA_NT: return launch_2sm<false, false, false>(ta, tb, tsa, tsb, p, stream);
+    case BSMMA_NN: return launch_2sm<false, false, true>(ta, tb, tsa, tsb, p, stream);
+    default:       return launch_2sm<false, true, true>(ta, tb, tsa, tsb, p, stream);
   }
 }
 

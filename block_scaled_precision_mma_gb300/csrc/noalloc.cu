@@ -56,15 +56,15 @@ bsmma_status mx_gemm_noalloc(const void* A, const uint8_t* sA, const void* B, co
   if (st != BSMMA_OK || M == 0 || N == 0) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (K == 0) return cuda_ok(cudaMemsetAsync(D, 0, static_cast<size_t>(M * N * 2), s));
-  const int64_t bytes_a = (mx_scale_tiled_bytes(M, K / 32) + 255) / 256 * 256;
-  const int64_t bytes_b = mx_scale_tiled_bytes(N, K / 32);
+  const int64_t bytes_a = (wide_scale_bytes(M, K / 32, 0) + 255) / 256 * 256;
+  const int64_t bytes_b = wide_scale_bytes(N, K / 32, 1);
   if (bytes_a + bytes_b > kNoAllocScratchBytes) return BSMMA_ERR_SCRATCH_LIMIT;
   uint8_t* scratch = nullptr;
   st = noalloc_scratch(&scratch);
   if (st != BSMMA_OK) return st;
   // every byte of both tiled buffers (padding included) is rewritten here, so the
   // previous call's contents never leak into this one
-  st = launch_relayout(sA, M, K / 32, scratch, sB, N, K / 32, scratch + bytes_a, s);
+  st = launch_wide_relayout(sA, M, scratch, sB, N, scratch + bytes_a, K / 32, s);
   if (st != BSMMA_OK) return st;
   return launch_mx_gemm(A, scratch, B, scratch + bytes_a, D, M, N, K, layout, a_fmt, b_fmt, s);
 }

@@ -61,6 +61,10 @@ typedef enum { BSMMA_NT = 0, BSMMA_NN = 1, BSMMA_TN = 2 } bsmma_layout;
 
 typedef enum { BSMMA_E4M3 = 0, BSMMA_E5M2 = 1, BSMMA_E2M1 = 2 } bsmma_fmt;
 
+/* Which operand a set of scales belongs to: the rows of op(A) (rows of D) or the
+ * rows of op(B) (columns of D).  The two sides use different tiled layouts. */
+typedef enum { BSMMA_SCALES_A = 0, BSMMA_SCALES_B = 1 } bsmma_scale_role;
+
 /*
  * mx_gemm -- dense MXFP8 / MXFP4 GEMM, D[M][N] (BF16) = op(A) . op(B)^T.
  *
@@ -77,8 +81,8 @@ typedef enum { BSMMA_E4M3 = 0, BSMMA_E5M2 = 1, BSMMA_E2M1 = 2 } bsmma_fmt;
  * bytes (NN/TN: N % 16 == 0, TN: M % 16 == 0); N % 8 == 0 (16-byte rows of D).
  * M == 0 or N == 0 is a no-op; K == 0 writes D = 0.
  *
- * The scales are first rearranged (mx_scale_relayout) into a library-owned
- * device workspace kept per (device, stream), which grows when needed: growing
+ * The scales are first rearranged (mx_scale_relayout, both roles in one launch) into
+ * a library-owned device workspace kept per (device, stream), which grows when needed: growing
  * synchronises `stream` once, and returns BSMMA_ERR_WORKSPACE if the stream is
  * being captured (call bsmma_reserve_workspace before capture).  Calls on the
  * same stream are ordered; calls on different streams use different workspaces.
@@ -89,10 +93,11 @@ bsmma_status mx_gemm(const void* A, const uint8_t* sA, const void* B, const uint
                      bsmma_fmt a_fmt, bsmma_fmt b_fmt, bsmma_stream stream);
 
 /*
- * mx_gemm_tiled -- mx_gemm with the scales already in the tensor-core atom layout
- * produced by mx_scale_relayout (sA_tiled for M rows, sB_tiled for N rows, each
- * of mx_scale_tiled_bytes(rows, K/32) bytes).  Lets callers relayout static
- * weight scales once.  One kernel launch; allocates nothing.
+ * mx_gemm_tiled -- mx_gemm with the scales already in the tiled layouts produced by
+ * mx_scale_relayout: sA_tiled with role BSMMA_SCALES_A for the M rows
+ * (mx_scale_tiled_bytes(M, K/32, BSMMA_SCALES_A) bytes), sB_tiled with role
+ * BSMMA_SCALES_B for the N rows.  Lets callers relayout static weight scales once.
+ * One kernel launch; allocates nothing.
  */
 bsmma_status mx_gemm_tiled(const void* A, const uint8_t* sA_tiled, const void* B,
                            const uint8_t* sB_tiled, void* D, int64_t M, int64_t N, int64_t K,
@@ -113,8 +118,8 @@ bsmma_status mx_gemm_tiled(const void* A, const uint8_t* sA_tiled, const void* B
  * belongs to the library; every GPU that loads the library holds that array until
  * the process exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
  *
- * Limit: mx_scale_tiled_bytes(M, K/32) rounded up to 256, plus
- * mx_scale_tiled_bytes(N, K/32), must not exceed BSMMA_NOALLOC_SCRATCH_BYTES;
+ * Limit: mx_scale_tiled_bytes(M, K/32, BSMMA_SCALES_A) rounded up to 256, plus
+ * mx_scale_tiled_bytes(N, K/32, BSMMA_SCALES_B), must not exceed BSMMA_NOALLOC_SCRATCH_BYTES;
  * larger problems return BSMMA_ERR_SCRATCH_LIMIT before any launch.
  * The first call on a device looks up the array's device address on that device
  * (cudaGetSymbolAddress) and caches it; make that first call before any stream
@@ -150,17 +155,25 @@ bsmma_status grouped_fp8_gemm(const uint8_t* A, const float* sA, const uint8_t* 
 
 /*
  * mx_scale_relayout -- rearranges plain E8M0 scales s_plain [rows][kblocks] into the
- * tensor-core block-scale layout: atoms of 128 rows x 4 K-blocks (512 bytes),
- * atom (rb, kg) at byte (rb*KG + kg)*512, row r / block k of an atom at byte
- * (r%32)*16 + (r/32)*4 + k.  Row blocks are padded to RB = 2*ceil(rows/256), block
- * groups to KG = 2*ceil(kblocks/8); padding holds 127 (the code of 1.0).
- * s_tiled must hold mx_scale_tiled_bytes(rows, kblocks) bytes.  One launch.
+ * tiled layout the GEMM kernels copy into tensor memory (128 lanes x 32 bytes per
+ * copy).  Byte (lane l, column c, byte b) of a block sits at
+ * (l/8)*256 + (c/4)*128 + (l%8)*16 + (c%4)*4 + b.
+ *   role BSMMA_SCALES_A: one 4096-byte chunk per 128 rows and 8 K-blocks, chunk
+ *     (rb, kq) at (rb*KQ + kq)*4096, RB = 2*ceil(rows/256) row blocks,
+ *     KQ = ceil(kblocks/8); lane l = row rb*128+l; column 4g + l/32 holds the row's
+ *     four scales of K group g (0, 1) of the chunk; other columns are padding.
+ *   role BSMMA_SCALES_B: one 4096-byte block per 256 rows and one K group (4
+ *     K-blocks), block (nb, kg) at (nb*KG + kg)*4096, KG = 2*ceil(kblocks/8); four
+ *     identical 1024-byte quarters in which lane i, column c holds the four scales of
+ *     row nb*256 + 32c + i.
+ * Padding holds 127 (the code of 1.0).  s_tiled must hold
+ * mx_scale_tiled_bytes(rows, kblocks, role) bytes.  One launch.
  */
 bsmma_status mx_scale_relayout(const uint8_t* s_plain, int64_t rows, int64_t kblocks,
-                               uint8_t* s_tiled, bsmma_stream stream);
+                               bsmma_scale_role role, uint8_t* s_tiled, bsmma_stream stream);
 
-/* Size in bytes of the tiled scale layout for [rows][kblocks] scales. */
-int64_t mx_scale_tiled_bytes(int64_t rows, int64_t kblocks);
+/* Size in bytes of the tiled layout of [rows][kblocks] scales of the given role. */
+int64_t mx_scale_tiled_bytes(int64_t rows, int64_t kblocks, bsmma_scale_role role);
 
 /* Grows the current (device, stream) scale workspace to at least `bytes`
  * (call before capturing mx_gemm into a CUDA graph). */
@@ -174,10 +187,10 @@ bsmma_status bsmma_device_status(bsmma_stream stream);
 bsmma_status bsmma_set_wait_limit_ns(int64_t ns);
 
 /* Selects the dense kernel variant for later mx_gemm / mx_gemm_tiled calls:
- * 0 automatic (default), 1 one CTA per 128x256 tile, 2 CTA pairs (2-CTA clusters
- * computing two vertically adjacent tiles that share one multicast B tile), 3 SM-pair
- * MMAs (2-CTA clusters issuing one 256x256 MMA over both SMs).  All variants compute
- * the same result; this is a tuning and testing control. */
+ * 0 automatic (default: SM-pair MMAs), 1 one CTA per 128x256 tile, 2 CTA pairs (2-CTA
+ * clusters computing two vertically adjacent tiles that share one multicast B tile),
+ * 3 SM-pair MMAs (2-CTA clusters issuing one 256x256 MMA over both SMs).  All
+ * variants compute the same result; this is a tuning and testing control. */
 bsmma_status bsmma_set_dense_variant(int variant);
 
 /* Selects the grouped kernel's tile width for later grouped_fp8_gemm calls: 0

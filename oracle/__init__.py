@@ -14,8 +14,10 @@ this module compiles it with gcc and exposes numpy-friendly wrappers:
 * :func:`grouped_fp8_gemm` -- grouped groupwise FP8 GEMM with per-1x128 activation
   scales in the per-group block layout and per-128x128 weight scales ("Add FlyDSL
   grouped groupwise FP8 GEMM for ROCm", introduction and the scale-layout fix).
-* :func:`scale_relayout` / :func:`scale_tiled_bytes` -- the integer permutation of
-  plain E8M0 scales into the 128x4 tensor-core atom layout.
+* :func:`wide_scale_relayout` / :func:`wide_scale_bytes` -- the integer
+  permutations (with padding) of plain E8M0 scales into the tiled layouts the GEMM
+  kernels copy into tensor memory, for the scales of op(A) (role 0) and op(B)
+  (role 1).
 * :func:`decode_table` -- the decode tables the oracle uses.
 """
 from __future__ import annotations
@@ -67,10 +69,6 @@ def bind(path: str):
     lib.oracle_mx_gemm.restype = i32
     lib.oracle_grouped_fp8_gemm.argtypes = [p, p, p, p, p, i32, i64, i64, i64, p, i64, p, i32]
     lib.oracle_grouped_fp8_gemm.restype = i32
-    lib.oracle_scale_tiled_bytes.argtypes = [i64, i64]
-    lib.oracle_scale_tiled_bytes.restype = i64
-    lib.oracle_scale_relayout.argtypes = [p, i64, i64, p]
-    lib.oracle_scale_relayout.restype = None
     lib.oracle_wide_scale_bytes.argtypes = [i64, i64, i32]
     lib.oracle_wide_scale_bytes.restype = i64
     lib.oracle_wide_scale_relayout.argtypes = [p, i64, i64, i32, p]
@@ -154,19 +152,6 @@ def grouped_fp8_gemm(X, sX, W, sW, m_sizes, N, K, rows=None, nthreads=None,
     if rc != 0:
         raise ValueError("oracle_grouped_fp8_gemm: bad arguments")
     return D
-
-
-def scale_tiled_bytes(rows: int, kblocks: int, lib=None) -> int:
-    return int(_load(lib).oracle_scale_tiled_bytes(rows, kblocks))
-
-
-def scale_relayout(s_plain: np.ndarray, lib=None) -> np.ndarray:
-    """Plain E8M0 scales [rows, kblocks] -> tensor-core atom layout (flat uint8)."""
-    s = np.ascontiguousarray(s_plain, dtype=np.uint8)
-    rows, kblocks = s.shape
-    out = np.empty(scale_tiled_bytes(rows, kblocks, lib), dtype=np.uint8)
-    _load(lib).oracle_scale_relayout(_ptr(s), rows, kblocks, _ptr(out))
-    return out
 
 
 def wide_scale_bytes(rows: int, kblocks: int, role: int, lib=None) -> int:

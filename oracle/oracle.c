@@ -31,7 +31,7 @@
  * Parity is pinned by the CPU test-suite: closed-form decode points, exact
  * rational brute force on tiny inputs, unit-scale = plain matmul, power-of-two
  * equivariance, layout equivalence, grouped = per-group dense concatenation,
- * and the scale-factor relayout round trip.
+ * and bijection / padding / hand-derived positions of the scale relayouts.
  */
 #include <math.h>
 #include <pthread.h>
@@ -280,31 +280,6 @@ int oracle_grouped_fp8_gemm(const uint8_t* X, const float* sX, const uint8_t* W,
 }
 
 /* ------------------------------------------------------------------------ */
-/* Scale-factor relayout (integer permutation).                              */
-/*                                                                           */
-/* Target: the tensor-core block-scale layout of 128-row x 4-block atoms of  */
-/* 512 bytes, atom (rb, kg) at byte (rb*KG + kg)*512, and inside an atom     */
-/* row r, block k at (r%32)*16 + (r/32)*4 + k.  Row blocks are padded to an  */
-/* even count (RB = 2*ceil(rows/256)) and block groups to an even count      */
-/* (KG = 2*ceil(kblocks/8)); padding bytes hold 127 (the E8M0 code of 1.0).  */
-/* ------------------------------------------------------------------------ */
-int64_t oracle_scale_tiled_bytes(int64_t rows, int64_t kblocks) {
-  int64_t RB = 2 * ((rows + 255) / 256), KG = 2 * ((kblocks + 7) / 8);
-  return RB * KG * 512;
-}
-
-void oracle_scale_relayout(const uint8_t* s, int64_t rows, int64_t kblocks, uint8_t* out) {
-  int64_t KG = 2 * ((kblocks + 7) / 8);
-  int64_t total = oracle_scale_tiled_bytes(rows, kblocks);
-  for (int64_t i = 0; i < total; ++i) out[i] = 127;
-  for (int64_t r = 0; r < rows; ++r)
-    for (int64_t kb = 0; kb < kblocks; ++kb) {
-      int64_t rb = r / 128, rr = r % 128, kg = kb / 4, kk = kb % 4;
-      out[(rb * KG + kg) * 512 + (rr % 32) * 16 + (rr / 32) * 4 + kk] = s[r * kblocks + kb];
-    }
-}
-
-/* ------------------------------------------------------------------------ */
 /* Wide scale layouts (integer permutations with padding), read by the      */
 /* tensor core's 128-lane x 32-byte copies.                                 */
 /*                                                                          */
@@ -317,9 +292,10 @@ void oracle_scale_relayout(const uint8_t* s, int64_t rows, int64_t kblocks, uint
 /*   row l's 4 scales of K group c/4 of the chunk when c%4 == q; every other */
 /*   column is padding.  Chunk (rb, kq) at (rb*KQ + kq)*4096,               */
 /*   RB = 2*ceil(rows/256), KQ = ceil(kblocks/8).                           */
-/* Column role (op(B) rows): 1024-byte block per 256 rows and one K group.  */
-/*   Lane i (0..31), column c holds the 4 scales of row 32c + i.            */
-/*   Block (nb, kg) at (nb*KG + kg)*1024, NB = ceil(rows/256),              */
+/* Column role (op(B) rows): 4096-byte block per 256 rows and one K group:  */
+/*   four identical 1024-byte quarters, one per lane quarter (q*1024);      */
+/*   in each, lane i (0..31), column c holds the 4 scales of row 32c + i.   */
+/*   Block (nb, kg) at (nb*KG + kg)*4096, NB = ceil(rows/256),              */
 /*   KG = 2*ceil(kblocks/8).                                                */
 /* Padding holds 127 (the E8M0 code of 1.0).                                */
 /* ------------------------------------------------------------------------ */
@@ -330,7 +306,7 @@ static int64_t lane_col_byte(int64_t l, int64_t c, int64_t b) {
 int64_t oracle_wide_scale_bytes(int64_t rows, int64_t kblocks, int role) {
   if (rows <= 0 || kblocks <= 0) return 0;
   if (role == 0) return 2 * ((rows + 255) / 256) * ((kblocks + 7) / 8) * 4096;
-  return ((rows + 255) / 256) * 2 * ((kblocks + 7) / 8) * 1024;
+  return ((rows + 255) / 256) * 2 * ((kblocks + 7) / 8) * 4096;
 }
 
 void oracle_wide_scale_relayout(const uint8_t* s, int64_t rows, int64_t kblocks, int role,
@@ -350,7 +326,9 @@ void oracle_wide_scale_relayout(const uint8_t* s, int64_t rows, int64_t kblocks,
     for (int64_t n = 0; n < rows; ++n)
       for (int64_t kb = 0; kb < kblocks; ++kb) {
         int64_t nb = n / 256, nn = n % 256, kg = kb / 4;
-        out[(nb * KG + kg) * 1024 + lane_col_byte(nn % 32, nn / 32, kb % 4)] = s[n * kblocks + kb];
+        for (int64_t q = 0; q < 4; ++q)
+          out[(nb * KG + kg) * 4096 + q * 1024 + lane_col_byte(nn % 32, nn / 32, kb % 4)] =
+              s[n * kblocks + kb];
       }
   }
 }

@@ -288,47 +288,6 @@ def pin_grouped_probes(lib=None):
 
 
 # ---------------------------------------------------------------- relayout
-def load_atom_positions():
-    """(row, kblock, byte offset) triples from the hand-derived golden fixture."""
-    out = []
-    with open(os.path.join(GOLDEN, "sf_atom_positions.txt")) as f:
-        for line in f:
-            line = line.split("#")[0].strip()
-            if line:
-                r, k, off = (int(t) for t in line.split())
-                out.append((r, k, off))
-    return out
-
-
-def pin_relayout(lib=None):
-    # sizes: row blocks padded to an even count of 128-row blocks, block groups to even
-    assert oracle.scale_tiled_bytes(1, 1, lib) == 2 * 2 * 512
-    assert oracle.scale_tiled_bytes(256, 8, lib) == 2 * 2 * 512
-    assert oracle.scale_tiled_bytes(257, 9, lib) == 4 * 4 * 512
-    rows, kblocks = 300, 11
-    RB, KG = 4, 4
-    # identify every output byte's source (row, kblock) with two passes of distinct values
-    r_ids = np.repeat((np.arange(rows) % 251)[:, None], kblocks, axis=1).astype(np.uint8)
-    k_ids = np.repeat(np.arange(kblocks)[None, :], rows, axis=0).astype(np.uint8)
-    hi = np.repeat((np.arange(rows) // 251)[:, None], kblocks, axis=1).astype(np.uint8)
-    out_r = oracle.scale_relayout(r_ids, lib)
-    out_k = oracle.scale_relayout(k_ids, lib)
-    out_h = oracle.scale_relayout(hi, lib)
-    ones = oracle.scale_relayout(np.zeros((rows, kblocks), dtype=np.uint8), lib)
-    assert out_r.size == RB * KG * 512
-    is_data = ones == 0
-    assert is_data.sum() == rows * kblocks            # every input byte appears once
-    assert np.all(ones[~is_data] == 127)              # padding holds the code of 1.0
-    src_r = out_h[is_data].astype(int) * 251 + out_r[is_data].astype(int)
-    src_k = out_k[is_data].astype(int)
-    assert len(set(zip(src_r.tolist(), src_k.tolist()))) == rows * kblocks
-    pos = {(r, k): p for r, k, p in zip(src_r.tolist(), src_k.tolist(),
-                                        np.nonzero(is_data)[0].tolist())}
-    for r, k, off in load_atom_positions():
-        rb, kg = r // 128, k // 4
-        assert pos[(r, k)] == (rb * KG + kg) * 512 + off, (r, k)
-
-
 def load_wide_positions():
     out = []
     with open(os.path.join(GOLDEN, "wide_scale_positions.txt")) as f:
@@ -344,11 +303,12 @@ def pin_wide_relayout(lib=None):
     hand-derived positions of the golden fixture."""
     assert oracle.wide_scale_bytes(1, 1, 0, lib) == 2 * 1 * 4096
     assert oracle.wide_scale_bytes(257, 9, 0, lib) == 4 * 2 * 4096
-    assert oracle.wide_scale_bytes(1, 1, 1, lib) == 1 * 2 * 1024
-    assert oracle.wide_scale_bytes(257, 9, 1, lib) == 2 * 4 * 1024
+    assert oracle.wide_scale_bytes(1, 1, 1, lib) == 1 * 2 * 4096
+    assert oracle.wide_scale_bytes(257, 9, 1, lib) == 2 * 4 * 4096
     rows, kblocks = 300, 14
     per = {0: (kblocks + 7) // 8, 1: 2 * ((kblocks + 7) // 8)}
-    size = {0: 4096, 1: 1024}
+    size = {0: 4096, 1: 4096}
+    copies = {0: 1, 1: 4}     # column-role blocks repeat each 1 KB quarter four times
     for role in (0, 1):
         r_ids = np.repeat((np.arange(rows) % 251)[:, None], kblocks, axis=1).astype(np.uint8)
         hi = np.repeat((np.arange(rows) // 251)[:, None], kblocks, axis=1).astype(np.uint8)
@@ -359,19 +319,23 @@ def pin_wide_relayout(lib=None):
         ones = oracle.wide_scale_relayout(np.zeros((rows, kblocks), dtype=np.uint8), role, lib)
         assert out_r.size == oracle.wide_scale_bytes(rows, kblocks, role, lib)
         is_data = ones == 0
-        assert is_data.sum() == rows * kblocks
+        assert is_data.sum() == rows * kblocks * copies[role]
         assert np.all(ones[~is_data] == 127)
         src = list(zip((out_h[is_data].astype(int) * 251 + out_r[is_data].astype(int)).tolist(),
                        out_k[is_data].astype(int).tolist()))
         assert len(set(src)) == rows * kblocks
-        pos = dict(zip(src, np.nonzero(is_data)[0].tolist()))
+        pos = {}
+        for key, at in zip(src, np.nonzero(is_data)[0].tolist()):
+            pos.setdefault(key, []).append(at)
+        assert all(len(v) == copies[role] for v in pos.values())
         for rl, r, k, off in load_wide_positions():
             if rl != role or r >= rows or k >= kblocks:
                 continue
             blk = (r // 128, k // 8) if role == 0 else (r // 256, k // 4)
-            assert pos[(r, k)] == (blk[0] * per[role] + blk[1]) * size[role] + off, (role, r, k)
+            base = (blk[0] * per[role] + blk[1]) * size[role] + off
+            assert sorted(pos[(r, k)]) == [base + q * 1024 for q in range(copies[role])], (role, r, k)
 
 
 ALL_PINS = [pin_decode_points, pin_decode_vs_torch, pin_dense_bruteforce, pin_dense_unit_scales,
             pin_dense_pow2, pin_dense_layouts, pin_grouped_concat, pin_grouped_g1_transpose,
-            pin_grouped_probes, pin_relayout, pin_wide_relayout]
+            pin_grouped_probes, pin_wide_relayout]

@@ -44,8 +44,8 @@ def run_dense(c: dict, tiled: bool = False, guard: bool = True):
     M, N, K = c["M"], c["N"], c["K"]
     buf, out = guarded_out(M, N) if guard else (None, None)
     if tiled:
-        tA = bs.mx_scale_relayout(sA)
-        tB = bs.mx_scale_relayout(sB)
+        tA = bs.mx_scale_relayout(sA, "A")
+        tB = bs.mx_scale_relayout(sB, "B")
         D = bs.mx_gemm_tiled(A, tA, B, tB, c["layout"], c["a_fmt"], c["b_fmt"], out=out,
                              M=M, N=N, K=K)
     else:

@@ -45,10 +45,15 @@ def test_status_strings(lib):
 
 
 def test_tiled_bytes(lib):
-    assert bs.mx_scale_tiled_bytes(256, 8) == 2048
-    assert bs.mx_scale_tiled_bytes(257, 9) == 8192
-    assert bs.mx_scale_tiled_bytes(8192, 256) == 8192 // 128 * 256 // 4 * 512
-    assert bs.mx_scale_tiled_bytes(0, 8) == 0
+    # A side: 4 KB per 128 rows (row blocks padded to an even count) x 8 K-blocks
+    assert bs.mx_scale_tiled_bytes(256, 8, "A") == 2 * 1 * 4096
+    assert bs.mx_scale_tiled_bytes(257, 9, "A") == 4 * 2 * 4096
+    assert bs.mx_scale_tiled_bytes(8192, 256, "A") == 64 * 32 * 4096
+    # B side: 4 KB per 256 rows x 4 K-blocks (K groups padded to an even count)
+    assert bs.mx_scale_tiled_bytes(256, 8, "B") == 1 * 2 * 4096
+    assert bs.mx_scale_tiled_bytes(257, 9, "B") == 2 * 4 * 4096
+    assert bs.mx_scale_tiled_bytes(0, 8, "A") == 0
+    assert lib.mx_scale_tiled_bytes(256, 8, 2) == 0        # no such role
 
 
 FAKE = 0x10000          # never dereferenced: every case fails validation first
@@ -94,9 +99,10 @@ def test_grouped_validation(lib, args, expect):
 
 
 def test_relayout_validation(lib):
-    assert lib.mx_scale_relayout(FAKE, -1, 8, FAKE, None) == 1
-    assert lib.mx_scale_relayout(FAKE, 128, 8, ODD, None) == 3
-    assert lib.mx_scale_relayout(None, 0, 8, None, None) == 0
+    assert lib.mx_scale_relayout(FAKE, -1, 8, 0, FAKE, None) == 1
+    assert lib.mx_scale_relayout(FAKE, 128, 8, 2, FAKE, None) == 1      # bad role
+    assert lib.mx_scale_relayout(FAKE, 128, 8, 1, ODD, None) == 3
+    assert lib.mx_scale_relayout(None, 0, 8, 0, None, None) == 0
 
 
 def test_wait_limit(lib):

@@ -17,13 +17,14 @@ def _lib():
     torch.cuda.init()
 
 
+@pytest.mark.parametrize("role", ["A", "B"])
 @pytest.mark.parametrize("rows,kblocks", [(1, 1), (128, 4), (300, 11), (8192, 256),
                                           (14336, 448), (129, 9), (4096, 128)])
-def test_relayout_bit_exact(rows, kblocks):
+def test_relayout_bit_exact(rows, kblocks, role):
     s = np.random.default_rng([3, rows, kblocks]).integers(0, 255, size=(rows, kblocks),
                                                            dtype=np.uint8)
-    got = bs.mx_scale_relayout(to_dev(s)).cpu().numpy()
-    assert np.array_equal(got, oracle.scale_relayout(s))
+    got = bs.mx_scale_relayout(to_dev(s), role).cpu().numpy()
+    assert np.array_equal(got, oracle.wide_scale_relayout(s, bs.ROLES[role]))
 
 
 def test_wait_timeout_is_reported_and_context_survives():
@@ -38,6 +39,6 @@ def test_wait_timeout_is_reported_and_context_survives():
 def test_launch_count_increments():
     n0 = bs.launch_count()
     s = torch.zeros((256, 8), dtype=torch.uint8, device="cuda")
-    bs.mx_scale_relayout(s)
+    bs.mx_scale_relayout(s, "A")
     torch.cuda.synchronize()
     assert bs.launch_count() == n0 + 1

@@ -26,12 +26,11 @@ MUTANTS = [
      "sW[((int64_t)g * (j->N / 128) + n / 128) * j->KB + kb]",
      "sW[((int64_t)g * (j->N / 128)) * j->KB + kb]"),
     ("grouped_block_boundary", "k < kb * 128 + 128", "k < kb * 128 + 64"),
-    ("relayout_line_order", "(rr % 32) * 16 + (rr / 32) * 4 + kk", "(rr / 4) * 16 + (rr % 4) * 4 + kk"),
-    ("relayout_atom_order", "(rb * KG + kg) * 512", "(kg * 2 + rb) * 512"),
     ("wide_half_order", "(l / 8) * 256 + (c / 4) * 128", "(l / 8) * 256 + (c % 2) * 128"),
     ("wide_row_quarter", "int64_t c = 4 * g + l / 32;", "int64_t c = 4 * g + l % 4;"),
     ("wide_chunk_kgroups", "kq = kg / 2, g = kg % 2", "kq = kg / 4, g = kg % 2"),
     ("wide_col_lane", "lane_col_byte(nn % 32, nn / 32, kb % 4)", "lane_col_byte(nn / 8, nn % 8, kb % 4)"),
+    ("wide_col_one_quarter", "for (int64_t q = 0; q < 4; ++q)", "for (int64_t q = 0; q < 1; ++q)"),
 ]
 
 

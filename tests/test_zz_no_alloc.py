@@ -55,7 +55,8 @@ def test_noalloc_rejects_problems_beyond_its_scratch(lib):
     """Checked on the host before anything touches the device."""
     M = N = 65536
     K = 16384
-    assert bs.mx_scale_tiled_bytes(M, K // 32) * 2 > SCRATCH_BYTES
+    assert bs.mx_scale_tiled_bytes(M, K // 32, "A") + bs.mx_scale_tiled_bytes(N, K // 32, "B") \
+        > SCRATCH_BYTES
     fake = 0x10000     # never dereferenced: the size check comes first
     assert lib.mx_gemm_noalloc(fake, fake, fake, fake, fake, M, N, K, 0, 0, 0, None) == SCRATCH_LIMIT
     assert bs.status_string(SCRATCH_LIMIT) == "BSMMA_ERR_SCRATCH_LIMIT"

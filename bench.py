@@ -359,7 +359,10 @@ def run_ours(args):
     achieved = flops_of(dom_g) / (per_gemm_ms[dom] * 1e-3) / 1e12
     step_achieved = step_flops / (gemm_step_ms * 1e-3) / 1e12
     value = ws * step_flops / (ms_per_step * 1e-3) / 1e12
-    kernel = "grouped_fp8_kernel" if args.workload == "grouped_fp8" else "mx_gemm_kernel"
+    if args.workload == "grouped_fp8":
+        kernel = "grouped_fp8_kernel"
+    else:
+        kernel = "mx_gemm_2sm_kernel" if args.dense_variant in (0, 3) else "mx_gemm_kernel"
     line = {
         "metric": METRIC,
         "value": round(value, 2),

@@ -66,7 +66,10 @@ __global__ void __launch_bounds__(128, 1) probe(int mode, int iters, int* status
 }
 
 // Pair probe: cta_group::2 MMAs over a 2-CTA cluster (256-row A split across the pair).
-// mode: 0 mxf8f6f4 256x256x32 ; 1 + 3 cp.cta_group::2 per 4 MMAs ; 2 f8f6f4 256x256x32 ; 3 mxf4 256x256x64
+// mode: 0 mxf8f6f4 256x256x32 ; 1 + 3 cp.cta_group::2 per 4 MMAs ; 2 f8f6f4 256x256x32 ; 3 mxf4 256x256x64 ;
+//       4 mxf8f6f4 with the dense kernel's scale addresses and copies (one 128x256b copy of
+//         column scales per 4 MMAs, one of row scales per 8) ; 5 the same addresses, no copies ;
+//       6 mxf4 with the dense kernel's copies (two column-scale copies and one row-scale copy per 4 MMAs)
 __global__ void __launch_bounds__(128, 1) probe2(int mode, int iters, int* status, unsigned long long* cycles) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -88,7 +91,7 @@ __global__ void __launch_bounds__(128, 1) probe2(int mode, int iters, int* statu
   tc_fence_before(); __syncthreads(); cluster_sync(); tc_fence_after();
   const uint32_t tmem = tslot;
   if (threadIdx.x == 0 && rank == 0) {
-    const bool fp4 = mode == 3;
+    const bool fp4 = mode == 3 || mode == 6;
     uint32_t idesc = (mode == 2) ? idesc_f8f6f4(0, 0, 0, 0, 256, 256)
                    : idesc_block_scaled(fp4 ? 1 : 0, fp4 ? 1 : 0, 0, 0, 256, 256);
     const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB), s0 = smem_u32(sSF);
@@ -97,12 +100,30 @@ __global__ void __launch_bounds__(128, 1) probe2(int mode, int iters, int* statu
       if (mode == 1)
         for (int c = 0; c < 3; ++c)
           asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(tmem + 256 + (it & 3) * 16 + c * 4), "l"(make_sdesc(s0 + c * 512, 0, 128, 0)) : "memory");
+      // the dense kernel's layout: row-scale chunks in columns 256-271 (two slots of 8),
+      // column-scale blocks in columns 288-319 (four slots of 8)
+      const int kgs = (mode == 6) ? 2 : 1;                 // column-scale blocks per 4 MMAs
+      const int spc = (mode == 6) ? 1 : 2;                 // iterations per row-scale chunk
+      const uint32_t sfa_t = tmem + 256 + ((it / spc) & 1) * 8;
+      const int sub = it % spc;
+      if ((mode == 4 || mode == 6) && sub == 0)
+        asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(sfa_t), "l"(make_sdesc(s0, 128, 256, 0)) : "memory");
+      uint32_t sfb_t[2];
+      for (int g = 0; g < kgs; ++g) {
+        sfb_t[g] = tmem + 288 + ((it * kgs + g) & 3) * 8;
+        if (mode == 4 || mode == 6)
+          asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(sfb_t[g]), "l"(make_sdesc(s0, 128, 256, 0)) : "memory");
+      }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const uint64_t ad = make_sdesc(a0 + j * 32, 16, 1024, kSwizzle128B);
         const uint64_t bd = make_sdesc(b0 + j * 32, 16, 1024, kSwizzle128B);
         if (mode == 2)
           asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem), "l"(ad), "l"(bd), "r"(idesc), "r"(1) : "memory");
+        else if (mode == 6)
+          asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}\n" ::"r"(tmem), "l"(ad), "l"(bd), "r"(idesc | idesc_sf_id((j & 1) * 2, (j & 1) * 2)), "r"(1), "r"(sfa_t + 4 * (j >> 1)), "r"(sfb_t[j >> 1]) : "memory");
+        else if (mode == 4 || mode == 5)
+          asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}\n" ::"r"(tmem), "l"(ad), "l"(bd), "r"(idesc | idesc_sf_id(j, j)), "r"(1), "r"(sfa_t + 4 * sub), "r"(sfb_t[0]) : "memory");
         else if (fp4)
           asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}\n" ::"r"(tmem), "l"(ad), "l"(bd), "r"(idesc | idesc_sf_id((j & 1) * 2, (j & 1) * 2)), "r"(1), "r"(tmem + 256), "r"(tmem + 288) : "memory");
         else
@@ -150,9 +171,11 @@ int main() {
            names[mode], (int)err, st, (double)c / (4.0 * iters), macs / (double)c, 2 * macs * sms / (ms * 1e-3) / 1e12);
   }
   const char* names2[] = {"pair mxf8f6f4 256x256x32", "pair mxf8f6f4 + 3 cp.cta_group::2/4 MMA",
-                          "pair f8f6f4 256x256x32", "pair mxf4 256x256x64"};
+                          "pair f8f6f4 256x256x32", "pair mxf4 256x256x64",
+                          "pair mxf8f6f4 + kernel's 128x256b copies", "pair mxf8f6f4 kernel addresses",
+                          "pair mxf4 + kernel's 128x256b copies"};
   cudaFuncSetAttribute(probe2, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  for (int mode = 0; mode < 4; ++mode) {
+  for (int mode = 0; mode < 7; ++mode) {
     const int iters = 4096;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -169,7 +192,7 @@ int main() {
     float ms; cudaEventElapsedTime(&ms, e0, e1);
     unsigned long long c; cudaMemcpy(&c, cyc, 8, cudaMemcpyDeviceToHost);
     int st; cudaMemcpy(&st, status, 4, cudaMemcpyDeviceToHost);
-    const double k = (mode == 3) ? 64 : 32;
+    const double k = (mode == 3 || mode == 6) ? 64 : 32;
     const double macs = 256.0 * 256 * k * 4 * iters;   // per pair
     printf("%-40s err=%d status=%d  %.1f cycles/MMA  %.0f MAC/clk/SM  %.1f TFLOPS (all SMs, event)\n",
            names2[mode], (int)err, st, (double)c / (4.0 * iters), macs / 2 / (double)c,

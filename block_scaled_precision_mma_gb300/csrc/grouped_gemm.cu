@@ -17,7 +17,8 @@
 //   warp 1      lane 0 issues kind::f8f6f4 MMAs: each 128-K block goes into a fresh
 //               FP32 partial in tensor memory (two partial slots, so the MMA of block
 //               kb+1 overlaps the fold of block kb);
-//   warps 2-9   fold: acc += sX(row,kb) * sW(g,nblk,kb) * partial in FP32 registers,
+//   warps 2-9   fold: acc += sX(row,kb) * sW(g,nblk,kb) * partial in FP32 registers
+//               (packed two-lane FMAs; scales copied four blocks ahead into shared memory),
 //               then BF16 round-to-nearest-even and masked 16-byte stores.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -44,7 +45,10 @@ struct GCfg {
   static constexpr int kStages = BN == 128 ? 6 : 4;
   static constexpr int kSlots = 512 / BN;         // partial slots in tensor memory (4 or 2)
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 2048;
+  static constexpr int kScaleAhead = 4;           // 128-K blocks of scales in flight per fold thread
+  static constexpr int kScaleSlots = kScaleAhead + 1;
+  static constexpr int kScaleRingBytes = kScaleSlots * 2 * kEpiWarps * 32 * 4;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 2048 + kScaleRingBytes;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -98,6 +102,9 @@ __global__ void __maxnreg__(168)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   GroupTable& gt = *reinterpret_cast<GroupTable*>(
       reinterpret_cast<uint8_t*>(full) + 512);
+  // fold scales: [kScaleSlots][sX, sW][fold thread], filled by each fold thread's own
+  // asynchronous copies
+  float* scale_ring = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 2048);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G;
@@ -235,29 +242,38 @@ __global__ void __maxnreg__(168)
       // takes part in the partial-slot handshake)
       const bool warp_rows = static_cast<int64_t>(mt - gt.tile_start[g]) * kBM + q * 32 < m_g;
       const float* sx = p.sX + gt.start[g] * KB + l;   // + kb * m_g
-      // weight scales of the 128-column block(s) of this warp's columns
+      // weight scale of the 128-column block of this warp's columns
+      static_assert(kCols <= 128, "a fold warp's columns lie in one 128-column scale block");
       const float* sw = p.sW + (static_cast<int64_t>(g) * (p.N / 128) +
-                                static_cast<int64_t>(nt) * (BN / 128)) * KB;
-      constexpr int kSwPerWarp = kCols >= 128 ? kCols / 128 : 1;   // 128-col blocks per warp
-      const int sw_blk0 = (h * kCols) / 128;
-      float acc[kCols];
+                                static_cast<int64_t>(nt) * (BN / 128) + (h * kCols) / 128) * KB;
+      // FP32 accumulators in pairs: one packed two-lane FMA (fma.rn.f32x2) per pair,
+      // rounding each lane exactly as a scalar fmaf would
+      float2 acc[kCols / 2];
 #pragma unroll
-      for (int i = 0; i < kCols; ++i) acc[i] = 0.f;
-      // scales for block kb are loaded one block ahead of their use
-      float sx_next = valid ? __ldg(sx) : 0.f;
-      float sw_next[kSwPerWarp];
-#pragma unroll
-      for (int b = 0; b < kSwPerWarp; ++b) sw_next[b] = __ldg(sw + (sw_blk0 + b) * KB);
-      for (int kb = 0; kb < KB; ++kb) {
-        const float sx_cur = sx_next;
-        float sw_cur[kSwPerWarp];
-#pragma unroll
-        for (int b = 0; b < kSwPerWarp; ++b) sw_cur[b] = sw_next[b];
-        if (kb + 1 < KB) {
-          sx_next = valid ? __ldg(sx + (kb + 1) * m_g) : 0.f;
-#pragma unroll
-          for (int b = 0; b < kSwPerWarp; ++b) sw_next[b] = __ldg(sw + (sw_blk0 + b) * KB + kb + 1);
+      for (int i = 0; i < kCols / 2; ++i) acc[i] = make_float2(0.f, 0.f);
+      // The scales of block kb are copied kScaleAhead blocks ahead of their use, one
+      // commit group per block (empty past the last block), so that with all but the
+      // newest kScaleAhead - 1 groups complete block kb has landed.  Block kb+kScaleAhead
+      // goes to the slot read in the previous iteration, never the one being read.
+      constexpr int kFoldThreads = kEpiWarps * 32;
+      float* ring = scale_ring + (threadIdx.x - 64);
+      auto fetch = [&](int kb) {
+        if (kb < KB) {
+          float* dst = ring + (kb % C::kScaleSlots) * 2 * kFoldThreads;
+          cp_async_4(dst, valid ? static_cast<const void*>(sx + static_cast<int64_t>(kb) * m_g)
+                                : static_cast<const void*>(p.sX),
+                     valid ? 4u : 0u);
+          cp_async_4(dst + kFoldThreads, sw + kb, 4u);
         }
+        cp_async_commit();
+      };
+#pragma unroll
+      for (int d = 0; d < C::kScaleAhead; ++d) fetch(d);
+      for (int kb = 0; kb < KB; ++kb) {
+        cp_async_wait<C::kScaleAhead - 1>();
+        const float* cur = ring + (kb % C::kScaleSlots) * 2 * kFoldThreads;
+        const float s = cur[0] * cur[kFoldThreads];
+        fetch(kb + C::kScaleAhead);
         const uint32_t slot = pcount % kSlots;
         if (!mbar_wait(&p_full[slot], (pcount / kSlots) & 1, p.limit_ns, abort_flag, p.status)) {
           ok = false;
@@ -273,8 +289,9 @@ __global__ void __maxnreg__(168)
           ++pcount;
           continue;
         }
-        if (kCols == 64) {
-          // the whole 64-column slice in one round trip
+        const float2 s2 = make_float2(s, s);
+        if constexpr (kCols == 64) {
+          // the whole 64-column slice in one round trip; the slot is released before the FMAs
           uint32_t r0[32], r1[32];
           tmem_ld32(taddr, r0);
           tmem_ld32(taddr + 32, r1);
@@ -283,26 +300,29 @@ __global__ void __maxnreg__(168)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&p_empty[slot]);
-          const float s = sx_cur * sw_cur[0];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[i] = fmaf(s, __uint_as_float(r0[i]), acc[i]);
+          for (int i = 0; i < 16; ++i)
+            acc[i] = __ffma2_rn(s2, make_float2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1])), acc[i]);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[32 + i] = fmaf(s, __uint_as_float(r1[i]), acc[32 + i]);
-          ++pcount;
-          continue;
+          for (int i = 0; i < 16; ++i)
+            acc[16 + i] = __ffma2_rn(s2, make_float2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])),
+                                     acc[16 + i]);
+        } else {
+          // 128 columns in sixteen-column pieces (the registers hold the accumulators)
+#pragma unroll
+          for (int c = 0; c < kCols / 16; ++c) {
+            uint32_t r[16];
+            tmem_ld16(taddr + c * 16, r);
+            tmem_ld_wait16(r);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              acc[c * 8 + i] = __ffma2_rn(s2, make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                                          acc[c * 8 + i]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&p_empty[slot]);
         }
-#pragma unroll
-        for (int c = 0; c < kCols / 16; ++c) {
-          uint32_t r[16];
-          tmem_ld16(taddr + c * 16, r);
-          tmem_ld_wait16(r);
-          const float s = sx_cur * sw_cur[(c * 16) / 128];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(s, __uint_as_float(r[i]), acc[c * 16 + i]);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_empty[slot]);
         ++pcount;
       }
       if (!ok) break;
@@ -311,12 +331,13 @@ __global__ void __maxnreg__(168)
         __nv_bfloat16* out = p.D + row * p.N + static_cast<int64_t>(nt) * BN + h * kCols;
 #pragma unroll
         for (int v = 0; v < kCols / 8; ++v)
-          st_global_v4_cs(out + v * 8, pack_bf16x2(acc[v * 8 + 0], acc[v * 8 + 1]),
-                       pack_bf16x2(acc[v * 8 + 2], acc[v * 8 + 3]),
-                       pack_bf16x2(acc[v * 8 + 4], acc[v * 8 + 5]),
-                       pack_bf16x2(acc[v * 8 + 6], acc[v * 8 + 7]));
+          st_global_v4_cs(out + v * 8, pack_bf16x2(acc[v * 4 + 0].x, acc[v * 4 + 0].y),
+                          pack_bf16x2(acc[v * 4 + 1].x, acc[v * 4 + 1].y),
+                          pack_bf16x2(acc[v * 4 + 2].x, acc[v * 4 + 2].y),
+                          pack_bf16x2(acc[v * 4 + 3].x, acc[v * 4 + 3].y));
       }
     }
+    cp_async_wait_all();   // no scale copy may land after the block has finished
   }
   __syncthreads();
   if (warp == 1) {

@@ -78,6 +78,16 @@ def test_grouped_random_small(sizes, gwidth):
     assert_close(got, ref, f"grouped {sizes}")
 
 
+@pytest.mark.parametrize("K", [128, 1280], ids=["one_kblock", "ring_wraps"])
+def test_grouped_k_extent(K, gwidth):
+    """One 128-K block, and more 128-K blocks than the fold's scale ring holds."""
+    ms = np.array([5, 0, 140, 1, 0, 33, 0, 100], dtype=np.int64)
+    c = synthetic.grouped_operands((40, 90 + K), ms, 512, K)
+    got = run_grouped(c)
+    ref = oracle.grouped_fp8_gemm(c["X"], c["sX"], c["W"], c["sW"], ms, 512, K)
+    assert_close(got, ref, f"grouped K={K}")
+
+
 def test_grouped_many_tiles(gwidth):
     """More tiles than SMs so every CTA loops, with uneven and empty groups."""
     ms = synthetic.gen_m_sizes(2000, 3)

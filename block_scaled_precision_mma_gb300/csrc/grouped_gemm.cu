@@ -257,23 +257,32 @@ __global__ void __maxnreg__(168)
       // goes to the slot read in the previous iteration, never the one being read.
       constexpr int kFoldThreads = kEpiWarps * 32;
       float* ring = scale_ring + (threadIdx.x - 64);
-      auto fetch = [&](int kb) {
-        if (kb < KB) {
-          float* dst = ring + (kb % C::kScaleSlots) * 2 * kFoldThreads;
-          cp_async_4(dst, valid ? static_cast<const void*>(sx + static_cast<int64_t>(kb) * m_g)
-                                : static_cast<const void*>(p.sX),
-                     valid ? 4u : 0u);
-          cp_async_4(dst + kFoldThreads, sw + kb, 4u);
+      // streaming source pointers: row scale of block kb at sx + kb*m_g (not read for rows
+      // past the group's end), weight scale at sw + kb
+      const float* sx_next = valid ? sx : p.sX;
+      const int64_t sx_step = valid ? m_g : 0;
+      const float* sw_next = sw;
+      int fetched = 0;
+      auto fetch = [&]() {
+        if (fetched < KB) {
+          float* dst = ring + (fetched % C::kScaleSlots) * 2 * kFoldThreads;
+          cp_async_4(dst, sx_next, valid ? 4u : 0u);
+          cp_async_4(dst + kFoldThreads, sw_next, 4u);
+          sx_next += sx_step;
+          ++sw_next;
         }
+        ++fetched;
         cp_async_commit();
       };
 #pragma unroll
-      for (int d = 0; d < C::kScaleAhead; ++d) fetch(d);
+      for (int d = 0; d < C::kScaleAhead; ++d) fetch();
+      int rd = 0;   // ring slot of block kb
       for (int kb = 0; kb < KB; ++kb) {
         cp_async_wait<C::kScaleAhead - 1>();
-        const float* cur = ring + (kb % C::kScaleSlots) * 2 * kFoldThreads;
+        const float* cur = ring + rd * 2 * kFoldThreads;
+        rd = rd + 1 == C::kScaleSlots ? 0 : rd + 1;
         const float s = cur[0] * cur[kFoldThreads];
-        fetch(kb + C::kScaleAhead);
+        fetch();
         const uint32_t slot = pcount % kSlots;
         if (!mbar_wait(&p_full[slot], (pcount / kSlots) & 1, p.limit_ns, abort_flag, p.status)) {
           ok = false;
@@ -308,16 +317,27 @@ __global__ void __maxnreg__(168)
             acc[16 + i] = __ffma2_rn(s2, make_float2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])),
                                      acc[16 + i]);
         } else {
-          // 128 columns in sixteen-column pieces (the registers hold the accumulators)
+          // 128 columns in sixteen-column pieces, software-pipelined: the load of piece
+          // c+1 is in flight while piece c is folded (one wait covers both)
+          uint32_t ra[16], rb[16];
+          tmem_ld16(taddr, ra);
+          tmem_ld_wait16(ra);
 #pragma unroll
-          for (int c = 0; c < kCols / 16; ++c) {
-            uint32_t r[16];
-            tmem_ld16(taddr + c * 16, r);
-            tmem_ld_wait16(r);
+          for (int c = 0; c < kCols / 16; c += 2) {
+            if (c + 1 < kCols / 16) tmem_ld16(taddr + (c + 1) * 16, rb);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              acc[c * 8 + i] = __ffma2_rn(s2, make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+              acc[c * 8 + i] = __ffma2_rn(s2, make_float2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1])),
                                           acc[c * 8 + i]);
+            if (c + 1 < kCols / 16) {
+              tmem_ld_wait16(rb);
+              if (c + 2 < kCols / 16) tmem_ld16(taddr + (c + 2) * 16, ra);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                acc[(c + 1) * 8 + i] = __ffma2_rn(s2, make_float2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1])),
+                                                  acc[(c + 1) * 8 + i]);
+              if (c + 2 < kCols / 16) tmem_ld_wait16(ra);
+            }
           }
           tc_fence_before();
           __syncwarp();

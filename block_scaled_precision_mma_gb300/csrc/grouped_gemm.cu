@@ -17,7 +17,8 @@
 //   warp 1      lane 0 issues kind::f8f6f4 MMAs: each 128-K block goes into a fresh
 //               FP32 partial in tensor memory (two partial slots, so the MMA of block
 //               kb+1 overlaps the fold of block kb);
-//   warps 2-9   fold: acc += sX(row,kb) * sW(g,nblk,kb) * partial in FP32 registers
+//   warps 2-3   idle (with warps 0-1 they form warpgroup 0, whose registers go to the fold)
+//   warps 4-11  fold: acc += sX(row,kb) * sW(g,nblk,kb) * partial in FP32 registers
 //               (packed two-lane FMAs; scales copied four blocks ahead into shared memory),
 //               then BF16 round-to-nearest-even and masked 16-byte stores.
 #include <cuda.h>
@@ -38,8 +39,12 @@ constexpr int kATileBytes = kBM * kBK;
 template <int BN>
 struct GCfg {
   static constexpr int kEpiWarps = 8;
+  static constexpr int kFoldWarp0 = 4;        // warpgroup 0: producer, MMA issuer, two idle warps
   static constexpr int kCols = BN / 2;        // accumulator columns per fold warp
-  static constexpr int kThreads = (2 + kEpiWarps) * 32;
+  static constexpr int kThreads = (kFoldWarp0 + kEpiWarps) * 32;
+  // Registers: 384 threads launch with 168 each; warpgroup 0 then gives back down to 40
+  // and the two fold warpgroups grow to 232 (128 x 40 + 256 x 232 = 384 x 168).
+  static constexpr int kLaunchRegs = 168, kCtrlRegs = 40, kFoldRegs = 232;
   static constexpr int kBTileBytes = BN * kBK;
   static constexpr int kStageBytes = kATileBytes + kBTileBytes;
   static constexpr int kStages = BN == 128 ? 6 : 4;
@@ -50,6 +55,7 @@ struct GCfg {
   static constexpr int kScaleRingBytes = kScaleSlots * 2 * kEpiWarps * 32 * 4;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 2048 + kScaleRingBytes;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(128 * kCtrlRegs + 256 * kFoldRegs <= kThreads * kLaunchRegs, "register split");
 };
 
 struct GroupedParams {
@@ -79,10 +85,11 @@ __device__ __forceinline__ int find_group(const GroupTable& gt, int G, int mt) {
   return g;
 }
 
-// 10 warps share an SM's four register-file quarters (16384 registers each) as
-// 3+3+2+2 warps, so a thread may hold at most 16384 / (3 * 32) = 170 registers.
+// 12 warps (three warpgroups) share an SM's four register-file quarters (16384
+// registers each) three to a quarter, so a thread launches with at most
+// 16384 / (3 * 32) = 170 registers (168 allocated); the warpgroups then rebalance.
 template <int BN>
-__global__ void __maxnreg__(168)
+__global__ void __launch_bounds__(384, 1)
     grouped_fp8_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                        const GroupedParams p) {
   using C = GCfg<BN>;
@@ -156,80 +163,93 @@ __global__ void __maxnreg__(168)
   const int NT = p.num_n_tiles, KB = p.num_kb;
   const int total_tiles = gt.tile_start[G] * NT;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ producer
-      int stage = 0;
-      uint32_t phase = 0, armed = 0, armed_parity = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-        const int mt = t / NT, nt = t - (t / NT) * NT;
-        const int g = find_group(gt, G, mt);
-        const int row0 = static_cast<int>(gt.start[g] + static_cast<int64_t>(mt - gt.tile_start[g]) * kBM);
-        const int wrow0 = static_cast<int>(static_cast<int64_t>(g) * p.N + static_cast<int64_t>(nt) * BN);
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, p.limit_ns, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&full[stage], kStageBytes);
-          armed |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          uint8_t* dst = ring + stage * kStageBytes;
-          tma_load_2d(&tmX, &full[stage], dst, kb * kBK, row0);
-          tma_load_2d(&tmW, &full[stage], dst + kATileBytes, kb * kBK, wrow0);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
+  if (warp < C::kFoldWarp0) {
+    setmaxnreg_dec<C::kCtrlRegs>();
+    if (warp == 0) {
+      if (lane == 0) {
+        // ------------------------------------------------------------ producer
+        int stage = 0;
+        uint32_t phase = 0, armed = 0, armed_parity = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+          const int mt = t / NT, nt = t - (t / NT) * NT;
+          const int g = find_group(gt, G, mt);
+          const int row0 = static_cast<int>(gt.start[g] + static_cast<int64_t>(mt - gt.tile_start[g]) * kBM);
+          const int wrow0 = static_cast<int>(static_cast<int64_t>(g) * p.N + static_cast<int64_t>(nt) * BN);
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1, p.limit_ns, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[stage], kStageBytes);
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+            uint8_t* dst = ring + stage * kStageBytes;
+            tma_load_2d(&tmX, &full[stage], dst, kb * kBK, row0);
+            tma_load_2d(&tmW, &full[stage], dst + kATileBytes, kb * kBK, wrow0);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
         }
+        for (int s = 0; s < kStages; ++s)
+          if (armed & (1u << s)) {
+            volatile int no_abort = 0;
+            mbar_wait(&full[s], (armed_parity >> s) & 1u, p.limit_ns / 4 + 1, &no_abort, nullptr);
+          }
       }
-      for (int s = 0; s < kStages; ++s)
-        if (armed & (1u << s)) {
-          volatile int no_abort = 0;
-          mbar_wait(&full[s], (armed_parity >> s) & 1u, p.limit_ns / 4 + 1, &no_abort, nullptr);
-        }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
-      int stage = 0;
-      uint32_t phase = 0, pcount = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-        for (int kb = 0; kb < KB; ++kb) {
-          const uint32_t slot = pcount % kSlots;
-          if (!mbar_wait(&full[stage], phase, p.limit_ns, abort_flag, p.status) ||
-              !mbar_wait(&p_empty[slot], ((pcount / kSlots) & 1) ^ 1, p.limit_ns, abort_flag,
-                         p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_base = smem_u32(ring + stage * kStageBytes);
-          const uint32_t b_base = a_base + kATileBytes;
+    } else if (warp == 1) {
+      if (lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        int stage = 0;
+        uint32_t phase = 0, pcount = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+          for (int kb = 0; kb < KB; ++kb) {
+            const uint32_t slot = pcount % kSlots;
+            if (!mbar_wait(&full[stage], phase, p.limit_ns, abort_flag, p.status) ||
+                !mbar_wait(&p_empty[slot], ((pcount / kSlots) & 1) ^ 1, p.limit_ns, abort_flag,
+                           p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(ring + stage * kStageBytes);
+            const uint32_t b_base = a_base + kATileBytes;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            mma_f8f6f4(tmem + slot * BN, make_sdesc(a_base + j * 32, 16, 1024, kSwizzle128B),
-                       make_sdesc(b_base + j * 32, 16, 1024, kSwizzle128B), p.idesc, j != 0);
-          tc_commit(&empty[stage]);
-          tc_commit(&p_full[slot]);
-          ++pcount;
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
+            for (int j = 0; j < 4; ++j)
+              mma_f8f6f4(tmem + slot * BN, make_sdesc(a_base + j * 32, 16, 1024, kSwizzle128B),
+                         make_sdesc(b_base + j * 32, 16, 1024, kSwizzle128B), p.idesc, j != 0);
+            tc_commit(&empty[stage]);
+            tc_commit(&p_full[slot]);
+            ++pcount;
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
         }
+        tc_commit(drain);
+        volatile int no_abort = 0;
+        mbar_wait(drain, 0, p.limit_ns, &no_abort, nullptr);
       }
-      tc_commit(drain);
-      volatile int no_abort = 0;
-      mbar_wait(drain, 0, p.limit_ns, &no_abort, nullptr);
     }
-  } else {
+    // both warpgroups meet once every MMA and tensor-memory read has been issued and fenced
+    named_barrier_sync(1, C::kThreads);
+    if (warp == 1) {
+      __syncwarp();
+      tc_fence_after();
+      tmem_dealloc(tmem, kTmemCols);
+    }
+    return;
+  }
+  setmaxnreg_inc<C::kFoldRegs>();
+  {
     // -------------------------------------------------------------- fold + epilogue
     constexpr int kCols = C::kCols;
     const int q = warp & 3;           // tensor-memory lane quarter
-    const int h = (warp - 2) >> 2;    // which half of the tile's columns
+    const int h = (warp - C::kFoldWarp0) >> 2;    // which half of the tile's columns
     uint32_t pcount = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
@@ -256,7 +276,7 @@ __global__ void __maxnreg__(168)
       // newest kScaleAhead - 1 groups complete block kb has landed.  Block kb+kScaleAhead
       // goes to the slot read in the previous iteration, never the one being read.
       constexpr int kFoldThreads = kEpiWarps * 32;
-      float* ring = scale_ring + (threadIdx.x - 64);
+      float* ring = scale_ring + (threadIdx.x - C::kFoldWarp0 * 32);
       // streaming source pointers: row scale of block kb at sx + kb*m_g (not read for rows
       // past the group's end), weight scale at sw + kb
       const float* sx_next = valid ? sx : p.sX;
@@ -317,27 +337,25 @@ __global__ void __maxnreg__(168)
             acc[16 + i] = __ffma2_rn(s2, make_float2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])),
                                      acc[16 + i]);
         } else {
-          // 128 columns in sixteen-column pieces, software-pipelined: the load of piece
-          // c+1 is in flight while piece c is folded (one wait covers both)
-          uint32_t ra[16], rb[16];
-          tmem_ld16(taddr, ra);
-          tmem_ld_wait16(ra);
+          // 128 columns in 32-column pieces, software-pipelined: the load of piece c+1
+          // is in flight while piece c is folded
+          uint32_t ra[32], rb[32];
+          tmem_ld32(taddr, ra);
+          tmem_ld_wait(ra);
 #pragma unroll
-          for (int c = 0; c < kCols / 16; c += 2) {
-            if (c + 1 < kCols / 16) tmem_ld16(taddr + (c + 1) * 16, rb);
+          for (int c = 0; c < kCols / 32; c += 2) {
+            tmem_ld32(taddr + (c + 1) * 32, rb);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              acc[c * 8 + i] = __ffma2_rn(s2, make_float2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1])),
-                                          acc[c * 8 + i]);
-            if (c + 1 < kCols / 16) {
-              tmem_ld_wait16(rb);
-              if (c + 2 < kCols / 16) tmem_ld16(taddr + (c + 2) * 16, ra);
+            for (int i = 0; i < 16; ++i)
+              acc[c * 16 + i] = __ffma2_rn(s2, make_float2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1])),
+                                           acc[c * 16 + i]);
+            tmem_ld_wait(rb);
+            if (c + 2 < kCols / 32) tmem_ld32(taddr + (c + 2) * 32, ra);
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                acc[(c + 1) * 8 + i] = __ffma2_rn(s2, make_float2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1])),
-                                                  acc[(c + 1) * 8 + i]);
-              if (c + 2 < kCols / 16) tmem_ld_wait16(ra);
-            }
+            for (int i = 0; i < 16; ++i)
+              acc[(c + 1) * 16 + i] = __ffma2_rn(s2, make_float2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1])),
+                                                 acc[(c + 1) * 16 + i]);
+            if (c + 2 < kCols / 32) tmem_ld_wait(ra);
           }
           tc_fence_before();
           __syncwarp();
@@ -359,12 +377,8 @@ __global__ void __maxnreg__(168)
     }
     cp_async_wait_all();   // no scale copy may land after the block has finished
   }
-  __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
+  tc_fence_before();
+  named_barrier_sync(1, C::kThreads);
 }
 
 template <int BN>

@@ -341,4 +341,23 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- warpgroup registers, barriers
+// Per-warpgroup register budget change (all four warps of a warpgroup execute it).  The
+// increases of all warpgroups must fit in what the block was launched with minus what
+// the decreases free, or the increase never completes.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+// Named hardware barrier `id` (1-15) over `threads` threads (a multiple of 32); the
+// calling warp is reconverged first.
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  __syncwarp();
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 }  // namespace bsmma

@@ -11,8 +11,9 @@
 //   every CTA reads m_sizes (int64, device memory), checks it (no negative entry,
 //   sum == total_M; otherwise nothing is written and a status is latched) and
 //   prefix-sums it into shared memory; a flat tile id -> (group, 128-row block of
-//   that group, 128-column block).  Empty groups own no tiles; no tile spans two
-//   groups; rows past a group's end are computed but never stored.
+//   that group, column block), in bands of row blocks walked along N.  Empty groups
+//   own no tiles; no tile spans two groups; rows past a group's end are computed but
+//   never stored.
 //   warp 0      TMA producer: 128x128 X and W tiles into a 6-stage ring;
 //   warp 1      lane 0 issues kind::f8f6f4 MMAs: each 128-K block goes into a fresh
 //               FP32 partial in tensor memory (two partial slots, so the MMA of block
@@ -76,6 +77,22 @@ struct GroupTable {
   int tile_start[kMaxG + 1];  // first 128-row block id of each group
   int bad;
 };
+
+// Tile t -> (128-row block mt, column block nt).  Tiles are walked in bands of kBandRows
+// row blocks: within a band the row block varies fastest, so the CTAs resident at one
+// time share a few weight column blocks and a band's rows of X, both of which stay in
+// L2 while the band is walked along N (row-fastest over all rows re-read every group's
+// whole weight matrix from DRAM for every few row blocks).
+constexpr int kBandRows = 16;
+__device__ __forceinline__ void tile_coords(int t, int NT, int rows, int& mt, int& nt) {
+  const int per_band = kBandRows * NT;
+  const int b = t / per_band;
+  const int r0 = b * kBandRows;
+  const int h = rows - r0 < kBandRows ? rows - r0 : kBandRows;
+  const int v = t - b * per_band;
+  mt = r0 + v % h;
+  nt = v / h;
+}
 
 // Group owning 128-row block `mt` (tile_start is non-decreasing; empty groups own none).
 __device__ __forceinline__ int find_group(const GroupTable& gt, int G, int mt) {
@@ -172,7 +189,8 @@ __global__ void __launch_bounds__(384, 1)
         uint32_t phase = 0, armed = 0, armed_parity = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-          const int mt = t / NT, nt = t - (t / NT) * NT;
+          int mt, nt;
+          tile_coords(t, NT, gt.tile_start[G], mt, nt);
           const int g = find_group(gt, G, mt);
           const int row0 = static_cast<int>(gt.start[g] + static_cast<int64_t>(mt - gt.tile_start[g]) * kBM);
           const int wrow0 = static_cast<int>(static_cast<int64_t>(g) * p.N + static_cast<int64_t>(nt) * BN);
@@ -253,7 +271,8 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t pcount = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-      const int mt = t / NT, nt = t - (t / NT) * NT;
+      int mt, nt;
+      tile_coords(t, NT, gt.tile_start[G], mt, nt);
       const int g = find_group(gt, G, mt);
       const int64_t m_g = gt.size[g];
       const int64_t l = static_cast<int64_t>(mt - gt.tile_start[g]) * kBM + q * 32 + lane;

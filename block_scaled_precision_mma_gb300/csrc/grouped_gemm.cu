@@ -430,10 +430,13 @@ bsmma_status launch_grouped(const uint8_t* X, const float* sX, const uint8_t* W,
   const DeviceInfo* dev = current_device(&st);
   if (!dev) return st;
   static_assert(sizeof(GroupTable) + 512 <= 2048, "group table fits its shared-memory slot");
-  // Wide tiles halve the W traffic per flop when there are enough rows to fill the
-  // GPU with them; narrow tiles keep every SM streaming W when rows are few.
+  // A 128x128 MMA takes as long as a 128x256 one, so wide tiles do the same work in half
+  // the MMA time and read W half as often per flop; they lose only when so few tiles
+  // remain that too few SMs stream W.  The row-block count is estimated from total_M
+  // (the sizes are on the device): each group adds on average half a partial block.
+  const int64_t row_blocks_est = (total_M + kBM - 1) / kBM + G / 2;
   const bool wide = (N % 256 == 0) &&
-                    ((total_M + kBM - 1) / kBM) * (N / 256) >= 2 * static_cast<int64_t>(dev->sm_count) &&
+                    row_blocks_est * (N / 256) * 2 >= static_cast<int64_t>(dev->sm_count) &&
                     grouped_tile_width() != 128;
   const bool force_wide = grouped_tile_width() == 256 && N % 256 == 0;
   const int bn = (wide || force_wide) ? 256 : 128;

@@ -316,18 +316,39 @@ def run_ours(args):
     d2h = sum(h["D"].numel() * h["D"].element_size() for _, _, h in gemms)
     e2e_steps = max(3, min(args.steps, 20))
 
+    # Every GEMM's inputs go host->device on one copy stream while the previous GEMM
+    # computes, and its result goes device->host on a second copy stream while the next
+    # one computes; events order each reuse of a device buffer across steps.
+    h2d_stream = torch.cuda.Stream(device=dev)
+    d2h_stream = torch.cuda.Stream(device=dev)
+    h2d_done = [torch.cuda.Event() for _ in gemms]
+    comp_done = [torch.cuda.Event() for _ in gemms]
+    d2h_done = [torch.cuda.Event() for _ in gemms]
+    recorded = [False] * len(gemms)
+
     def e2e_step():
-        for g, t, h in gemms:
-            if g["kind"] == "grouped":
-                for k in ("X", "sX", "W", "sW", "m_sizes"):
+        for i, (g, t, h) in enumerate(gemms):
+            with torch.cuda.stream(h2d_stream):
+                if recorded[i]:
+                    h2d_stream.wait_event(comp_done[i])     # the last step's GEMM i read its inputs
+                keys = ("X", "sX", "W", "sW", "m_sizes") if g["kind"] == "grouped" else ("A", "sA", "B", "sB")
+                for k in keys:
                     t[k].copy_(h[k], non_blocking=True)
+                h2d_done[i].record(h2d_stream)
+            stream.wait_event(h2d_done[i])
+            if recorded[i]:
+                stream.wait_event(d2h_done[i])              # the last step's result i is on the host
+            if g["kind"] == "grouped":
                 bs.grouped_fp8_gemm(t["X"], t["sX"], t["W"], t["sW"], t["m_sizes"], out=t["D"])
             else:
-                for k in ("A", "sA", "B", "sB"):
-                    t[k].copy_(h[k], non_blocking=True)
                 bs.mx_gemm(t["A"], t["sA"], t["B"], t["sB"], g["layout"], g["a"], g["b"],
                            out=t["D"], M=g["M"], N=g["N"], K=g["K"])
-            h["D"].copy_(t["D"], non_blocking=True)
+            comp_done[i].record(stream)
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(comp_done[i])
+                h["D"].copy_(t["D"], non_blocking=True)
+                d2h_done[i].record(d2h_stream)
+            recorded[i] = True
 
     if args.no_e2e:
         e2e_steps = 0
@@ -339,8 +360,11 @@ def run_ours(args):
     if dist:
         dist.barrier()
     e0.record(stream)
+    h2d_stream.wait_stream(stream)      # no copy of the timed steps starts before e0
     for _ in range(e2e_steps):
         e2e_step()
+    stream.wait_stream(d2h_stream)      # e1 follows the last result's arrival on the host
+    stream.wait_stream(h2d_stream)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps if e2e_steps else float("nan")
@@ -394,7 +418,8 @@ def run_ours(args):
             "value": round(ws * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "api": "mx_gemm / grouped_fp8_gemm with host->device copies of every input "
-                   "and device->host copy of D inside the timed region"},
+                   "and device->host copy of D inside the timed region; the copies run on two "
+                   "copy streams, overlapping the neighbouring GEMMs' compute"},
         "gpu_launches": int(n_launch),
         "clocks": clk.summary(),
         "wall_s_timed": round(wall, 3),

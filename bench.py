@@ -197,10 +197,18 @@ def reduce_max(values, dist):
     return v.tolist()
 
 
-def kernel_source_hash() -> str:
+# The sources each workload's dominant kernel is built from (the traffic record is
+# valid only while they are unchanged).
+KERNEL_SOURCES = {
+    "grouped_fp8": ("grouped_gemm.cu", "ptx.cuh", "internal.h"),
+    "dense": ("mx_gemm_2sm.cu", "mx_gemm.cu", "ptx.cuh", "internal.h"),
+}
+
+
+def kernel_source_hash(workload: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_scaled_precision_mma_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES["grouped_fp8" if workload == "grouped_fp8" else "dense"]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -216,7 +224,7 @@ def recorded_traffic(workload: str):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 kv[k.strip()] = v.strip()
-        if kv.get("kernel_sources_sha256_16") != kernel_source_hash():
+        if kv.get("kernel_sources_sha256_16") != kernel_source_hash(workload):
             return None
         return float(kv["dram_bytes_per_launch"])
     except Exception:

@@ -19,6 +19,12 @@ this module compiles it with gcc and exposes numpy-friendly wrappers:
   kernels copy into tensor memory, for the scales of op(A) (role 0) and op(B)
   (role 1).
 * :func:`decode_table` -- the decode tables the oracle uses.
+* :func:`mx_quantize`, :func:`fp8_group_quantize`, :func:`fp8_block_quantize` -- the
+  quantisers before the GEMM: MX rowwise / columnwise with E8M0 block scales ("[gfx1250]
+  Add MXFP4 GEMM support to FlyDSL backend", the MXFP4 test helpers and their review),
+  and the groupwise FP8 activation / weight quantisers with FP32 scales in the
+  per-group block layout ("Add FlyDSL grouped groupwise FP8 GEMM for ROCm",
+  quantize_fp8_group).  Inputs are FP32 values; BF16 inputs convert exactly.
 """
 from __future__ import annotations
 
@@ -73,6 +79,12 @@ def bind(path: str):
     lib.oracle_wide_scale_bytes.restype = i64
     lib.oracle_wide_scale_relayout.argtypes = [p, i64, i64, i32, p]
     lib.oracle_wide_scale_relayout.restype = None
+    lib.oracle_mx_quantize.argtypes = [p, i64, i64, i32, i32, p, p]
+    lib.oracle_mx_quantize.restype = i32
+    lib.oracle_fp8_group_quantize.argtypes = [p, i64, i64, p, i32, p, p]
+    lib.oracle_fp8_group_quantize.restype = i32
+    lib.oracle_fp8_block_quantize.argtypes = [p, i64, i64, i64, p, p]
+    lib.oracle_fp8_block_quantize.restype = i32
     return lib
 
 
@@ -166,3 +178,56 @@ def wide_scale_relayout(s_plain: np.ndarray, role: int, lib=None) -> np.ndarray:
     out = np.empty(wide_scale_bytes(rows, kblocks, role, lib), dtype=np.uint8)
     _load(lib).oracle_wide_scale_relayout(_ptr(s), rows, kblocks, role, _ptr(out))
     return out
+
+
+def _f32(x) -> np.ndarray:
+    """FP32 values of x (numpy, or a CPU torch tensor of BF16/FP32: exact conversions)."""
+    if hasattr(x, "detach"):
+        x = x.detach().float().cpu().numpy()
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
+def mx_quantize(x, fmt="e4m3", colwise=False, lib=None):
+    """MX quantisation of x[rows, cols] -> (codes, scales).
+
+    Rowwise: blocks of 32 along cols; codes [rows, cols] ([rows, cols/2] packed for
+    e2m1), scales [rows, cols/32].  Columnwise: blocks of 32 along rows; codes
+    [rows, cols], scales [cols, rows/32].  E8M0 scale codes, element codes per format.
+    """
+    x = _f32(x)
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols // 2 if fmt == "e2m1" else cols), dtype=np.uint8)
+    scales = np.zeros((cols, rows // 32) if colwise else (rows, cols // 32), dtype=np.uint8)
+    rc = _load(lib).oracle_mx_quantize(_ptr(x), rows, cols, FMT[fmt], int(bool(colwise)),
+                                       _ptr(codes), _ptr(scales))
+    if rc != 0:
+        raise ValueError("oracle_mx_quantize: unsupported arguments")
+    return codes, scales
+
+
+def fp8_group_quantize(x, m_sizes, lib=None):
+    """Groupwise E4M3 quantisation of activations x[total_M, K] over 1x128 blocks ->
+    (codes [total_M, K], sX float32 [total_M * K/128] in the per-group block layout)."""
+    x = _f32(x)
+    total_M, K = x.shape
+    ms = np.ascontiguousarray(m_sizes, dtype=np.int64)
+    codes = np.zeros((total_M, K), dtype=np.uint8)
+    sx = np.zeros(total_M * (K // 128), dtype=np.float32)
+    rc = _load(lib).oracle_fp8_group_quantize(_ptr(x), total_M, K, _ptr(ms), ms.size,
+                                              _ptr(codes), _ptr(sx))
+    if rc != 0:
+        raise ValueError("oracle_fp8_group_quantize: bad arguments")
+    return codes, sx
+
+
+def fp8_block_quantize(w, lib=None):
+    """Blockwise E4M3 quantisation of weights w[G, N, K] over 128x128 blocks ->
+    (codes [G, N, K], sW float32 [G, N/128, K/128])."""
+    w = _f32(w)
+    G, N, K = w.shape
+    codes = np.zeros((G, N, K), dtype=np.uint8)
+    sw = np.zeros((G, N // 128, K // 128), dtype=np.float32)
+    rc = _load(lib).oracle_fp8_block_quantize(_ptr(w), G, N, K, _ptr(codes), _ptr(sw))
+    if rc != 0:
+        raise ValueError("oracle_fp8_block_quantize: bad arguments")
+    return codes, sw

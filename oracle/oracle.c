@@ -28,10 +28,17 @@
  * definitions (OCP E4M3FN, E5M2, E2M1, E8M0).  Every operand row is decoded
  * once into an FP64 buffer, then plain sequential dot products are taken.
  *
+ *   quantisers (the step before the GEMM): MX rowwise / columnwise with E8M0 block
+ *   scales, and the groupwise FP8 activation (1x128) and weight (128x128)
+ *   quantisers with FP32 scales; see the section at the end of this file.
+ *
  * Parity is pinned by the CPU test-suite: closed-form decode points, exact
  * rational brute force on tiny inputs, unit-scale = plain matmul, power-of-two
  * equivariance, layout equivalence, grouped = per-group dense concatenation,
- * and bijection / padding / hand-derived positions of the scale relayouts.
+ * bijection / padding / hand-derived positions of the scale relayouts, and for
+ * the quantisers closed-form codes (ties, saturation, zero blocks, nibble order),
+ * exact round trips of representable values, an independent numpy/torch
+ * quantiser, and the half-step error bound.
  */
 #include <math.h>
 #include <pthread.h>
@@ -331,4 +338,176 @@ void oracle_wide_scale_relayout(const uint8_t* s, int64_t rows, int64_t kblocks,
               s[n * kblocks + kb];
       }
   }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Quantisers: the step before the GEMM.                                     */
+/*                                                                           */
+/* MX ("[gfx1250] Add MXFP4 GEMM support to FlyDSL backend", the MXFP4 test   */
+/* helpers and their review: rowwise and columnwise data are quantised        */
+/* separately; the quantiser takes BF16 input, FP32 asked for as well): per    */
+/* block of 32 values along the quantised dimension, amax = max|x|, E8M0 scale */
+/* 2^e with e = floor(log2 amax) - emax (emax 8 / 15 / 2 for E4M3 / E5M2 /     */
+/* E2M1), clamped to [-127, 127]; amax == 0 gives scale code 127.  Codes are   */
+/* round-to-nearest-even of x * 2^-e (an FP32 product), saturated to the       */
+/* largest finite value, with the sign of x.                                   */
+/*                                                                           */
+/* Groupwise FP8 ("Add FlyDSL grouped groupwise FP8 GEMM for ROCm":            */
+/* quantize_fp8_group(m_sizes=...) and the per-group block layout of its       */
+/* scales; 1x128 activation blocks, 128x128 weight blocks): FP32 scale          */
+/* s = amax / 448 (1 when amax == 0), codes = RNE-saturate(x / s) in E4M3,      */
+/* both divisions in FP32.  Inputs are FP32 values (BF16 converts exactly).    */
+/* ------------------------------------------------------------------------ */
+static int fmt_emax(int fmt) { return fmt == FMT_E4M3 ? 8 : fmt == FMT_E5M2 ? 15 : 2; }
+static int fmt_top(int fmt) { return fmt == FMT_E4M3 ? 0x7E : fmt == FMT_E5M2 ? 0x7B : 7; }
+static const double* fmt_table(int fmt) {
+  return fmt == FMT_E4M3 ? T_E4M3 : fmt == FMT_E5M2 ? T_E5M2 : T_E2M1;
+}
+
+/* Nearest finite code of |v| (ties to the even code, i.e. even mantissa), saturated at
+ * the largest finite magnitude; the sign bit follows the sign of v (so -0 and small
+ * negatives that round to zero keep it). */
+static uint8_t encode_rne_sat(double v, int fmt) {
+  const double* T = fmt_table(fmt);
+  const int top = fmt_top(fmt);
+  const double a = fabs(v);
+  int c;
+  if (a >= T[top]) {
+    c = top;
+  } else {
+    int lo = 0, hi = top;            /* T[lo] <= a < T[hi]; positive codes increase with value */
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) / 2;
+      if (T[mid] <= a) lo = mid;
+      else hi = mid;
+    }
+    const double below = a - T[lo], above = T[hi] - a;
+    if (below < above) c = lo;
+    else if (above < below) c = hi;
+    else c = (lo & 1) ? hi : lo;
+  }
+  if (signbit(v)) c |= (fmt == FMT_E2M1) ? 0x8 : 0x80;
+  return (uint8_t)c;
+}
+
+/* floor(log2 a) for a finite a > 0, exactly (frexp gives a = f * 2^p, f in [0.5, 1)). */
+static int floor_log2(double a) {
+  int p;
+  (void)frexp(a, &p);
+  return p - 1;
+}
+
+/* MX quantisation of x[rows][cols] (row-major FP32 values).
+ *   colwise == 0: blocks of 32 along cols; codes [rows][cols] (E2M1: [rows][cols/2],
+ *                 even column in the low nibble); scales [rows][cols/32].
+ *   colwise == 1: blocks of 32 along rows; codes [rows][cols] (same layout as x);
+ *                 scales [cols][rows/32].  Not for E2M1.
+ * Returns 0, or -1 for unsupported arguments. */
+int oracle_mx_quantize(const float* x, int64_t rows, int64_t cols, int fmt, int colwise,
+                       uint8_t* codes, uint8_t* scales) {
+  init_tables();
+  if (rows < 0 || cols < 0 || fmt < FMT_E4M3 || fmt > FMT_E2M1) return -1;
+  if (colwise ? (rows % 32 != 0 || fmt == FMT_E2M1) : (cols % 32 != 0)) return -1;
+  const int64_t outer = colwise ? cols : rows;       /* one line of blocks per row / column */
+  const int64_t len = colwise ? rows : cols;         /* values along the quantised dimension */
+  for (int64_t o = 0; o < outer; ++o)
+    for (int64_t b = 0; b < len / 32; ++b) {
+      float amax = 0.0f;
+      for (int64_t t = 0; t < 32; ++t) {
+        const int64_t i = colwise ? (b * 32 + t) * cols + o : o * cols + b * 32 + t;
+        const float m = fabsf(x[i]);
+        if (m > amax) amax = m;
+      }
+      int e = 0;
+      if (amax > 0.0f) {
+        e = floor_log2((double)amax) - fmt_emax(fmt);
+        if (e < -127) e = -127;
+        if (e > 127) e = 127;
+      }
+      const uint8_t scode = (uint8_t)(amax > 0.0f ? e + 127 : 127);
+      scales[o * (len / 32) + b] = scode;
+      const float inv = ldexpf(1.0f, 127 - (int)scode);   /* 2^-e */
+      for (int64_t t = 0; t < 32; ++t) {
+        const int64_t i = colwise ? (b * 32 + t) * cols + o : o * cols + b * 32 + t;
+        const float y = x[i] * inv;
+        const uint8_t q = encode_rne_sat((double)y, fmt);
+        if (fmt == FMT_E2M1) {
+          const int64_t k = b * 32 + t;
+          uint8_t* byte = &codes[o * (cols / 2) + k / 2];
+          if ((k & 1) == 0) *byte = (uint8_t)((*byte & 0xF0) | q);
+          else *byte = (uint8_t)((*byte & 0x0F) | (q << 4));
+        } else {
+          codes[i] = q;
+        }
+      }
+    }
+  return 0;
+}
+
+/* E4M3 codes of one block of values with FP32 scale s = amax / 448 (1 when amax == 0). */
+static float group_scale(float amax) { return amax > 0.0f ? amax / 448.0f : 1.0f; }
+
+/* Groupwise quantisation of activations X[total_M][K] (FP32 values) over 1x128 blocks.
+ * codes [total_M][K]; sx in the per-group block layout: group g starts at
+ * M_start_g * (K/128) and holds (local row l, block kb) at l + kb * m_g.
+ * Returns 0, or -1 when K % 128 != 0 or m_sizes do not partition total_M. */
+int oracle_fp8_group_quantize(const float* x, int64_t total_M, int64_t K,
+                              const int64_t* m_sizes, int G, uint8_t* codes, float* sx) {
+  init_tables();
+  if (K % 128 != 0 || G < 1 || total_M < 0) return -1;
+  int64_t sum = 0;
+  for (int g = 0; g < G; ++g) {
+    if (m_sizes[g] < 0) return -1;
+    sum += m_sizes[g];
+  }
+  if (sum != total_M) return -1;
+  const int64_t KB = K / 128;
+  int64_t start = 0;
+  for (int g = 0; g < G; ++g) {
+    const int64_t mg = m_sizes[g];
+    for (int64_t l = 0; l < mg; ++l) {
+      const int64_t r = start + l;
+      for (int64_t kb = 0; kb < KB; ++kb) {
+        float amax = 0.0f;
+        for (int64_t t = 0; t < 128; ++t) {
+          const float m = fabsf(x[r * K + kb * 128 + t]);
+          if (m > amax) amax = m;
+        }
+        const float s = group_scale(amax);
+        sx[start * KB + l + kb * mg] = s;
+        for (int64_t t = 0; t < 128; ++t) {
+          const int64_t i = r * K + kb * 128 + t;
+          codes[i] = encode_rne_sat((double)(x[i] / s), FMT_E4M3);
+        }
+      }
+    }
+    start += mg;
+  }
+  return 0;
+}
+
+/* Blockwise quantisation of weights W[G][N][K] (FP32 values) over 128x128 blocks.
+ * codes [G][N][K]; sw [G][N/128][K/128].  Returns 0, or -1 unless N, K % 128 == 0. */
+int oracle_fp8_block_quantize(const float* w, int64_t G, int64_t N, int64_t K, uint8_t* codes,
+                              float* sw) {
+  init_tables();
+  if (N % 128 != 0 || K % 128 != 0 || G < 0) return -1;
+  for (int64_t g = 0; g < G; ++g)
+    for (int64_t nb = 0; nb < N / 128; ++nb)
+      for (int64_t kb = 0; kb < K / 128; ++kb) {
+        float amax = 0.0f;
+        for (int64_t n = nb * 128; n < nb * 128 + 128; ++n)
+          for (int64_t k = kb * 128; k < kb * 128 + 128; ++k) {
+            const float m = fabsf(w[(g * N + n) * K + k]);
+            if (m > amax) amax = m;
+          }
+        const float s = group_scale(amax);
+        sw[(g * (N / 128) + nb) * (K / 128) + kb] = s;
+        for (int64_t n = nb * 128; n < nb * 128 + 128; ++n)
+          for (int64_t k = kb * 128; k < kb * 128 + 128; ++k) {
+            const int64_t i = (g * N + n) * K + k;
+            codes[i] = encode_rne_sat((double)(w[i] / s), FMT_E4M3);
+          }
+      }
+  return 0;
 }

@@ -336,6 +336,161 @@ def pin_wide_relayout(lib=None):
             assert sorted(pos[(r, k)]) == [base + q * 1024 for q in range(copies[role])], (role, r, k)
 
 
+# ---------------------------------------------------------------- quantisers
+EMAX = {"e4m3": 8, "e5m2": 15, "e2m1": 2}
+
+
+def _rowwise(x, fmt, lib):
+    return oracle.mx_quantize(np.asarray(x, dtype=np.float32), fmt, lib=lib)
+
+
+def pin_quant_closed_form(lib=None):
+    """Hand-derived codes: ties to even, saturation, zero / negative-zero blocks,
+    exponent clamping, E5M2 and E2M1 points, nibble order."""
+    # E4M3, amax 1: e = 0 - 8, scale code 119; 1 * 2^8 = 256 = exponent field 15 -> 0x78
+    c, s = _rowwise(np.ones((1, 32)), "e4m3", lib)
+    assert s[0, 0] == 119 and (c == 0x78).all()
+    # amax 1.875: e = -8; 1.875 * 256 = 480 lies past 448 and saturates to 0x7E
+    x = np.zeros((1, 32)); x[0, 0] = 1.875; x[0, 1] = -1.875
+    c, s = _rowwise(x, "e4m3", lib)
+    assert s[0, 0] == 119 and c[0, 0] == 0x7E and c[0, 1] == 0xFE
+    # amax 256: e = 0 (code 127); 17 sits halfway between 16 (0x58) and 18 (0x59): even -> 0x58;
+    # 19 halfway between 18 (0x59) and 20 (0x5A): even -> 0x5A; -17 -> 0xD8
+    x = np.zeros((1, 32)); x[0, :4] = [256.0, 17.0, 19.0, -17.0]
+    c, s = _rowwise(x, "e4m3", lib)
+    assert s[0, 0] == 127 and list(c[0, :4]) == [0x78, 0x58, 0x5A, 0xD8]
+    # zero block: scale code 127, codes 0; negative zeros keep the sign
+    x = np.zeros((1, 64)); x[0, 32:] = -0.0
+    c, s = _rowwise(x, "e4m3", lib)
+    assert (s == 127).all() and (c[0, :32] == 0).all() and (c[0, 32:] == 0x80).all()
+    # tiny amax 2^-140: e = -148 clamps to -127 (code 0); 2^-140 * 2^127 = 2^-13 rounds to 0
+    x = np.zeros((1, 32)); x[0, 0] = 2.0 ** -140
+    c, s = _rowwise(x, "e4m3", lib)
+    assert s[0, 0] == 0 and c[0, 0] == 0
+    # huge amax 1.5 * 2^127: e = 127 - 8 = 119 (code 246); 1.5 * 2^8 = 384: exponent
+    # field 15, mantissa 100b -> 0x7C
+    x = np.zeros((1, 32)); x[0, 0] = 1.5 * 2.0 ** 127
+    c, s = _rowwise(x, "e4m3", lib)
+    assert s[0, 0] == 246 and c[0, 0] == 0x7C
+    # E5M2, amax 3: e = 1 - 15 = -14 (code 113); 3 * 2^14 = 49152 = 1.5 * 2^15 -> 0x7A
+    x = np.zeros((1, 32)); x[0, 0] = 3.0
+    c, s = _rowwise(x, "e5m2", lib)
+    assert s[0, 0] == 113 and c[0, 0] == 0x7A
+    # E2M1, amax 6 (code 7): e = 2 - 2 = 0; halfway values go to the even code:
+    # 0.25 -> 0 (code 0), 0.75 -> 1.0 (code 2), 2.5 -> 2 (code 4), 5 -> 4 (code 6); -1.5 -> 0xB
+    x = np.zeros((1, 32)); x[0, :6] = [6.0, 0.25, 0.75, 2.5, 5.0, -1.5]
+    c, s = _rowwise(x, "e2m1", lib)
+    assert s[0, 0] == 127
+    # packed: element 2k in the low nibble of byte k
+    assert c[0, 0] == (0x7 | (0x0 << 4)) and c[0, 1] == (0x2 | (0x4 << 4)) and c[0, 2] == (0x6 | (0xB << 4))
+    # columnwise = rowwise of the transpose (codes transposed back, same scales)
+    g = np.random.default_rng(7)
+    x = g.standard_normal((64, 96)).astype(np.float32)
+    cc, sc = oracle.mx_quantize(x, "e4m3", colwise=True, lib=lib)
+    cr, sr = oracle.mx_quantize(np.ascontiguousarray(x.T), "e4m3", lib=lib)
+    assert np.array_equal(cc, cr.T) and np.array_equal(sc, sr)
+
+
+def pin_quant_vs_independent(lib=None):
+    """The numpy/torch generator quantiser (float64 log2 for the exponent, torch float8
+    casts / explicit thresholds for the rounding) agrees code for code."""
+    g = np.random.default_rng(11)
+    for fmt in ("e4m3", "e5m2", "e2m1"):
+        for shape, spread in (((37, 64), 1.0), ((5, 256), 1e-30), ((9, 96), 1e30)):
+            x = (g.standard_normal(shape) * spread).astype(np.float32)
+            x[0, :32] = 0.0
+            x[1, 32:64] *= np.float32(2.0 ** -20)
+            c, s = oracle.mx_quantize(x, fmt, lib=lib)
+            c2, s2 = synthetic.quantize_mx(x, fmt)
+            assert np.array_equal(s, s2), fmt
+            assert np.array_equal(c, c2), fmt
+
+
+def _decode_codes(codes, fmt):
+    return torch_decode(unpack_fp4(codes) if fmt == "e2m1" else codes, fmt)
+
+
+def pin_quant_roundtrip(lib=None):
+    """Values decode(code) * 2^e with a top-binade value in every block quantise back to
+    the same codes and scale."""
+    g = np.random.default_rng(13)
+    top = {"e4m3": [0x78, 0x7E], "e5m2": [0x78, 0x7B], "e2m1": [0x6, 0x7]}
+    for fmt in ("e4m3", "e5m2", "e2m1"):
+        rows, K = 6, 128
+        codes = random_finite_codes(g, (rows, K), fmt)
+        # the first value of every block lies in the format's top binade, so the block's
+        # exponent is exactly e (every other finite magnitude is at most that binade's top)
+        codes[:, ::32] = g.choice(top[fmt], size=(rows, K // 32))
+        e = g.integers(-40, 40, size=(rows, K // 32))
+        vals = torch_decode(codes, fmt) * np.ldexp(1.0, np.repeat(e, 32, axis=1))
+        c, s = oracle.mx_quantize(vals.astype(np.float32), fmt, lib=lib)
+        assert np.array_equal(s.astype(np.int64), e + 127), fmt
+        got = unpack_fp4(c) if fmt == "e2m1" else c
+        assert np.array_equal(got, codes), fmt
+
+
+def pin_quant_error_bound(lib=None):
+    """|decode(q) 2^e - x| is at most half the grid step at |x| 2^-e (or x was past the
+    largest finite value and q is saturated)."""
+    g = np.random.default_rng(17)
+    for fmt in ("e4m3", "e5m2", "e2m1"):
+        x = g.standard_normal((16, 128)).astype(np.float32) * 3
+        c, s = oracle.mx_quantize(x, fmt, lib=lib)
+        scale = np.ldexp(1.0, np.repeat(s.astype(np.int64) - 127, 32, axis=1))
+        y = x.astype(np.float64) / scale
+        q = _decode_codes(c, fmt)
+        grid = np.unique(np.abs(torch_decode(np.arange(16 if fmt == "e2m1" else 256, dtype=np.uint8), fmt)))
+        grid = grid[np.isfinite(grid)]
+        fmax = grid.max()
+        idx = np.clip(np.searchsorted(grid, np.abs(y)), 1, grid.size - 1)
+        step = grid[idx] - grid[idx - 1]
+        sat = np.abs(y) >= fmax
+        assert (np.abs(q - y)[~sat] <= step[~sat] / 2 + 1e-300).all(), fmt
+        assert (np.abs(q[sat]) == fmax).all(), fmt
+        assert (np.sign(q) * np.sign(y) >= 0).all(), fmt
+
+
+def pin_group_quant(lib=None):
+    """Groupwise FP8 quantisers against a numpy/torch restatement (FP32 divisions,
+    torch E4M3 cast) and the per-group block layout written out by hand."""
+    g = np.random.default_rng(19)
+    ms = np.array([3, 0, 130, 1, 0, 17], dtype=np.int64)
+    T, K = int(ms.sum()), 384
+    x = g.standard_normal((T, K)).astype(np.float32)
+    x[4, 128:256] = 0.0                     # a zero block: scale 1
+    codes, sx = oracle.fp8_group_quantize(x, ms, lib=lib)
+    KB = K // 128
+    start = 0
+    for gi, m in enumerate(ms):
+        for l in range(m):
+            r = start + l
+            for kb in range(KB):
+                blk = x[r, kb * 128:(kb + 1) * 128]
+                amax = np.float32(np.abs(blk).max())
+                s = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+                assert sx[start * KB + l + kb * m] == s
+                y = (blk / s).astype(np.float32)
+                want = synthetic.encode(y, "e4m3")
+                assert np.array_equal(codes[r, kb * 128:(kb + 1) * 128], want)
+        start += m
+    # one group: the block layout is the plain [K/128, total_M] transpose
+    c1, s1 = oracle.fp8_group_quantize(x, np.array([T]), lib=lib)
+    amax = np.abs(x.reshape(T, KB, 128)).max(axis=2)
+    s_ref = np.where(amax > 0, (amax / np.float32(448.0)).astype(np.float32), np.float32(1.0))
+    assert np.array_equal(s1.reshape(KB, T), s_ref.T)
+    # weights: 128x128 blocks, [G, N/128, K/128]
+    w = g.standard_normal((2, 256, 256)).astype(np.float32)
+    w[1, 128:, :128] *= np.float32(1e-3)
+    cw, sw = oracle.fp8_block_quantize(w, lib=lib)
+    blocks = w.reshape(2, 2, 128, 2, 128)
+    amax = np.abs(blocks).max(axis=(2, 4))
+    s_ref = (amax / np.float32(448.0)).astype(np.float32)
+    assert np.array_equal(sw, s_ref)
+    y = (blocks / s_ref[:, :, None, :, None]).astype(np.float32).reshape(2, 256, 256)
+    assert np.array_equal(cw, synthetic.encode(y, "e4m3").reshape(2, 256, 256))
+
+
 ALL_PINS = [pin_decode_points, pin_decode_vs_torch, pin_dense_bruteforce, pin_dense_unit_scales,
             pin_dense_pow2, pin_dense_layouts, pin_grouped_concat, pin_grouped_g1_transpose,
-            pin_grouped_probes, pin_wide_relayout]
+            pin_grouped_probes, pin_wide_relayout, pin_quant_closed_form, pin_quant_vs_independent,
+            pin_quant_roundtrip, pin_quant_error_bound, pin_group_quant]

@@ -31,6 +31,20 @@ MUTANTS = [
     ("wide_chunk_kgroups", "kq = kg / 2, g = kg % 2", "kq = kg / 4, g = kg % 2"),
     ("wide_col_lane", "lane_col_byte(nn % 32, nn / 32, kb % 4)", "lane_col_byte(nn / 8, nn % 8, kb % 4)"),
     ("wide_col_one_quarter", "for (int64_t q = 0; q < 4; ++q)", "for (int64_t q = 0; q < 1; ++q)"),
+    ("quant_emax", "fmt == FMT_E4M3 ? 8 : fmt == FMT_E5M2 ? 15 : 2", "fmt == FMT_E4M3 ? 7 : fmt == FMT_E5M2 ? 15 : 2"),
+    ("quant_floor_log2", "return p - 1;", "return p;"),
+    ("quant_ties_odd", "else c = (lo & 1) ? hi : lo;", "else c = (lo & 1) ? lo : hi;"),
+    ("quant_ties_away", "else c = (lo & 1) ? hi : lo;", "else c = hi;"),
+    ("quant_saturate_past_top", "    c = top;\n", "    c = top + 1;\n"),
+    ("quant_sign_from_comparison", "if (signbit(v)) c |=", "if (v < 0) c |="),
+    ("quant_nibble_order", "if ((k & 1) == 0) *byte", "if ((k & 1) == 1) *byte"),
+    ("quant_colwise_scale_order", "scales[o * (len / 32) + b] = scode;", "scales[b * outer + o] = scode;"),
+    ("quant_no_clamp_low", "if (e < -127) e = -127;", "if (e < -127) e = e + 256;"),
+    ("group_scale_fmax", "amax / 448.0f", "amax / 512.0f"),
+    ("group_sx_rowmajor", "sx[start * KB + l + kb * mg] = s;", "sx[start * KB + l * KB + kb] = s;"),
+    ("group_block_rows", "for (int64_t t = 0; t < 128; ++t) {\n          const float m = fabsf(x[r * K + kb * 128 + t]);",
+     "for (int64_t t = 0; t < 64; ++t) {\n          const float m = fabsf(x[r * K + kb * 128 + t]);"),
+    ("block_sw_kmajor", "sw[(g * (N / 128) + nb) * (K / 128) + kb] = s;", "sw[(g * (K / 128) + kb) * (N / 128) + nb] = s;"),
 ]
 
 

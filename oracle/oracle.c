@@ -355,8 +355,9 @@ void oracle_wide_scale_relayout(const uint8_t* s, int64_t rows, int64_t kblocks,
 /* Groupwise FP8 ("Add FlyDSL grouped groupwise FP8 GEMM for ROCm":            */
 /* quantize_fp8_group(m_sizes=...) and the per-group block layout of its       */
 /* scales; 1x128 activation blocks, 128x128 weight blocks): FP32 scale          */
-/* s = amax / 448 (1 when amax == 0), codes = RNE-saturate(x / s) in E4M3,      */
-/* both divisions in FP32.  Inputs are FP32 values (BF16 converts exactly).    */
+/* s = amax / 448 (1 when amax == 0, at least 2^-149), codes =                  */
+/* RNE-saturate(x / s) in E4M3, both divisions in FP32.  Inputs are FP32        */
+/* values (BF16 converts exactly).                                            */
 /* ------------------------------------------------------------------------ */
 static int fmt_emax(int fmt) { return fmt == FMT_E4M3 ? 8 : fmt == FMT_E5M2 ? 15 : 2; }
 static int fmt_top(int fmt) { return fmt == FMT_E4M3 ? 0x7E : fmt == FMT_E5M2 ? 0x7B : 7; }
@@ -444,8 +445,15 @@ int oracle_mx_quantize(const float* x, int64_t rows, int64_t cols, int fmt, int 
   return 0;
 }
 
-/* E4M3 codes of one block of values with FP32 scale s = amax / 448 (1 when amax == 0). */
-static float group_scale(float amax) { return amax > 0.0f ? amax / 448.0f : 1.0f; }
+/* FP32 scale of one block: s = amax / 448, 1 when amax == 0, and never below the
+ * smallest positive FP32 (2^-149), so that a block whose amax / 448 underflows (FP32
+ * inputs under 448 * 2^-150) still divides by a positive number. */
+static float group_scale(float amax) {
+  if (!(amax > 0.0f)) return 1.0f;
+  const float s = amax / 448.0f;
+  const float tiny = ldexpf(1.0f, -149);
+  return s > tiny ? s : tiny;
+}
 
 /* Groupwise quantisation of activations X[total_M][K] (FP32 values) over 1x128 blocks.
  * codes [total_M][K]; sx in the per-group block layout: group g starts at

@@ -467,12 +467,18 @@ def pin_group_quant(lib=None):
             for kb in range(KB):
                 blk = x[r, kb * 128:(kb + 1) * 128]
                 amax = np.float32(np.abs(blk).max())
-                s = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+                s = (max(np.float32(amax / np.float32(448.0)), np.float32(2.0 ** -149))
+                     if amax > 0 else np.float32(1.0))
                 assert sx[start * KB + l + kb * m] == s
                 y = (blk / s).astype(np.float32)
                 want = synthetic.encode(y, "e4m3")
                 assert np.array_equal(codes[r, kb * 128:(kb + 1) * 128], want)
         start += m
+    # a block whose amax / 448 underflows in FP32 divides by 2^-149: amax = 2^-149 gives
+    # s = 2^-149 and code 1.0 (0x38) for the block maximum
+    xt = np.zeros((1, 128), dtype=np.float32); xt[0, 5] = np.float32(2.0 ** -149)
+    ct, st = oracle.fp8_group_quantize(xt, np.array([1]), lib=lib)
+    assert st[0] == np.float32(2.0 ** -149) and ct[0, 5] == 0x38 and (np.delete(ct[0], 5) == 0).all()
     # one group: the block layout is the plain [K/128, total_M] transpose
     c1, s1 = oracle.fp8_group_quantize(x, np.array([T]), lib=lib)
     amax = np.abs(x.reshape(T, KB, 128)).max(axis=2)

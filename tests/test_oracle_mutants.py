@@ -44,6 +44,7 @@ MUTANTS = [
     ("group_sx_rowmajor", "sx[start * KB + l + kb * mg] = s;", "sx[start * KB + l * KB + kb] = s;"),
     ("group_block_rows", "for (int64_t t = 0; t < 128; ++t) {\n          const float m = fabsf(x[r * K + kb * 128 + t]);",
      "for (int64_t t = 0; t < 64; ++t) {\n          const float m = fabsf(x[r * K + kb * 128 + t]);"),
+    ("group_scale_no_floor", "return s > tiny ? s : tiny;", "return s;"),
     ("block_sw_kmajor", "sw[(g * (N / 128) + nb) * (K / 128) + kb] = s;", "sw[(g * (K / 128) + kb) * (N / 128) + nb] = s;"),
 ]
 

@@ -10,7 +10,8 @@ MiB write) before every GEMM, outside the timed events.
 
 Other workloads (``--workload``): mxfp4_dense (8192^3 and 1024x14336x4096),
 grouped_fp8 (G=8, totM 128/1024/16384 x three (N,K)), linear_triple (fwd/dgrad/
-wgrad of X[8192,4096], W[14336,4096], dY[8192,14336]), mxfp8_256 (256^3).
+wgrad of X[8192,4096], W[14336,4096], dY[8192,14336]), mxfp8_256 (256^3), and
+quantize (the quantisers that make the operands, in GB/s against HBM bandwidth).
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead
 (on a bounded row sample of the same workload, on the host cores).  Multi-GPU
@@ -201,6 +202,7 @@ def reduce_max(values, dist):
 # valid only while they are unchanged).
 KERNEL_SOURCES = {
     "grouped_fp8": ("grouped_gemm.cu", "ptx.cuh", "internal.h"),
+    "quantize": ("quantize.cu", "ptx.cuh", "internal.h"),
     "dense": ("mx_gemm_2sm.cu", "mx_gemm.cu", "ptx.cuh", "internal.h"),
 }
 
@@ -208,7 +210,7 @@ KERNEL_SOURCES = {
 def kernel_source_hash(workload: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_scaled_precision_mma_gb300", "csrc")
-    for f in KERNEL_SOURCES["grouped_fp8" if workload == "grouped_fp8" else "dense"]:
+    for f in KERNEL_SOURCES[workload if workload in KERNEL_SOURCES else "dense"]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -437,6 +439,283 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- quantisers
+QUANT_METRIC = "quantiser GB/s (algorithmic bytes read + written per second) and % of measured HBM copy bandwidth"
+QUANT_TEXT = ("quantisers on BF16 inputs: MX E4M3 rowwise and columnwise of X[8192,8192] (the Linear "
+              "forward and wgrad operands), groupwise E4M3 of X[16384,7168] with G=8 seeded m_sizes "
+              "(1x128 FP32 scales, per-group block layout), blockwise E4M3 of W[8,2048,7168] "
+              "(128x128 FP32 scales)")
+
+
+def quant_ops():
+    """The quantiser calls of one step: (name, input shape, seed, kind)."""
+    return [("mx_rows_e4m3", (8192, 8192), 0, "rows"), ("mx_cols_e4m3", (8192, 8192), 0, "cols"),
+            ("group_x_e4m3", (16384, 7168), 1, "group"), ("block_w_e4m3", (8, 2048, 7168), 2, "block")]
+
+
+def quant_bytes(kind, shape, in_bytes=2):
+    n = int(np.prod(shape))
+    if kind in ("rows", "cols"):
+        return n * in_bytes + n + n // 32
+    if kind == "group":
+        return n * in_bytes + n + (n // 128) * 4
+    return n * in_bytes + n + (n // (128 * 128)) * 4
+
+
+def quant_input(shape, seed):
+    import synthetic
+    return synthetic.normal((6, seed), shape)
+
+
+def quant_call(bs, kind, x, out, m_sizes, stream=None):
+    if kind == "rows":
+        bs.mx_quantize(x, "e4m3", codes=out[0], scales=out[1], stream=stream)
+    elif kind == "cols":
+        bs.mx_quantize(x, "e4m3", colwise=True, codes=out[0], scales=out[1], stream=stream)
+    elif kind == "group":
+        bs.fp8_group_quantize(x, m_sizes, codes=out[0], scales=out[1], stream=stream)
+    else:
+        bs.fp8_block_quantize(x, codes=out[0], scales=out[1], stream=stream)
+
+
+def quant_outputs(torch, kind, shape, dev, pinned=False):
+    def mk(sh, dt):
+        t = torch.empty(sh, dtype=dt, device="cpu" if pinned else dev)
+        return t.pin_memory() if pinned else t
+    if kind == "rows":
+        return mk(shape, torch.uint8), mk((shape[0], shape[1] // 32), torch.uint8)
+    if kind == "cols":
+        return mk(shape, torch.uint8), mk((shape[1], shape[0] // 32), torch.uint8)
+    if kind == "group":
+        return mk(shape, torch.uint8), mk((shape[0] * (shape[1] // 128),), torch.float32)
+    return mk(shape, torch.uint8), mk((shape[0], shape[1] // 128, shape[2] // 128), torch.float32)
+
+
+def quant_oracle_sample(cache, frac, nthreads=None):
+    """Oracle quantisation of a `frac` share of every call's rows (rows, columns or weight
+    blocks are independent); returns (seconds, algorithmic bytes)."""
+    import oracle
+    import synthetic
+    secs, nbytes = 0.0, 0.0
+    for name, shape, seed, kind in quant_ops():
+        if name not in cache:
+            x = quant_input(shape, seed)
+            import torch
+            cache[name] = torch.from_numpy(x).to(torch.bfloat16).float().numpy()
+        x = cache[name]
+        if kind in ("rows", "group"):
+            r = max(1, int(shape[0] * frac))
+            sub = x[:r]
+            t0 = time.perf_counter()
+            if kind == "rows":
+                oracle.mx_quantize(sub, "e4m3")
+            else:
+                oracle.fp8_group_quantize(sub, np.array([r // 3, 0, r - r // 3]))
+            secs += time.perf_counter() - t0
+            nbytes += quant_bytes(kind, sub.shape)
+        elif kind == "cols":
+            c = max(16, int(shape[1] * frac) // 16 * 16)
+            sub = np.ascontiguousarray(x[:, :c])
+            t0 = time.perf_counter()
+            oracle.mx_quantize(sub, "e4m3", colwise=True)
+            secs += time.perf_counter() - t0
+            nbytes += quant_bytes(kind, sub.shape)
+        else:
+            n = max(128, int(shape[1] * frac) // 128 * 128)
+            sub = np.ascontiguousarray(x[:1, :n])
+            t0 = time.perf_counter()
+            oracle.fp8_block_quantize(sub)
+            secs += time.perf_counter() - t0
+            nbytes += quant_bytes(kind, sub.shape)
+    return secs, nbytes
+
+
+def run_quantize(args):
+    import torch
+    import block_scaled_precision_mma_gb300 as bs
+
+    ws, rank, local = dist_env()
+    dist = init_dist(ws)
+    torch.cuda.set_device(local)
+    bs.build()
+    bs.load()
+    dev = torch.device("cuda", local)
+    import synthetic
+    ms_host = torch.from_numpy(synthetic.gen_m_sizes(16384, 6)).pin_memory()
+    ms = ms_host.to(dev)
+    ops = []
+    for name, shape, seed, kind in quant_ops():
+        xh = torch.from_numpy(quant_input(shape, seed)).to(torch.bfloat16).pin_memory()
+        ops.append(dict(name=name, kind=kind, shape=shape, x=xh.to(dev), xh=xh,
+                        out=quant_outputs(torch, kind, shape, dev),
+                        outh=quant_outputs(torch, kind, shape, dev, pinned=True),
+                        bytes=quant_bytes(kind, shape)))
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    step_bytes = sum(o["bytes"] for o in ops)
+
+    def step(events):
+        for o, ev in zip(ops, events):
+            flush.zero_()
+            ev[0].record(stream)
+            quant_call(bs, o["kind"], o["x"], o["out"], ms)
+            ev[1].record(stream)
+
+    mk = lambda: [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in ops]
+    for _ in range(args.warmup):
+        step(mk())
+    torch.cuda.synchronize()
+    if bs.device_status() != 0:
+        raise SystemExit("device status error during warm-up")
+    all_events = [mk() for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    n0 = bs.launch_count()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            step(all_events[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    n_launch = bs.launch_count() - n0
+    st = bs.device_status()
+    if st != 0:
+        raise SystemExit(f"device status {bs.status_string(st)}")
+    per_op_ms = [sum(evs[j][0].elapsed_time(evs[j][1]) for evs in all_events) / args.steps
+                 for j in range(len(ops))]
+
+    # end to end: inputs up on one copy stream, codes and scales down on another
+    h2d_stream = torch.cuda.Stream(device=dev)
+    d2h_stream = torch.cuda.Stream(device=dev)
+    h2d_done = [torch.cuda.Event() for _ in ops]
+    comp_done = [torch.cuda.Event() for _ in ops]
+    d2h_done = [torch.cuda.Event() for _ in ops]
+    recorded = [False] * len(ops)
+
+    def e2e_step():
+        for i, o in enumerate(ops):
+            with torch.cuda.stream(h2d_stream):
+                if recorded[i]:
+                    h2d_stream.wait_event(comp_done[i])
+                o["x"].copy_(o["xh"], non_blocking=True)
+                h2d_done[i].record(h2d_stream)
+            stream.wait_event(h2d_done[i])
+            if recorded[i]:
+                stream.wait_event(d2h_done[i])
+            quant_call(bs, o["kind"], o["x"], o["out"], ms)
+            comp_done[i].record(stream)
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(comp_done[i])
+                for dst, src in zip(o["outh"], o["out"]):
+                    dst.copy_(src, non_blocking=True)
+                d2h_done[i].record(d2h_stream)
+            recorded[i] = True
+
+    e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 20))
+    h2d = sum(o["xh"].numel() * o["xh"].element_size() for o in ops)
+    d2h = sum(t.numel() * t.element_size() for o in ops for t in o["outh"])
+    if e2e_steps:
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    e0.record(stream)
+    h2d_stream.wait_stream(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    stream.wait_stream(d2h_stream)
+    stream.wait_stream(h2d_stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps if e2e_steps else float("nan")
+
+    step_ms = sum(per_op_ms)
+    step_ms, e2e_ms = reduce_max([step_ms, e2e_ms], dist)
+    if rank != 0:
+        return
+    _, hbm_peak, peak_src = measured_peaks()
+    dom = max(range(len(ops)), key=lambda j: ops[j]["bytes"])
+    achieved = ops[dom]["bytes"] / (per_op_ms[dom] * 1e-3) / 1e9
+    kernel = {"rows": "mx_quant_rows_kernel", "cols": "mx_quant_cols_kernel",
+              "group": "group_quant_kernel", "block": "block_quant_kernel"}[ops[dom]["kind"]]
+    line = {
+        "metric": QUANT_METRIC,
+        "value": round(ws * step_bytes / (step_ms * 1e-3) / 1e9, 1),
+        "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 in, e4m3 + e8m0/f32 scales out",
+        "data": "synthetic (seeded N(0,1) as BF16)",
+        "config": {"workload": "quantize: " + QUANT_TEXT,
+                   "l2": "flushed before every call by a 256 MiB write outside the timed events",
+                   "parallelism": f"replicas x{ws}",
+                   "per_call_ms": {o["name"]: round(t, 4) for o, t in zip(ops, per_op_ms)},
+                   "per_call_gbs": {o["name"]: round(o["bytes"] / (t * 1e-3) / 1e9, 1)
+                                    for o, t in zip(ops, per_op_ms)}},
+        "roofline": {"bound": "hbm", "kernel": kernel, "launch": ops[dom]["name"],
+                     "achieved": round(achieved, 1), "peak": round(hbm_peak, 1), "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4),
+                     "peak_source": f"{peak_src} HBM copy bandwidth",
+                     "traffic": recorded_traffic("quantize")},
+        "e2e": None if args.no_e2e else {
+            "value": round(ws * step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "api": "mx_quantize / fp8_group_quantize / fp8_block_quantize with the BF16 input "
+                   "copied host->device and codes + scales device->host inside the timed "
+                   "region, on two copy streams overlapping the neighbouring calls"},
+        "gpu_launches": int(n_launch),
+        "clocks": clk.summary(),
+        "wall_s_timed": round(wall, 3),
+    }
+    if not args.no_cpu_baseline and rank == 0:
+        cache = {}
+        s0, _ = quant_oracle_sample(cache, 1 / 512)            # calibration
+        frac = min(1.0, (1 / 512) * args.cpu_seconds / max(s0, 1e-3))
+        secs, nb = quant_oracle_sample(cache, frac)
+        line["cpu_baseline"] = {"value": round(nb / secs / 1e9, 4), "unit": "GB/s", "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"{frac:.4f} of each call's rows / columns / weight rows "
+                                          f"({nb / 1e6:.1f} MB algorithmic, {secs:.1f} s, "
+                                          f"single-threaded C oracle)"}
+    print(json.dumps(line), flush=True)
+
+
+def run_quantize_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    cache = {}
+    s0, _ = quant_oracle_sample(cache, 1 / 1024)
+    per_step = max(0.2, args.ref_seconds / max(1, args.steps + args.warmup))
+    frac = min(1.0, (1 / 1024) * per_step / max(s0, 1e-3))
+    for _ in range(args.warmup):
+        quant_oracle_sample(cache, frac)
+    secs, nb = 0.0, 0.0
+    for _ in range(args.steps):
+        a, b = quant_oracle_sample(cache, frac)
+        secs += a
+        nb += b
+    value = nb / secs / 1e9
+    line = {
+        "impl": "reference", "metric": QUANT_METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 in, e4m3 + scales out",
+        "data": "synthetic (seeded N(0,1) as BF16)",
+        "config": {"workload": "quantize: " + QUANT_TEXT, "parallelism": "host core"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"per step: {frac:.4f} of each call's rows / columns / weight rows"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- oracle timing
 def time_oracle_sample(spec, rows_per_gemm: int, inputs_cache: dict, nthreads: int):
     """Runs the oracle on `rows_per_gemm` sampled output rows (all columns) of every
@@ -522,7 +801,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mxfp8_dense",
-                    choices=["mxfp8_dense", "mxfp8_256", "mxfp4_dense", "linear_triple", "grouped_fp8"])
+                    choices=["mxfp8_dense", "mxfp8_256", "mxfp4_dense", "linear_triple", "grouped_fp8",
+                             "quantize"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
     ap.add_argument("--grouped-width", type=int, default=0, choices=[0, 128, 256],
@@ -534,7 +814,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.workload == "quantize":
+        run_quantize_reference(args) if args.impl == "reference" else run_quantize(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

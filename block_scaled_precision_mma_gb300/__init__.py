@@ -10,6 +10,8 @@ Functions mirror the C names:
 * :func:`mx_gemm`, :func:`mx_gemm_tiled` -- dense MXFP8 / MXFP4 GEMM, BF16 out.
 * :func:`grouped_fp8_gemm` -- grouped groupwise FP8 GEMM, BF16 out.
 * :func:`mx_scale_relayout`, :func:`mx_scale_tiled_bytes` -- scale-factor relayout.
+* :func:`mx_quantize`, :func:`fp8_group_quantize`, :func:`fp8_block_quantize` -- the
+  quantisers that make the GEMMs' operands from BF16 / FP32 tensors.
 * :func:`device_status`, :func:`reserve_workspace`, :func:`set_wait_limit_ns`,
   :func:`launch_count`, :func:`probe_wait_timeout`, :func:`status_string`.
 """
@@ -24,6 +26,7 @@ import torch
 from .build import LIB_PATH, build
 
 __all__ = ["mx_gemm", "mx_gemm_tiled", "mx_gemm_noalloc", "grouped_fp8_gemm", "mx_scale_relayout",
+           "mx_quantize", "fp8_group_quantize", "fp8_block_quantize",
            "mx_scale_tiled_bytes", "device_status", "reserve_workspace", "set_wait_limit_ns",
            "set_dense_variant", "set_grouped_tile_width",
            "launch_count", "probe_wait_timeout", "status_string", "BsmmaError", "load",
@@ -75,11 +78,15 @@ def load(path: str | None = None):
         lib.bsmma_launch_count.argtypes = []
         lib.bsmma_launch_count.restype = i64
         lib.bsmma_probe_wait_timeout.argtypes = [i64, p]
+        lib.mx_quantize.argtypes = [p, i32, i64, i64, i32, i32, p, p, p]
+        lib.fp8_group_quantize.argtypes = [p, i32, i64, i64, p, i32, p, p, p]
+        lib.fp8_block_quantize.argtypes = [p, i32, i64, i64, i64, p, p, p]
         for name in ("mx_gemm", "mx_gemm_tiled", "mx_gemm_noalloc", "grouped_fp8_gemm",
                      "mx_scale_relayout",
                      "bsmma_reserve_workspace", "bsmma_device_status", "bsmma_set_wait_limit_ns",
                      "bsmma_set_dense_variant", "bsmma_set_grouped_tile_width",
-                     "bsmma_probe_wait_timeout"):
+                     "bsmma_probe_wait_timeout", "mx_quantize", "fp8_group_quantize",
+                     "fp8_block_quantize"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -223,3 +230,58 @@ def status_string(code: int) -> str:
 
 def probe_wait_timeout(limit_ns: int, stream=None) -> int:
     return int(load().bsmma_probe_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+DTYPES = {torch.bfloat16: 0, torch.float32: 1}
+
+
+def _dtype_code(t) -> int:
+    if t.dtype not in DTYPES:
+        raise ValueError("quantiser inputs are bfloat16 or float32")
+    return DTYPES[t.dtype]
+
+
+def mx_quantize(x, fmt="e4m3", colwise=False, codes=None, scales=None, stream=None):
+    """MX quantisation of x[rows, cols] (BF16 or FP32) -> (codes, scales); see
+    ``mx_quantize`` in bsmma.h.  Rowwise: codes [rows, cols] ([rows, cols/2] for e2m1),
+    scales [rows, cols/32].  Columnwise: codes [rows, cols], scales [cols, rows/32]."""
+    rows, cols = x.shape
+    if codes is None:
+        codes = torch.empty((rows, cols // 2 if fmt == "e2m1" else cols), dtype=torch.uint8,
+                            device=x.device)
+    if scales is None:
+        shape = (cols, rows // 32) if colwise else (rows, cols // 32)
+        scales = torch.empty(shape, dtype=torch.uint8, device=x.device)
+    _check(load().mx_quantize(_ptr(x), _dtype_code(x), rows, cols, FORMATS[fmt], int(bool(colwise)),
+                              _ptr(codes), _ptr(scales), _stream(stream)), "mx_quantize")
+    return codes, scales
+
+
+def fp8_group_quantize(x, m_sizes, codes=None, scales=None, stream=None):
+    """Groupwise E4M3 quantisation of activations x[total_M, K] over 1x128 blocks ->
+    (codes [total_M, K], scales float32 [total_M * K/128] in the per-group block layout);
+    m_sizes: int64 [G] on the device.  See ``fp8_group_quantize`` in bsmma.h."""
+    total_M, K = x.shape
+    if codes is None:
+        codes = torch.empty((total_M, K), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(total_M * (K // 128), dtype=torch.float32, device=x.device)
+    _check(load().fp8_group_quantize(_ptr(x) if total_M else None, _dtype_code(x), total_M, K,
+                                     _ptr(m_sizes), m_sizes.numel(),
+                                     _ptr(codes) if total_M else None,
+                                     _ptr(scales) if total_M else None, _stream(stream)),
+           "fp8_group_quantize")
+    return codes, scales
+
+
+def fp8_block_quantize(w, codes=None, scales=None, stream=None):
+    """Blockwise E4M3 quantisation of weights w[G, N, K] over 128x128 blocks ->
+    (codes [G, N, K], scales float32 [G, N/128, K/128]).  See ``fp8_block_quantize``."""
+    G, N, K = w.shape
+    if codes is None:
+        codes = torch.empty((G, N, K), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((G, N // 128, K // 128), dtype=torch.float32, device=w.device)
+    _check(load().fp8_block_quantize(_ptr(w), _dtype_code(w), G, N, K, _ptr(codes), _ptr(scales),
+                                     _stream(stream)), "fp8_block_quantize")
+    return codes, scales

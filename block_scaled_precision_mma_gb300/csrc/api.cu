@@ -282,6 +282,50 @@ bsmma_status grouped_fp8_gemm(const uint8_t* A, const float* sA, const uint8_t* 
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
+bsmma_status mx_quantize(const void* x, bsmma_dtype x_dtype, int64_t rows, int64_t cols,
+                         bsmma_fmt fmt, int colwise, uint8_t* codes, uint8_t* scales,
+                         bsmma_stream stream) {
+  if (x_dtype != BSMMA_BF16 && x_dtype != BSMMA_F32) return BSMMA_ERR_INVALID_ARG;
+  if (fmt != BSMMA_E4M3 && fmt != BSMMA_E5M2 && fmt != BSMMA_E2M1) return BSMMA_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || (colwise != 0 && colwise != 1)) return BSMMA_ERR_INVALID_ARG;
+  if (colwise && fmt == BSMMA_E2M1) return BSMMA_ERR_UNSUPPORTED;
+  if (colwise ? (rows % 32 != 0 || cols % 16 != 0) : (cols % 32 != 0)) return BSMMA_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return BSMMA_OK;
+  if (!x || !codes || !scales) return BSMMA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(codes)) return BSMMA_ERR_MISALIGNED;
+  return launch_mx_quantize(x, x_dtype == BSMMA_F32, rows, cols, fmt, colwise != 0, codes, scales,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+bsmma_status fp8_group_quantize(const void* x, bsmma_dtype x_dtype, int64_t total_M, int64_t K,
+                                const int64_t* m_sizes, int G, uint8_t* codes, float* scales,
+                                bsmma_stream stream) {
+  if (x_dtype != BSMMA_BF16 && x_dtype != BSMMA_F32) return BSMMA_ERR_INVALID_ARG;
+  if (G < 1 || G > 64 || total_M < 0 || K <= 0 || K % 128 != 0) return BSMMA_ERR_INVALID_ARG;
+  if (!m_sizes) return BSMMA_ERR_INVALID_ARG;
+  if (total_M > 0 && (!x || !codes || !scales)) return BSMMA_ERR_INVALID_ARG;
+  if ((total_M + 63) / 64 * (K / 128) >= INT32_MAX) return BSMMA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(m_sizes) & 7u) != 0) return BSMMA_ERR_MISALIGNED;
+  if (total_M > 0 && (!aligned16(x) || !aligned16(codes) ||
+                      (reinterpret_cast<uintptr_t>(scales) & 3u) != 0))
+    return BSMMA_ERR_MISALIGNED;
+  return launch_group_quantize(x, x_dtype == BSMMA_F32, total_M, K, m_sizes, G, codes, scales,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+bsmma_status fp8_block_quantize(const void* w, bsmma_dtype w_dtype, int64_t G, int64_t N,
+                                int64_t K, uint8_t* codes, float* scales, bsmma_stream stream) {
+  if (w_dtype != BSMMA_BF16 && w_dtype != BSMMA_F32) return BSMMA_ERR_INVALID_ARG;
+  if (G < 0 || N < 0 || K < 0 || N % 128 != 0 || K % 128 != 0) return BSMMA_ERR_INVALID_ARG;
+  if (G == 0 || N == 0 || K == 0) return BSMMA_OK;
+  if (G * (N / 128) * (K / 128) >= INT32_MAX) return BSMMA_ERR_INVALID_ARG;
+  if (!w || !codes || !scales) return BSMMA_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u) != 0)
+    return BSMMA_ERR_MISALIGNED;
+  return launch_block_quantize(w, w_dtype == BSMMA_F32, G, N, K, codes, scales,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
 bsmma_status bsmma_reserve_workspace(int64_t bytes, bsmma_stream stream) {
   if (bytes < 0) return BSMMA_ERR_INVALID_ARG;
   void* p = nullptr;

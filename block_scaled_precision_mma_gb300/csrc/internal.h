@@ -59,6 +59,15 @@ bsmma_status launch_grouped(const uint8_t* X, const float* sX, const uint8_t* W,
                             void* D, const int64_t* m_sizes, int64_t total_M, int G, int64_t N,
                             int64_t K, cudaStream_t stream);
 
+// Quantisers (arguments already validated by the entry points).
+bsmma_status launch_mx_quantize(const void* x, bool f32, int64_t rows, int64_t cols, bsmma_fmt fmt,
+                                bool colwise, uint8_t* codes, uint8_t* scales, cudaStream_t stream);
+bsmma_status launch_group_quantize(const void* x, bool f32, int64_t total_M, int64_t K,
+                                   const int64_t* m_sizes, int G, uint8_t* codes, float* scales,
+                                   cudaStream_t stream);
+bsmma_status launch_block_quantize(const void* w, bool f32, int64_t G, int64_t N, int64_t K,
+                                   uint8_t* codes, float* scales, cudaStream_t stream);
+
 inline bsmma_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? BSMMA_OK : BSMMA_ERR_CUDA; }
 
 }  // namespace bsmma

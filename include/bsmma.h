@@ -175,6 +175,64 @@ bsmma_status mx_scale_relayout(const uint8_t* s_plain, int64_t rows, int64_t kbl
 /* Size in bytes of the tiled layout of [rows][kblocks] scales of the given role. */
 int64_t mx_scale_tiled_bytes(int64_t rows, int64_t kblocks, bsmma_scale_role role);
 
+/* Element type of the high-precision inputs of the quantisers. */
+typedef enum { BSMMA_BF16 = 0, BSMMA_F32 = 1 } bsmma_dtype;
+
+/*
+ * mx_quantize -- MX quantisation, the step that makes mx_gemm's operands.  Source:
+ * "[gfx1250] Add MXFP4 GEMM support to FlyDSL backend", the MXFP4 test helpers and
+ * their review (rowwise and columnwise data are quantised separately, each the
+ * layout one GEMM operand reads; BF16 input, FP32 input asked for as well).
+ *   x        [rows][cols] BF16 or FP32 (x_dtype), row-major.
+ *   Per block of 32 consecutive values along the quantised dimension:
+ *     amax = max |x|;  e = floor(log2 amax) - emax, emax = 8 (E4M3), 15 (E5M2) or
+ *     2 (E2M1), clamped to [-127, 127];  scale code = e + 127 (127 if amax == 0);
+ *     code = round-to-nearest-even of the FP32 product x * 2^-e, saturated to the
+ *     largest finite value (448, 57344, 6), with the sign bit of x.
+ *   colwise == 0 (rowwise): blocks run along cols.  codes [rows][cols] (E2M1:
+ *     [rows][cols/2], the even column in the low nibble); scales [rows][cols/32].
+ *     This is mx_gemm's A or B of an NT GEMM, its A of NN, ...: an operand whose
+ *     reduction dimension is contiguous.
+ *   colwise == 1: blocks run along rows.  codes [rows][cols] (same layout as x);
+ *     scales [cols][rows/32] (indexed by column, then row block).  This is the
+ *     MN-major B of NN and the A and B of TN.  E4M3 and E5M2 only.
+ * Preconditions: 16-byte-aligned x and codes; rowwise cols % 32 == 0, columnwise
+ *   rows % 32 == 0 and cols % 16 == 0.  Inputs must be finite.  One launch (none
+ *   for an empty tensor).
+ */
+bsmma_status mx_quantize(const void* x, bsmma_dtype x_dtype, int64_t rows, int64_t cols,
+                         bsmma_fmt fmt, int colwise, uint8_t* codes, uint8_t* scales,
+                         bsmma_stream stream);
+
+/*
+ * fp8_group_quantize -- groupwise E4M3 quantisation of the grouped GEMM's activations
+ * (quantize_fp8_group(m_sizes=...) in "Add FlyDSL grouped groupwise FP8 GEMM for
+ * ROCm", and the commit that fixes the activation-scale layout).
+ *   x [total_M][K] BF16 or FP32; per row and 128-K block: s = amax / 448 (1 when
+ *   amax == 0, both FP32), code = RNE-saturate(x / s) in E4M3 (FP32 division).
+ *   codes [total_M][K] E4M3;  scales FP32 in the per-group block layout that
+ *   grouped_fp8_gemm reads: group g starts at M_start_g*(K/128) and holds (local row
+ *   l, block kb) at l + kb*m_g.
+ *   m_sizes: int64 [G] in DEVICE memory; if an entry is negative or the entries do
+ *   not sum to total_M, nothing is written and BSMMA_DEV_BAD_MSIZES is latched.
+ * Preconditions: K % 128 == 0, 1 <= G <= 64, total_M >= 0, 16-byte-aligned x and
+ *   codes.  One launch.
+ */
+bsmma_status fp8_group_quantize(const void* x, bsmma_dtype x_dtype, int64_t total_M, int64_t K,
+                                const int64_t* m_sizes, int G, uint8_t* codes, float* scales,
+                                bsmma_stream stream);
+
+/*
+ * fp8_block_quantize -- blockwise E4M3 quantisation of the grouped GEMM's weights
+ * (128x128 blocks; same source).
+ *   w [G][N][K] BF16 or FP32; per 128x128 block: s = amax / 448 (1 when amax == 0),
+ *   code = RNE-saturate(w / s).  codes [G][N][K] E4M3;  scales FP32 [G][N/128][K/128].
+ * Preconditions: N % 128 == 0, K % 128 == 0, G >= 0, 16-byte-aligned w and codes.
+ *   One launch.
+ */
+bsmma_status fp8_block_quantize(const void* w, bsmma_dtype w_dtype, int64_t G, int64_t N,
+                                int64_t K, uint8_t* codes, float* scales, bsmma_stream stream);
+
 /* Grows the current (device, stream) scale workspace to at least `bytes`
  * (call before capturing mx_gemm into a CUDA graph). */
 bsmma_status bsmma_reserve_workspace(int64_t bytes, bsmma_stream stream);

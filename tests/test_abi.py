@@ -30,7 +30,8 @@ def declared_functions():
 def test_header_declares_entry_points():
     names = declared_functions()
     for n in ("mx_gemm", "mx_gemm_tiled", "grouped_fp8_gemm", "mx_scale_relayout",
-              "mx_scale_tiled_bytes", "bsmma_device_status", "bsmma_status_string"):
+              "mx_scale_tiled_bytes", "bsmma_device_status", "bsmma_status_string",
+              "mx_quantize", "fp8_group_quantize", "fp8_block_quantize"):
         assert n in names
 
 
@@ -103,6 +104,40 @@ def test_relayout_validation(lib):
     assert lib.mx_scale_relayout(FAKE, 128, 8, 2, FAKE, None) == 1      # bad role
     assert lib.mx_scale_relayout(FAKE, 128, 8, 1, ODD, None) == 3
     assert lib.mx_scale_relayout(None, 0, 8, 0, None, None) == 0
+
+
+@pytest.mark.parametrize("args,expect", [
+    # (x, x_dtype, rows, cols, fmt, colwise, codes, scales)
+    ((FAKE, 0, 64, 48, 0, 0, FAKE, FAKE), 1),       # rowwise cols % 32
+    ((FAKE, 0, 48, 64, 0, 1, FAKE, FAKE), 1),       # columnwise rows % 32
+    ((FAKE, 0, 64, 40, 0, 1, FAKE, FAKE), 1),       # columnwise cols % 16
+    ((FAKE, 2, 64, 64, 0, 0, FAKE, FAKE), 1),       # bad dtype
+    ((FAKE, 0, 64, 64, 3, 0, FAKE, FAKE), 1),       # bad format
+    ((FAKE, 0, 64, 64, 0, 2, FAKE, FAKE), 1),       # bad colwise flag
+    ((FAKE, 0, 64, 64, 2, 1, FAKE, FAKE), 2),       # columnwise E2M1
+    ((ODD, 0, 64, 64, 0, 0, FAKE, FAKE), 3),        # x misaligned
+    ((FAKE, 1, 64, 64, 1, 0, ODD, FAKE), 3),        # codes misaligned
+    ((None, 0, 64, 64, 0, 0, FAKE, FAKE), 1),       # null x
+    ((None, 0, 0, 64, 0, 0, None, None), 0),        # empty: no-op
+    ((FAKE, 0, -1, 64, 0, 0, FAKE, FAKE), 1),       # negative rows
+])
+def test_mx_quantize_validation(lib, args, expect):
+    assert lib.mx_quantize(*args, None) == expect
+
+
+def test_group_block_quantize_validation(lib):
+    # (x, dtype, total_M, K, m_sizes, G, codes, scales)
+    assert lib.fp8_group_quantize(FAKE, 0, 256, 200, FAKE, 8, FAKE, FAKE, None) == 1   # K % 128
+    assert lib.fp8_group_quantize(FAKE, 0, 256, 256, FAKE, 0, FAKE, FAKE, None) == 1   # G = 0
+    assert lib.fp8_group_quantize(FAKE, 0, 256, 256, None, 8, FAKE, FAKE, None) == 1   # null m_sizes
+    assert lib.fp8_group_quantize(FAKE, 0, 256, 256, FAKE + 4, 8, FAKE, FAKE, None) == 3
+    assert lib.fp8_group_quantize(ODD, 1, 256, 256, FAKE, 8, FAKE, FAKE, None) == 3
+    assert lib.fp8_group_quantize(FAKE, 0, 256, 256, FAKE, 8, FAKE, FAKE + 2, None) == 3
+    # (w, dtype, G, N, K, codes, scales)
+    assert lib.fp8_block_quantize(FAKE, 0, 2, 200, 256, FAKE, FAKE, None) == 1         # N % 128
+    assert lib.fp8_block_quantize(FAKE, 0, -1, 256, 256, FAKE, FAKE, None) == 1
+    assert lib.fp8_block_quantize(FAKE, 0, 2, 256, 256, ODD, FAKE, None) == 3
+    assert lib.fp8_block_quantize(None, 0, 0, 256, 256, None, None, None) == 0         # empty
 
 
 def test_wait_limit(lib):

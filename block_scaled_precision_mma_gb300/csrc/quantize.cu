@@ -284,11 +284,16 @@ __global__ void __launch_bounds__(kThreads) group_quant_kernel(const void* x, in
       if (r >= total_M) continue;     // whole half-warps (the row is shared by 16 threads)
       const float s = group_scale(amax);
       __stcs(reinterpret_cast<uint2*>(codes + r * K + kb * 128 + seg * 8), e4m3_codes8(v[i], s));
-      if (seg == 0) {
-        int g = 0;
-        while (g + 1 < G && start[g + 1] <= r) ++g;   // the group owning row r (empty ones own none)
-        sx[start[g] * KB + (r - start[g]) + static_cast<int64_t>(kb) * size[g]] = s;
+      // the group owning row r: the last g with start[g] <= r (an empty group shares its
+      // start with the next one, so it is never the last), by a binary search every lane
+      // runs (no divergent scan)
+      int lo = 0, hi = G;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (start[mid] <= r) lo = mid;
+        else hi = mid;
       }
+      if (seg == 0) sx[start[lo] * KB + (r - start[lo]) + static_cast<int64_t>(kb) * size[lo]] = s;
     }
   }
 }

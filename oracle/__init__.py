@@ -19,6 +19,8 @@ this module compiles it with gcc and exposes numpy-friendly wrappers:
   kernels copy into tensor memory, for the scales of op(A) (role 0) and op(B)
   (role 1).
 * :func:`decode_table` -- the decode tables the oracle uses.
+* :func:`bias_act` -- act(D + bias) after the GEMM (ReLU, GELU in its erf form, SiLU;
+  the follow-up named in "[gfx1250] Add MXFP4 GEMM support to FlyDSL backend").
 * :func:`mx_quantize`, :func:`fp8_group_quantize`, :func:`fp8_block_quantize` -- the
   quantisers before the GEMM: MX rowwise / columnwise with E8M0 block scales ("[gfx1250]
   Add MXFP4 GEMM support to FlyDSL backend", the MXFP4 test helpers and their review),
@@ -85,6 +87,8 @@ def bind(path: str):
     lib.oracle_fp8_group_quantize.restype = i32
     lib.oracle_fp8_block_quantize.argtypes = [p, i64, i64, i64, p, p]
     lib.oracle_fp8_block_quantize.restype = i32
+    lib.oracle_bias_act.argtypes = [p, i64, i64, p, i32]
+    lib.oracle_bias_act.restype = i32
     return lib
 
 
@@ -231,3 +235,21 @@ def fp8_block_quantize(w, lib=None):
     if rc != 0:
         raise ValueError("oracle_fp8_block_quantize: bad arguments")
     return codes, sw
+
+
+ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2, "silu": 3}
+
+
+def bias_act(D, bias=None, act="none", lib=None) -> np.ndarray:
+    """act(D + bias) in FP64 for an FP64 D[rows, N] (bias: N values, e.g. a BF16 vector's
+    FP32 values, or None)."""
+    D = np.array(D, dtype=np.float64, copy=True, order="C")
+    rows, N = D.shape
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    if b is not None:
+        assert b.size == N
+    rc = _load(lib).oracle_bias_act(_ptr(D), rows, N, None if b is None else _ptr(b),
+                                    ACTIVATIONS[act])
+    if rc != 0:
+        raise ValueError("oracle_bias_act: bad arguments")
+    return D

@@ -519,3 +519,26 @@ int oracle_fp8_block_quantize(const float* w, int64_t G, int64_t N, int64_t K, u
       }
   return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Bias and activation after the GEMM ("[gfx1250] Add MXFP4 GEMM support to   */
+/* FlyDSL backend", Description: activation and bias are a follow-up to the   */
+/* plain GEMM).  D[i][n] <- act(D[i][n] + bias[n]) in FP64, bias optional      */
+/* (FP32 values of the BF16 bias).  act: 0 none, 1 ReLU, 2 GELU (erf form:     */
+/* x * (1 + erf(x / sqrt 2)) / 2), 3 SiLU (x / (1 + exp(-x))).                 */
+/* ------------------------------------------------------------------------ */
+int oracle_bias_act(double* D, int64_t rows, int64_t N, const float* bias, int act) {
+  if (act < 0 || act > 3 || rows < 0 || N < 0) return -1;
+  for (int64_t i = 0; i < rows; ++i)
+    for (int64_t n = 0; n < N; ++n) {
+      double v = D[i * N + n] + (bias ? (double)bias[n] : 0.0);
+      switch (act) {
+        case 1: v = v > 0.0 ? v : 0.0; break;
+        case 2: v = 0.5 * v * (1.0 + erf(v / sqrt(2.0))); break;
+        case 3: v = v / (1.0 + exp(-v)); break;
+        default: break;
+      }
+      D[i * N + n] = v;
+    }
+  return 0;
+}

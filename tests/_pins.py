@@ -496,7 +496,30 @@ def pin_group_quant(lib=None):
     assert np.array_equal(cw, synthetic.encode(y, "e4m3").reshape(2, 256, 256))
 
 
+# ---------------------------------------------------------------- bias and activation
+def pin_bias_act(lib=None):
+    """Closed-form points and torch's float64 functional activations."""
+    x = np.array([[-3.0, -1.0, 0.0, 0.5, 1.0, 2.0, 7.5, -0.25]])
+    assert np.array_equal(oracle.bias_act(x, act="relu", lib=lib), np.maximum(x, 0.0))
+    g = oracle.bias_act(np.array([[1.0, 0.0, -1.0]]), act="gelu", lib=lib)[0]
+    assert abs(g[0] - 0.8413447460685429) < 1e-15 and g[1] == 0.0 and abs(g[2] + 0.15865525393145707) < 1e-15
+    s = oracle.bias_act(np.array([[1.0, 0.0]]), act="silu", lib=lib)[0]
+    assert abs(s[0] - 0.7310585786300049) < 1e-15 and s[1] == 0.0
+    rng = np.random.default_rng(23)
+    D = rng.standard_normal((5, 16)) * 4
+    b = rng.standard_normal(16).astype(np.float32)
+    t = torch.from_numpy(D + b.astype(np.float64))
+    F = torch.nn.functional
+    want = {"none": t, "relu": F.relu(t), "gelu": F.gelu(t), "silu": F.silu(t)}
+    for act, ref in want.items():
+        got = oracle.bias_act(D, b, act, lib=lib)
+        assert np.allclose(got, ref.numpy(), rtol=1e-14, atol=1e-14), act
+    # bias is added per column (a row vector), not per row
+    got = oracle.bias_act(np.zeros((2, 3)), np.array([1.0, 2.0, 3.0], dtype=np.float32), lib=lib)
+    assert np.array_equal(got, np.array([[1.0, 2.0, 3.0], [1.0, 2.0, 3.0]]))
+
+
 ALL_PINS = [pin_decode_points, pin_decode_vs_torch, pin_dense_bruteforce, pin_dense_unit_scales,
             pin_dense_pow2, pin_dense_layouts, pin_grouped_concat, pin_grouped_g1_transpose,
             pin_grouped_probes, pin_wide_relayout, pin_quant_closed_form, pin_quant_vs_independent,
-            pin_quant_roundtrip, pin_quant_error_bound, pin_group_quant]
+            pin_quant_roundtrip, pin_quant_error_bound, pin_group_quant, pin_bias_act]

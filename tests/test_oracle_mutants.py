@@ -45,6 +45,10 @@ MUTANTS = [
     ("group_block_rows", "for (int64_t t = 0; t < 128; ++t) {\n          const float m = fabsf(x[r * K + kb * 128 + t]);",
      "for (int64_t t = 0; t < 64; ++t) {\n          const float m = fabsf(x[r * K + kb * 128 + t]);"),
     ("group_scale_no_floor", "return s > tiny ? s : tiny;", "return s;"),
+    ("bias_per_row", "D[i * N + n] + (bias ? (double)bias[n] : 0.0)", "D[i * N + n] + (bias ? (double)bias[i % N] : 0.0)"),
+    ("gelu_tanh_scale", "0.5 * v * (1.0 + erf(v / sqrt(2.0)))", "0.5 * v * (1.0 + erf(v / 2.0))"),
+    ("silu_sign", "v = v / (1.0 + exp(-v));", "v = v / (1.0 + exp(v));"),
+    ("relu_leaky", "v = v > 0.0 ? v : 0.0;", "v = v > 0.0 ? v : 0.01 * v;"),
     ("block_sw_kmajor", "sw[(g * (N / 128) + nb) * (K / 128) + kb] = s;", "sw[(g * (K / 128) + kb) * (N / 128) + nb] = s;"),
 ]
 

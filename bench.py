@@ -10,7 +10,8 @@ MiB write) before every GEMM, outside the timed events.
 
 Other workloads (``--workload``): mxfp4_dense (8192^3 and 1024x14336x4096),
 grouped_fp8 (G=8, totM 128/1024/16384 x three (N,K)), linear_triple (fwd/dgrad/
-wgrad of X[8192,4096], W[14336,4096], dY[8192,14336]), mxfp8_256 (256^3), and
+wgrad of X[8192,4096], W[14336,4096], dY[8192,14336]), mxfp8_256 (256^3),
+mxfp8_bias_gelu (the default GEMMs with a fused bias + GELU output stage), and
 quantize (the quantisers that make the operands, in GB/s against HBM bandwidth).
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead
@@ -47,6 +48,11 @@ def workload_spec(name: str):
                 dict(kind="dense", M=4096, N=4096, K=14336, layout="NT", a="e4m3", b="e4m3", key=(2, 11)),
                 dict(kind="dense", M=8192, N=8192, K=8192, layout="NT", a="e4m3", b="e4m3", key=(2, 12)),
                 dict(kind="dense", M=8192, N=8192, K=8192, layout="NT", a="e4m3", b="e5m2", key=(2, 13))]
+    if name == "mxfp8_bias_gelu":
+        out = workload_spec("mxfp8_dense")
+        for g in out:
+            g.update(act="gelu", bias=True)
+        return out
     if name == "mxfp8_256":
         return [dict(kind="dense", M=256, N=256, K=256, layout="NT", a="e4m3", b="e4m3", key=(1, 0))]
     if name == "mxfp4_dense":
@@ -66,6 +72,8 @@ def workload_spec(name: str):
 WORKLOAD_TEXT = {
     "mxfp8_dense": "MXFP8 dense NT: (4096,14336,4096),(4096,4096,14336),(8192,8192,8192) E4M3xE4M3 "
                    "+ (8192,8192,8192) E4M3xE5M2; E8M0 per 32 along K; BF16 out",
+    "mxfp8_bias_gelu": "the mxfp8_dense GEMMs with the fused output stage: D = GELU(acc + bias[n]) "
+                       "(erf form), BF16 bias [N] from seeded N(0,1)",
     "mxfp8_256": "MXFP8 NT 256^3 E4M3xE4M3",
     "mxfp4_dense": "MXFP4 dense NT: 8192^3 and (1024,14336,4096), packed E2M1, E8M0 per 32",
     "linear_triple": "MXFP8 Linear triple: fwd NT (8192,14336,4096), dgrad NN (8192,4096,14336), "
@@ -91,7 +99,12 @@ def make_inputs(g):
     """Host numpy operands for one GEMM description."""
     import synthetic
     if g["kind"] == "dense":
-        return synthetic.mx_operands(g["key"], g["M"], g["N"], g["K"], g["layout"], g["a"], g["b"])
+        c = synthetic.mx_operands(g["key"], g["M"], g["N"], g["K"], g["layout"], g["a"], g["b"])
+        if g.get("bias"):
+            import torch
+            c["bias"] = torch.from_numpy(synthetic.normal((*g["key"], 9), (g["N"],))).to(
+                torch.bfloat16).float().numpy()
+        return c
     if g["kind"] == "triple":
         global _TRIPLE
         if "_TRIPLE" not in globals() or _TRIPLE is None:
@@ -260,6 +273,8 @@ def run_ours(args):
         else:
             t = {k: torch.from_numpy(np.ascontiguousarray(c[k])).to(dev) for k in ("A", "sA", "B", "sB")}
             t["D"] = torch.empty((g["M"], g["N"]), dtype=torch.bfloat16, device=dev)
+            t["bias"] = (torch.from_numpy(c["bias"]).to(torch.bfloat16).to(dev)
+                         if "bias" in c else None)
             t["tA"] = torch.empty(bs.mx_scale_tiled_bytes(g["M"], g["K"] // 32, "A"), dtype=torch.uint8,
                                   device=dev)
             t["tB"] = torch.empty(bs.mx_scale_tiled_bytes(g["N"], g["K"] // 32, "B"), dtype=torch.uint8,
@@ -286,7 +301,8 @@ def run_ours(args):
             bs.mx_scale_relayout(t["sB"], "B", out=t["tB"])
             ev[1].record(stream)
             bs.mx_gemm_tiled(t["A"], t["tA"], t["B"], t["tB"], g["layout"], g["a"], g["b"],
-                             out=t["D"], M=g["M"], N=g["N"], K=g["K"])
+                             out=t["D"], M=g["M"], N=g["N"], K=g["K"], bias=t.get("bias"),
+                             act=g.get("act", "none"))
         ev[2].record(stream)
 
     def step(events):
@@ -352,7 +368,8 @@ def run_ours(args):
                 bs.grouped_fp8_gemm(t["X"], t["sX"], t["W"], t["sW"], t["m_sizes"], out=t["D"])
             else:
                 bs.mx_gemm(t["A"], t["sA"], t["B"], t["sB"], g["layout"], g["a"], g["b"],
-                           out=t["D"], M=g["M"], N=g["N"], K=g["K"])
+                           out=t["D"], M=g["M"], N=g["N"], K=g["K"], bias=t.get("bias"),
+                           act=g.get("act", "none"))
             comp_done[i].record(stream)
             with torch.cuda.stream(d2h_stream):
                 d2h_stream.wait_event(comp_done[i])
@@ -738,8 +755,10 @@ def time_oracle_sample(spec, rows_per_gemm: int, inputs_cache: dict, nthreads: i
             M = c["M"]
             rows = np.random.default_rng([8, i]).choice(M, size=min(rows_per_gemm, M), replace=False)
             t0 = time.perf_counter()
-            oracle.mx_gemm(c["A"], c["sA"], c["B"], c["sB"], c["M"], c["N"], c["K"], c["layout"],
-                           c["a_fmt"], c["b_fmt"], rows=np.sort(rows), nthreads=nthreads)
+            d = oracle.mx_gemm(c["A"], c["sA"], c["B"], c["sB"], c["M"], c["N"], c["K"], c["layout"],
+                               c["a_fmt"], c["b_fmt"], rows=np.sort(rows), nthreads=nthreads)
+            if g.get("act"):
+                oracle.bias_act(d, c.get("bias"), g["act"])
             secs += time.perf_counter() - t0
             flops += 2.0 * len(rows) * c["N"] * c["K"]
     return secs, flops
@@ -801,8 +820,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mxfp8_dense",
-                    choices=["mxfp8_dense", "mxfp8_256", "mxfp4_dense", "linear_triple", "grouped_fp8",
-                             "quantize"])
+                    choices=["mxfp8_dense", "mxfp8_bias_gelu", "mxfp8_256", "mxfp4_dense",
+                             "linear_triple", "grouped_fp8", "quantize"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
     ap.add_argument("--grouped-width", type=int, default=0, choices=[0, 128, 256],

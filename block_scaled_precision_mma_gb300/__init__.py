@@ -7,7 +7,8 @@ shared library is missing or fails to load, every call raises.
 
 Functions mirror the C names:
 
-* :func:`mx_gemm`, :func:`mx_gemm_tiled` -- dense MXFP8 / MXFP4 GEMM, BF16 out.
+* :func:`mx_gemm`, :func:`mx_gemm_tiled` -- dense MXFP8 / MXFP4 GEMM, BF16 out, optionally
+  with a fused per-column bias and activation.
 * :func:`grouped_fp8_gemm` -- grouped groupwise FP8 GEMM, BF16 out.
 * :func:`mx_scale_relayout`, :func:`mx_scale_tiled_bytes` -- scale-factor relayout.
 * :func:`mx_quantize`, :func:`fp8_group_quantize`, :func:`fp8_block_quantize` -- the
@@ -33,6 +34,7 @@ __all__ = ["mx_gemm", "mx_gemm_tiled", "mx_gemm_noalloc", "grouped_fp8_gemm", "m
            "LAYOUTS", "FORMATS", "ROLES", "build", "LIB_PATH"]
 
 LAYOUTS = {"NT": 0, "NN": 1, "TN": 2}
+ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2, "silu": 3}
 ROLES = {"A": 0, "B": 1}      # scales of op(A) rows / of op(B) rows
 FORMATS = {"e4m3": 0, "e5m2": 1, "e2m1": 2}
 STATUS = ["BSMMA_OK", "BSMMA_ERR_INVALID_ARG", "BSMMA_ERR_UNSUPPORTED", "BSMMA_ERR_MISALIGNED",
@@ -79,6 +81,8 @@ def load(path: str | None = None):
         lib.bsmma_launch_count.restype = i64
         lib.bsmma_probe_wait_timeout.argtypes = [i64, p]
         lib.mx_quantize.argtypes = [p, i32, i64, i64, i32, i32, p, p, p]
+        lib.mx_gemm_bias_act.argtypes = [p, p, p, p, p, i32, p, i64, i64, i64, i32, i32, i32, p]
+        lib.mx_gemm_tiled_bias_act.argtypes = [p, p, p, p, p, i32, p, i64, i64, i64, i32, i32, i32, p]
         lib.fp8_group_quantize.argtypes = [p, i32, i64, i64, p, i32, p, p, p]
         lib.fp8_block_quantize.argtypes = [p, i32, i64, i64, i64, p, p, p]
         for name in ("mx_gemm", "mx_gemm_tiled", "mx_gemm_noalloc", "grouped_fp8_gemm",
@@ -86,7 +90,7 @@ def load(path: str | None = None):
                      "bsmma_reserve_workspace", "bsmma_device_status", "bsmma_set_wait_limit_ns",
                      "bsmma_set_dense_variant", "bsmma_set_grouped_tile_width",
                      "bsmma_probe_wait_timeout", "mx_quantize", "fp8_group_quantize",
-                     "fp8_block_quantize"):
+                     "fp8_block_quantize", "mx_gemm_bias_act", "mx_gemm_tiled_bias_act"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -113,8 +117,10 @@ def _check(code: int, where: str):
 
 
 def mx_gemm(A, sA, B, sB, layout="NT", a_fmt="e4m3", b_fmt="e4m3", out=None, M=None, N=None,
-            K=None, stream=None, tiled=False):
-    """D = op(A) . op(B)^T in BF16 for MX operands (see ``mx_gemm`` in bsmma.h).
+            K=None, stream=None, tiled=False, bias=None, act="none"):
+    """D = op(A) . op(B)^T in BF16 for MX operands (see ``mx_gemm`` in bsmma.h); with a
+    BF16 ``bias`` [N] and/or ``act`` ('relu', 'gelu', 'silu') the output stage computes
+    act(acc + bias) before rounding (``mx_gemm_bias_act``).
 
     A, B: 1-byte tensors in the storage layout of `layout` (FP4 packed, NT only);
     sA [M, K/32], sB [N, K/32] uint8 E8M0 codes (or tiled buffers when
@@ -134,6 +140,14 @@ def mx_gemm(A, sA, B, sB, layout="NT", a_fmt="e4m3", b_fmt="e4m3", out=None, M=N
         K = kk * 2 if fp4 else kk
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if bias is not None or act != "none":
+        fn = load().mx_gemm_tiled_bias_act if tiled else load().mx_gemm_bias_act
+        if bias is not None and (bias.dtype != torch.bfloat16 or bias.numel() != N):
+            raise ValueError("bias must be a BF16 vector of N values")
+        _check(fn(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(bias), ACTIVATIONS[act], _ptr(out),
+                  M, N, K, LAYOUTS[layout], FORMATS[a_fmt], FORMATS[b_fmt], _stream(stream)),
+               "mx_gemm_bias_act")
+        return out
     fn = load().mx_gemm_tiled if tiled else load().mx_gemm
     _check(fn(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(out), M, N, K, LAYOUTS[layout],
               FORMATS[a_fmt], FORMATS[b_fmt], _stream(stream)),
@@ -156,10 +170,10 @@ def mx_gemm_noalloc(A, sA, B, sB, layout="NT", a_fmt="e4m3", b_fmt="e4m3", out=N
 
 
 def mx_gemm_tiled(A, sA_tiled, B, sB_tiled, layout="NT", a_fmt="e4m3", b_fmt="e4m3", out=None,
-                  M=None, N=None, K=None, stream=None):
+                  M=None, N=None, K=None, stream=None, bias=None, act="none"):
     """``mx_gemm`` with scales already relayouted by :func:`mx_scale_relayout`."""
     return mx_gemm(A, sA_tiled, B, sB_tiled, layout, a_fmt, b_fmt, out, M, N, K, stream,
-                   tiled=True)
+                   tiled=True, bias=bias, act=act)
 
 
 def grouped_fp8_gemm(X, sX, W, sW, m_sizes, out=None, stream=None):

@@ -15,6 +15,7 @@
 #include <mutex>
 #include <vector>
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -212,6 +213,42 @@ bsmma_status validate_dense(const void* A, const void* sA, const void* B, const 
   return BSMMA_OK;
 }
 
+// Validation of the fused output stage's extra arguments.
+bsmma_status check_epilogue(const void* bias, bsmma_activation act) {
+  if (act < BSMMA_ACT_NONE || act > BSMMA_ACT_SILU) return BSMMA_ERR_INVALID_ARG;
+  if (bias && !aligned16(bias)) return BSMMA_ERR_MISALIGNED;
+  return BSMMA_OK;
+}
+
+namespace {
+// D[m][n] = act(bias[n]) (the output stage of an all-zero accumulator, K == 0).
+__global__ void bias_act_fill_kernel(Epilogue e, __nv_bfloat16* D, int64_t M, int64_t N) {
+  const uint32_t zero[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  const int64_t vecs = M * (N / 8);
+  for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < vecs;
+       v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t m = v / (N / 8), c = (v - m * (N / 8)) * 8;
+    store8(D + m * N + c, zero, c, e);
+  }
+}
+}  // namespace
+
+// K == 0: no products, so D = act(bias) per column (zero without a bias: every activation
+// maps 0 to 0).
+bsmma_status zero_k_epilogue(const void* bias, bsmma_activation act, void* D, int64_t M, int64_t N,
+                             cudaStream_t s) {
+  if (!bias) return cuda_ok(cudaMemsetAsync(D, 0, static_cast<size_t>(M * N * 2), s));
+  bsmma_status st;
+  const DeviceInfo* dev = current_device(&st);
+  if (!dev) return st;
+  Epilogue e;
+  e.bias = static_cast<const __nv_bfloat16*>(bias);
+  e.act = static_cast<int>(act);
+  bias_act_fill_kernel<<<dev->sm_count * 4, 256, 0, s>>>(e, static_cast<__nv_bfloat16*>(D), M, N);
+  count_launches(1);
+  return cuda_ok(cudaGetLastError());
+}
+
 }  // namespace bsmma
 
 using namespace bsmma;
@@ -264,6 +301,43 @@ bsmma_status mx_gemm(const void* A, const uint8_t* sA, const void* B, const uint
   st = launch_wide_relayout(sA, M, ta, sB, N, tb, K / 32, s);
   if (st != BSMMA_OK) return st;
   return launch_mx_gemm(A, ta, B, tb, D, M, N, K, layout, a_fmt, b_fmt, s);
+}
+
+
+bsmma_status mx_gemm_tiled_bias_act(const void* A, const uint8_t* sA_tiled, const void* B,
+                                    const uint8_t* sB_tiled, const void* bias,
+                                    bsmma_activation act, void* D, int64_t M, int64_t N,
+                                    int64_t K, bsmma_layout layout, bsmma_fmt a_fmt,
+                                    bsmma_fmt b_fmt, bsmma_stream stream) {
+  bsmma_status st = validate_dense(A, sA_tiled, B, sB_tiled, D, M, N, K, layout, a_fmt, b_fmt);
+  if (st == BSMMA_OK) st = check_epilogue(bias, act);
+  if (st != BSMMA_OK || M == 0 || N == 0) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return zero_k_epilogue(bias, act, D, M, N, s);
+  return launch_mx_gemm(A, sA_tiled, B, sB_tiled, D, M, N, K, layout, a_fmt, b_fmt, s, bias,
+                        static_cast<int>(act));
+}
+
+bsmma_status mx_gemm_bias_act(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
+                              const void* bias, bsmma_activation act, void* D, int64_t M,
+                              int64_t N, int64_t K, bsmma_layout layout, bsmma_fmt a_fmt,
+                              bsmma_fmt b_fmt, bsmma_stream stream) {
+  bsmma_status st = validate_dense(A, sA, B, sB, D, M, N, K, layout, a_fmt, b_fmt);
+  if (st == BSMMA_OK) st = check_epilogue(bias, act);
+  if (st != BSMMA_OK || M == 0 || N == 0) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return zero_k_epilogue(bias, act, D, M, N, s);
+  const int64_t bytes_a = align_up(wide_scale_bytes(M, K / 32, 0), 256);
+  const int64_t bytes_b = wide_scale_bytes(N, K / 32, 1);
+  void* ws = nullptr;
+  st = get_workspace(bytes_a + bytes_b, s, &ws);
+  if (st != BSMMA_OK) return st;
+  uint8_t* ta = static_cast<uint8_t*>(ws);
+  uint8_t* tb = ta + bytes_a;
+  st = launch_wide_relayout(sA, M, ta, sB, N, tb, K / 32, s);
+  if (st != BSMMA_OK) return st;
+  return launch_mx_gemm(A, ta, B, tb, D, M, N, K, layout, a_fmt, b_fmt, s, bias,
+                        static_cast<int>(act));
 }
 
 bsmma_status grouped_fp8_gemm(const uint8_t* A, const float* sA, const uint8_t* B,

@@ -48,13 +48,15 @@ bsmma_status launch_wide_relayout(const uint8_t* sa, int64_t rows_a, uint8_t* ou
                                   int64_t kblocks, cudaStream_t stream);
 
 // Launchers (arguments already validated by the entry points).
+// bias: BF16 [N] or nullptr; act: bsmma_activation (0 = none).
 bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, const uint8_t* sfb,
                             void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
-                            bsmma_fmt a_fmt, bsmma_fmt b_fmt, cudaStream_t stream);
+                            bsmma_fmt a_fmt, bsmma_fmt b_fmt, cudaStream_t stream,
+                            const void* bias = nullptr, int act = 0);
 bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B,
                                 const uint8_t* sfb, void* D, int64_t M, int64_t N, int64_t K,
                                 bsmma_layout layout, bsmma_fmt a_fmt, bsmma_fmt b_fmt,
-                                cudaStream_t stream);
+                                cudaStream_t stream, const void* bias = nullptr, int act = 0);
 bsmma_status launch_grouped(const uint8_t* X, const float* sX, const uint8_t* W, const float* sW,
                             void* D, const int64_t* m_sizes, int64_t total_M, int G, int64_t N,
                             int64_t K, cudaStream_t stream);

@@ -24,6 +24,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "epilogue.cuh"
 #include "ptx.cuh"
 
 namespace bsmma {
@@ -54,6 +55,7 @@ struct Cfg {
 
 struct DenseParams {
   __nv_bfloat16* D;
+  Epilogue epi;         // optional bias and activation
   int64_t M, N;
   int sfa_kq;               // row-scale chunks per 128-row block
   int sfb_kg;               // column-scale blocks per 256-column block
@@ -103,7 +105,9 @@ __device__ __forceinline__ void tc_cp_wide(uint32_t taddr, uint64_t sdesc) {
 
 // 10 warps share an SM's four register-file quarters (16384 registers each) as
 // 3+3+2+2 warps, so a thread may hold at most 16384 / (3 * 32) = 170 registers.
-template <bool FP4, bool A_MN, bool B_MN, bool PAIR>
+// EPI: the output stage adds a bias and / or applies an activation (a separate
+// instantiation, so the plain GEMM's registers and code are unchanged).
+template <bool FP4, bool A_MN, bool B_MN, bool PAIR, bool EPI>
 __global__ void __maxnreg__(168)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSFA,
@@ -339,12 +343,16 @@ __global__ void __maxnreg__(168)
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             const int o = c * 32 + v * 8;
-            if (col0 + o < p.N)
-              st_global_v4_cs(out + o,
-                              pack_bf16x2(__uint_as_float(r[c][v * 8 + 0]), __uint_as_float(r[c][v * 8 + 1])),
-                              pack_bf16x2(__uint_as_float(r[c][v * 8 + 2]), __uint_as_float(r[c][v * 8 + 3])),
-                              pack_bf16x2(__uint_as_float(r[c][v * 8 + 4]), __uint_as_float(r[c][v * 8 + 5])),
-                              pack_bf16x2(__uint_as_float(r[c][v * 8 + 6]), __uint_as_float(r[c][v * 8 + 7])));
+            if (col0 + o < p.N) {
+              if constexpr (EPI)
+                store8(out + o, &r[c][v * 8], col0 + o, p.epi);
+              else
+                st_global_v4_cs(out + o,
+                                pack_bf16x2(__uint_as_float(r[c][v * 8 + 0]), __uint_as_float(r[c][v * 8 + 1])),
+                                pack_bf16x2(__uint_as_float(r[c][v * 8 + 2]), __uint_as_float(r[c][v * 8 + 3])),
+                                pack_bf16x2(__uint_as_float(r[c][v * 8 + 4]), __uint_as_float(r[c][v * 8 + 5])),
+                                pack_bf16x2(__uint_as_float(r[c][v * 8 + 6]), __uint_as_float(r[c][v * 8 + 7])));
+            }
           }
       }
     }
@@ -359,12 +367,12 @@ __global__ void __maxnreg__(168)
   if (PAIR) cluster_sync();
 }
 
-template <bool FP4, bool A_MN, bool B_MN, bool PAIR>
+template <bool FP4, bool A_MN, bool B_MN, bool PAIR, bool EPI>
 bsmma_status launch_dense(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                           const CUtensorMap& tsb, const DenseParams& p, int sm_count,
                           cudaStream_t stream) {
   using C = Cfg<FP4>;
-  auto kern = mx_gemm_kernel<FP4, A_MN, B_MN, PAIR>;
+  auto kern = mx_gemm_kernel<FP4, A_MN, B_MN, PAIR, EPI>;
   static int max_clusters = -1;   // benign race: every thread computes the same value
   if (max_clusters < 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
@@ -420,11 +428,12 @@ bool use_pair(int num_m_tiles) {
 
 bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, const uint8_t* sfb,
                             void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
-                            bsmma_fmt a_fmt, bsmma_fmt b_fmt, cudaStream_t stream) {
+                            bsmma_fmt a_fmt, bsmma_fmt b_fmt, cudaStream_t stream,
+                            const void* bias, int act) {
   // SM-pair MMAs unless a one-CTA variant is asked for
   const int variant = dense_variant();
   if (variant == 0 || variant == 3)
-    return launch_mx_gemm_2sm(A, sfa, B, sfb, D, M, N, K, layout, a_fmt, b_fmt, stream);
+    return launch_mx_gemm_2sm(A, sfa, B, sfb, D, M, N, K, layout, a_fmt, b_fmt, stream, bias, act);
   bsmma_status st;
   const DeviceInfo* dev = current_device(&st);
   if (!dev) return st;
@@ -452,6 +461,8 @@ bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, co
 
   DenseParams p;
   p.D = static_cast<__nv_bfloat16*>(D);
+  p.epi.bias = static_cast<const __nv_bfloat16*>(bias);
+  p.epi.act = act;
   p.M = M;
   p.N = N;
   p.sfa_kq = static_cast<int>(kq);
@@ -465,20 +476,25 @@ bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, co
   p.status = dev->status;
   p.limit_ns = wait_limit_ns();
   const int sms = dev->sm_count;
+  const bool epi = bias != nullptr || act != 0;
+#define BSMMA_DENSE(F, A, B, P)                                                  \
+  (epi ? launch_dense<F, A, B, P, true>(ta, tb, tsa, tsb, p, sms, stream)        \
+       : launch_dense<F, A, B, P, false>(ta, tb, tsa, tsb, p, sms, stream))
   if (pair) {
-    if (fp4) return launch_dense<true, false, false, true>(ta, tb, tsa, tsb, p, sms, stream);
+    if (fp4) return BSMMA_DENSE(true, false, false, true);
     switch (layout) {
-      case BSMMA_NT: return launch_dense<false, false, false, true>(ta, tb, tsa, tsb, p, sms, stream);
-      case BSMMA_NN: return launch_dense<false, false, true, true>(ta, tb, tsa, tsb, p, sms, stream);
-      default:       return launch_dense<false, true, true, true>(ta, tb, tsa, tsb, p, sms, stream);
+      case BSMMA_NT: return BSMMA_DENSE(false, false, false, true);
+      case BSMMA_NN: return BSMMA_DENSE(false, false, true, true);
+      default:       return BSMMA_DENSE(false, true, true, true);
     }
   }
-  if (fp4) return launch_dense<true, false, false, false>(ta, tb, tsa, tsb, p, sms, stream);
+  if (fp4) return BSMMA_DENSE(true, false, false, false);
   switch (layout) {
-    case BSMMA_NT: return launch_dense<false, false, false, false>(ta, tb, tsa, tsb, p, sms, stream);
-    case BSMMA_NN: return launch_dense<false, false, true, false>(ta, tb, tsa, tsb, p, sms, stream);
-    default:       return launch_dense<false, true, true, false>(ta, tb, tsa, tsb, p, sms, stream);
+    case BSMMA_NT: return BSMMA_DENSE(false, false, false, false);
+    case BSMMA_NN: return BSMMA_DENSE(false, false, true, false);
+    default:       return BSMMA_DENSE(false, true, true, false);
   }
+#undef BSMMA_DENSE
 }
 
 }  // namespace bsmma

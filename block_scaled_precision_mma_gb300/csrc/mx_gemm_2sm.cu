@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "epilogue.cuh"
 #include "ptx.cuh"
 
 namespace bsmma {
@@ -51,6 +52,7 @@ struct Cfg2 {
 
 struct Pair2Params {
   __nv_bfloat16* D;
+  Epilogue epi;         // optional bias and activation
   int64_t M, N;
   int sfa_kq;           // row-scale chunks per 128-row block
   int sfb_kg;           // column-scale blocks per 256-column block
@@ -143,7 +145,9 @@ __device__ __forceinline__ void unit_tile2(const Pair2Params& p, int u, int& ur,
 
 // 10 warps share an SM's four register-file quarters (16384 registers each) as
 // 3+3+2+2 warps, so a thread may hold at most 16384 / (3 * 32) = 170 registers.
-template <bool FP4, bool A_MN, bool B_MN>
+// EPI: the output stage adds a bias and / or applies an activation (a separate
+// instantiation, so the plain GEMM's registers and code are unchanged).
+template <bool FP4, bool A_MN, bool B_MN, bool EPI>
 __global__ void __maxnreg__(168)
     mx_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmSFA,
@@ -342,12 +346,16 @@ __global__ void __maxnreg__(168)
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             const int o = c * 32 + v * 8;
-            if (col0 + o < p.N)
-              st_global_v4_cs(out + o,
-                              pack_bf16x2(__uint_as_float(r[c][v * 8 + 0]), __uint_as_float(r[c][v * 8 + 1])),
-                              pack_bf16x2(__uint_as_float(r[c][v * 8 + 2]), __uint_as_float(r[c][v * 8 + 3])),
-                              pack_bf16x2(__uint_as_float(r[c][v * 8 + 4]), __uint_as_float(r[c][v * 8 + 5])),
-                              pack_bf16x2(__uint_as_float(r[c][v * 8 + 6]), __uint_as_float(r[c][v * 8 + 7])));
+            if (col0 + o < p.N) {
+              if constexpr (EPI)
+                store8(out + o, &r[c][v * 8], col0 + o, p.epi);
+              else
+                st_global_v4_cs(out + o,
+                                pack_bf16x2(__uint_as_float(r[c][v * 8 + 0]), __uint_as_float(r[c][v * 8 + 1])),
+                                pack_bf16x2(__uint_as_float(r[c][v * 8 + 2]), __uint_as_float(r[c][v * 8 + 3])),
+                                pack_bf16x2(__uint_as_float(r[c][v * 8 + 4]), __uint_as_float(r[c][v * 8 + 5])),
+                                pack_bf16x2(__uint_as_float(r[c][v * 8 + 6]), __uint_as_float(r[c][v * 8 + 7])));
+            }
           }
       }
     }
@@ -362,11 +370,11 @@ __global__ void __maxnreg__(168)
   cluster_sync();
 }
 
-template <bool FP4, bool A_MN, bool B_MN>
+template <bool FP4, bool A_MN, bool B_MN, bool EPI>
 bsmma_status launch_2sm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                         const CUtensorMap& tsb, const Pair2Params& p, cudaStream_t stream) {
   using C = Cfg2<FP4>;
-  auto kern = mx_gemm_2sm_kernel<FP4, A_MN, B_MN>;
+  auto kern = mx_gemm_2sm_kernel<FP4, A_MN, B_MN, EPI>;
   static int max_clusters = -1;   // benign race: every thread computes the same value
   if (max_clusters < 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
@@ -415,7 +423,7 @@ bsmma_status launch_2sm(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
 bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B,
                                 const uint8_t* sfb, void* D, int64_t M, int64_t N, int64_t K,
                                 bsmma_layout layout, bsmma_fmt a_fmt, bsmma_fmt b_fmt,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, const void* bias, int act) {
   bsmma_status st;
   const DeviceInfo* dev = current_device(&st);
   if (!dev) return st;
@@ -440,6 +448,8 @@ bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B
   if (st != BSMMA_OK) return st;
   Pair2Params p;
   p.D = static_cast<__nv_bfloat16*>(D);
+  p.epi.bias = static_cast<const __nv_bfloat16*>(bias);
+  p.epi.act = act;
   p.M = M;
   p.N = N;
   p.sfa_kq = static_cast<int>(kq);
@@ -453,12 +463,17 @@ bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B
   p.idesc = idesc_block_scaled(af, bf, layout == BSMMA_TN, layout != BSMMA_NT, 256, 256);
   p.status = dev->status;
   p.limit_ns = wait_limit_ns();
-  if (fp4) return launch_2sm<true, false, false>(ta, tb, tsa, tsb, p, stream);
+  const bool epi = bias != nullptr || act != 0;
+#define BSMMA_2SM(F, A, B)                                                       \
+  (epi ? launch_2sm<F, A, B, true>(ta, tb, tsa, tsb, p, stream)                  \
+       : launch_2sm<F, A, B, false>(ta, tb, tsa, tsb, p, stream))
+  if (fp4) return BSMMA_2SM(true, false, false);
   switch (layout) {
-    case BSMMA_NT: return launch_2sm<false, false, false>(ta, tb, tsa, tsb, p, stream);
-    case BSMMA_NN: return launch_2sm<false, false, true>(ta, tb, tsa, tsb, p, stream);
-    default:       return launch_2sm<false, true, true>(ta, tb, tsa, tsb, p, stream);
+    case BSMMA_NT: return BSMMA_2SM(false, false, false);
+    case BSMMA_NN: return BSMMA_2SM(false, false, true);
+    default:       return BSMMA_2SM(false, true, true);
   }
+#undef BSMMA_2SM
 }
 
 }  // namespace bsmma

@@ -175,6 +175,35 @@ bsmma_status mx_scale_relayout(const uint8_t* s_plain, int64_t rows, int64_t kbl
 /* Size in bytes of the tiled layout of [rows][kblocks] scales of the given role. */
 int64_t mx_scale_tiled_bytes(int64_t rows, int64_t kblocks, bsmma_scale_role role);
 
+/* Activation of the fused epilogue (mx_gemm_bias_act). */
+typedef enum {
+  BSMMA_ACT_NONE = 0,
+  BSMMA_ACT_RELU = 1,   /* max(x, 0)                          */
+  BSMMA_ACT_GELU = 2,   /* x * (1 + erf(x / sqrt 2)) / 2       */
+  BSMMA_ACT_SILU = 3    /* x / (1 + exp(-x))                   */
+} bsmma_activation;
+
+/*
+ * mx_gemm_bias_act / mx_gemm_tiled_bias_act -- mx_gemm / mx_gemm_tiled with the output
+ * stage fused: D[m][n] = act(acc[m][n] + bias[n]) rounded to BF16, where acc is the
+ * FP32 accumulation mx_gemm rounds directly.  Activation and bias are the follow-up
+ * named in "[gfx1250] Add MXFP4 GEMM support to FlyDSL backend", Description (the
+ * plain GEMM has neither); the activation set and the erf form of GELU are this
+ * library's reading.
+ *   bias  BF16 [N] in device memory, 16-byte aligned, or NULL for none.
+ *   act   a bsmma_activation.
+ * Everything else, including preconditions and errors, is as for mx_gemm / mx_gemm_tiled.
+ */
+bsmma_status mx_gemm_bias_act(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
+                              const void* bias, bsmma_activation act, void* D, int64_t M,
+                              int64_t N, int64_t K, bsmma_layout layout, bsmma_fmt a_fmt,
+                              bsmma_fmt b_fmt, bsmma_stream stream);
+bsmma_status mx_gemm_tiled_bias_act(const void* A, const uint8_t* sA_tiled, const void* B,
+                                    const uint8_t* sB_tiled, const void* bias,
+                                    bsmma_activation act, void* D, int64_t M, int64_t N,
+                                    int64_t K, bsmma_layout layout, bsmma_fmt a_fmt,
+                                    bsmma_fmt b_fmt, bsmma_stream stream);
+
 /* Element type of the high-precision inputs of the quantisers. */
 typedef enum { BSMMA_BF16 = 0, BSMMA_F32 = 1 } bsmma_dtype;
 

@@ -125,6 +125,18 @@ def test_mx_quantize_validation(lib, args, expect):
     assert lib.mx_quantize(*args, None) == expect
 
 
+def test_bias_act_validation(lib):
+    # (A, sA, B, sB, bias, act, D, M, N, K, layout, a_fmt, b_fmt)
+    ok = (FAKE, FAKE, FAKE, FAKE)
+    assert lib.mx_gemm_bias_act(*ok, FAKE, 4, FAKE, 128, 128, 64, 0, 0, 0, None) == 1      # act
+    assert lib.mx_gemm_bias_act(*ok, FAKE, -1, FAKE, 128, 128, 64, 0, 0, 0, None) == 1
+    assert lib.mx_gemm_bias_act(*ok, ODD, 2, FAKE, 128, 128, 64, 0, 0, 0, None) == 3       # bias
+    assert lib.mx_gemm_bias_act(*ok, FAKE, 2, FAKE, 128, 128, 48, 0, 0, 0, None) == 1      # K % 32
+    assert lib.mx_gemm_tiled_bias_act(*ok, ODD, 1, FAKE, 128, 128, 64, 0, 0, 0, None) == 3
+    assert lib.mx_gemm_tiled_bias_act(None, None, None, None, None, 3, None, 0, 128, 64, 0, 0, 0,
+                                      None) == 0                                          # M == 0
+
+
 def test_group_block_quantize_validation(lib):
     # (x, dtype, total_M, K, m_sizes, G, codes, scales)
     assert lib.fp8_group_quantize(FAKE, 0, 256, 200, FAKE, 8, FAKE, FAKE, None) == 1   # K % 128

@@ -27,7 +27,8 @@ import torch
 from .build import LIB_PATH, build
 
 __all__ = ["mx_gemm", "mx_gemm_tiled", "mx_gemm_noalloc", "grouped_fp8_gemm", "mx_scale_relayout",
-           "mx_quantize", "fp8_group_quantize", "fp8_block_quantize",
+           "mx_quantize", "fp8_group_quantize", "fp8_block_quantize", "autotune_configure",
+           "autotune_lookup",
            "mx_scale_tiled_bytes", "device_status", "reserve_workspace", "set_wait_limit_ns",
            "set_dense_variant", "set_grouped_tile_width",
            "launch_count", "probe_wait_timeout", "status_string", "BsmmaError", "load",
@@ -82,6 +83,9 @@ def load(path: str | None = None):
         lib.bsmma_probe_wait_timeout.argtypes = [i64, p]
         lib.mx_quantize.argtypes = [p, i32, i64, i64, i32, i32, p, p, p]
         lib.mx_gemm_bias_act.argtypes = [p, p, p, p, p, i32, p, i64, i64, i64, i32, i32, i32, p]
+        lib.bsmma_autotune_configure.argtypes = [i32, ctypes.c_char_p]
+        lib.bsmma_autotune_lookup.argtypes = [ctypes.c_char_p]
+        lib.bsmma_autotune_lookup.restype = i32
         lib.mx_gemm_tiled_bias_act.argtypes = [p, p, p, p, p, i32, p, i64, i64, i64, i32, i32, i32, p]
         lib.fp8_group_quantize.argtypes = [p, i32, i64, i64, p, i32, p, p, p]
         lib.fp8_block_quantize.argtypes = [p, i32, i64, i64, i64, p, p, p]
@@ -90,7 +94,8 @@ def load(path: str | None = None):
                      "bsmma_reserve_workspace", "bsmma_device_status", "bsmma_set_wait_limit_ns",
                      "bsmma_set_dense_variant", "bsmma_set_grouped_tile_width",
                      "bsmma_probe_wait_timeout", "mx_quantize", "fp8_group_quantize",
-                     "fp8_block_quantize", "mx_gemm_bias_act", "mx_gemm_tiled_bias_act"):
+                     "fp8_block_quantize", "mx_gemm_bias_act", "mx_gemm_tiled_bias_act",
+                     "bsmma_autotune_configure"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -299,3 +304,16 @@ def fp8_block_quantize(w, codes=None, scales=None, stream=None):
     _check(load().fp8_block_quantize(_ptr(w), _dtype_code(w), G, N, K, _ptr(codes), _ptr(scales),
                                      _stream(stream)), "fp8_block_quantize")
     return codes, scales
+
+
+def autotune_configure(enable=-1, cache_path=None):
+    """Turns tile autotuning on (1) / off (0) / to the environment's BSMMA_AUTOTUNE (-1)
+    and selects its cache file (None: BSMMA_AUTOTUNE_CACHE or the user cache directory);
+    see ``bsmma_autotune_configure`` in bsmma.h."""
+    path = None if cache_path is None else os.fsencode(cache_path)
+    _check(load().bsmma_autotune_configure(int(enable), path), "bsmma_autotune_configure")
+
+
+def autotune_lookup(key: str) -> int:
+    """The stored choice for a shape-class key, or -1."""
+    return int(load().bsmma_autotune_lookup(key.encode()))

@@ -423,6 +423,13 @@ bsmma_status launch_grouped_bn(const CUtensorMap& tx, const CUtensorMap& tw, Gro
 
 }  // namespace
 
+namespace {
+bsmma_status launch_grouped_width(const uint8_t* X, const float* sX, const uint8_t* W,
+                                  const float* sW, void* D, const int64_t* m_sizes, int64_t total_M,
+                                  int G, int64_t N, int64_t K, int bn, const DeviceInfo* dev,
+                                  cudaStream_t stream);
+}  // namespace
+
 bsmma_status launch_grouped(const uint8_t* X, const float* sX, const uint8_t* W, const float* sW,
                             void* D, const int64_t* m_sizes, int64_t total_M, int G, int64_t N,
                             int64_t K, cudaStream_t stream) {
@@ -439,7 +446,24 @@ bsmma_status launch_grouped(const uint8_t* X, const float* sX, const uint8_t* W,
                     row_blocks_est * (N / 256) * 2 >= static_cast<int64_t>(dev->sm_count) &&
                     grouped_tile_width() != 128;
   const bool force_wide = grouped_tile_width() == 256 && N % 256 == 0;
-  const int bn = (wide || force_wide) ? 256 : 128;
+  int bn = (wide || force_wide) ? 256 : 128;
+  if (grouped_tile_width() == 0 && N % 256 == 0) {
+    // opt-in autotuning per (nextPow2(total_M), N, K, G)
+    const std::string key = "grouped " + std::to_string(next_pow2(total_M)) + " " +
+                            std::to_string(N) + " " + std::to_string(K) + " " + std::to_string(G);
+    bn = autotune_pick(key, {256, 128}, bn, stream, [&](int c) {
+      return launch_grouped_width(X, sX, W, sW, D, m_sizes, total_M, G, N, K, c, dev, stream);
+    });
+  }
+  return launch_grouped_width(X, sX, W, sW, D, m_sizes, total_M, G, N, K, bn, dev, stream);
+}
+
+namespace {
+bsmma_status launch_grouped_width(const uint8_t* X, const float* sX, const uint8_t* W,
+                                  const float* sW, void* D, const int64_t* m_sizes, int64_t total_M,
+                                  int G, int64_t N, int64_t K, int bn, const DeviceInfo* dev,
+                                  cudaStream_t stream) {
+  bsmma_status st;
   CUtensorMap tx, tw;
   // With no rows there is no X tile to load; W's address stands in for the map.
   st = encode_tmap_u8(&tx, total_M > 0 ? static_cast<const void*>(X) : W, K,
@@ -461,5 +485,6 @@ bsmma_status launch_grouped(const uint8_t* X, const float* sX, const uint8_t* W,
   if (bn == 256) return launch_grouped_bn<256>(tx, tw, p, total_M, G, dev->sm_count, stream);
   return launch_grouped_bn<128>(tx, tw, p, total_M, G, dev->sm_count, stream);
 }
+}  // namespace
 
 }  // namespace bsmma

@@ -4,6 +4,9 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <functional>
+#include <string>
+#include <vector>
 
 #include "bsmma.h"
 
@@ -69,6 +72,13 @@ bsmma_status launch_group_quantize(const void* x, bool f32, int64_t total_M, int
                                    cudaStream_t stream);
 bsmma_status launch_block_quantize(const void* w, bool f32, int64_t G, int64_t N, int64_t K,
                                    uint8_t* codes, float* scales, cudaStream_t stream);
+
+// Autotuning (opt-in): the cached choice for `key`, else -- when tuning is enabled and the
+// stream is not capturing -- the fastest of `candidates` timed with `launch`, else
+// `fallback`.
+int64_t next_pow2(int64_t v);
+int autotune_pick(const std::string& key, const std::vector<int>& candidates, int fallback,
+                  cudaStream_t stream, const std::function<bsmma_status(int)>& launch);
 
 inline bsmma_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? BSMMA_OK : BSMMA_ERR_CUDA; }
 

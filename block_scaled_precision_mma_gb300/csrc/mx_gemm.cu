@@ -418,21 +418,47 @@ bsmma_status launch_dense(const CUtensorMap& ta, const CUtensorMap& tb, const CU
 }
 
 // One CTA per 128x256 tile (variant 1) or CTA pairs sharing a multicast B tile (2).
-bool use_pair(int num_m_tiles) {
-  const int v = dense_variant();
+bool use_pair(int num_m_tiles, int v) {
   if (v == 1) return false;
   return kPairDefault && num_m_tiles >= 1;
 }
 
 }  // namespace
 
+namespace {
+bsmma_status launch_mx_gemm_variant(const void* A, const uint8_t* sfa, const void* B,
+                                    const uint8_t* sfb, void* D, int64_t M, int64_t N, int64_t K,
+                                    bsmma_layout layout, bsmma_fmt a_fmt, bsmma_fmt b_fmt,
+                                    cudaStream_t stream, const void* bias, int act, int variant);
+}  // namespace
+
 bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, const uint8_t* sfb,
                             void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
                             bsmma_fmt a_fmt, bsmma_fmt b_fmt, cudaStream_t stream,
                             const void* bias, int act) {
-  // SM-pair MMAs unless a one-CTA variant is asked for
-  const int variant = dense_variant();
-  if (variant == 0 || variant == 3)
+  // SM-pair MMAs unless a one-CTA variant is asked for, or (opt-in) tuning per
+  // (nextPow2(M), N, K, layout, formats) picks another
+  int variant = dense_variant();
+  if (variant == 0) {
+    const std::string key = "dense " + std::to_string(next_pow2(M)) + " " + std::to_string(N) +
+                            " " + std::to_string(K) + " " + std::to_string(static_cast<int>(layout)) +
+                            " " + std::to_string(static_cast<int>(a_fmt)) + " " +
+                            std::to_string(static_cast<int>(b_fmt));
+    variant = autotune_pick(key, {3, 2, 1}, 3, stream, [&](int v) {
+      return launch_mx_gemm_variant(A, sfa, B, sfb, D, M, N, K, layout, a_fmt, b_fmt, stream, bias,
+                                    act, v);
+    });
+  }
+  return launch_mx_gemm_variant(A, sfa, B, sfb, D, M, N, K, layout, a_fmt, b_fmt, stream, bias,
+                                act, variant);
+}
+
+namespace {
+bsmma_status launch_mx_gemm_variant(const void* A, const uint8_t* sfa, const void* B,
+                                    const uint8_t* sfb, void* D, int64_t M, int64_t N, int64_t K,
+                                    bsmma_layout layout, bsmma_fmt a_fmt, bsmma_fmt b_fmt,
+                                    cudaStream_t stream, const void* bias, int act, int variant) {
+  if (variant == 3)
     return launch_mx_gemm_2sm(A, sfa, B, sfb, D, M, N, K, layout, a_fmt, b_fmt, stream, bias, act);
   bsmma_status st;
   const DeviceInfo* dev = current_device(&st);
@@ -443,7 +469,7 @@ bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, co
   const int64_t kq = (kblocks + 7) / 8;          // row-scale chunks per 128 rows
   const int64_t kgp = 2 * ((kblocks + 7) / 8);   // column-scale blocks per 256 columns
   const int num_m_tiles = static_cast<int>((M + kBM - 1) / kBM);
-  const bool pair = use_pair(num_m_tiles);
+  const bool pair = use_pair(num_m_tiles, variant);
   CUtensorMap ta, tb, tsa, tsb;
   if (layout == BSMMA_TN) st = encode_tmap_u8(&ta, A, M, K, M, 128, 128);
   else st = encode_tmap_u8(&ta, A, kbytes, M, kbytes, 128, 128);
@@ -496,5 +522,6 @@ bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, co
   }
 #undef BSMMA_DENSE
 }
+}  // namespace
 
 }  // namespace bsmma

@@ -204,6 +204,32 @@ bsmma_status mx_gemm_tiled_bias_act(const void* A, const uint8_t* sA_tiled, cons
                                     int64_t K, bsmma_layout layout, bsmma_fmt a_fmt,
                                     bsmma_fmt b_fmt, bsmma_stream stream);
 
+/*
+ * Autotuning (opt-in).  "Add FlyDSL grouped groupwise FP8 GEMM for ROCm", Tile
+ * selection: candidates are timed once per shape class and the winner persisted to
+ * disk, behind a gate, with a fixed choice when the gate is off and no tuning during
+ * graph capture.
+ *   Shape classes and candidates: grouped_fp8_gemm per (nextPow2(total_M), N, K, G),
+ *   tile widths 256 and 128 (when N % 256 == 0); the dense GEMMs per (nextPow2(M), N, K,
+ *   layout, a_fmt, b_fmt), the SM-pair, CTA-pair and single-CTA kernels (3, 2, 1).
+ *   The first call of a new class on a non-capturing stream runs each candidate twice
+ *   and waits for it (it synchronises that stream); later calls, and calls in any
+ *   process that reads the same cache file, use the stored choice.  A variant or width
+ *   set with bsmma_set_dense_variant / bsmma_set_grouped_tile_width takes precedence.
+ *   Every candidate computes the same result.
+ * bsmma_autotune_configure -- enable: 1 on, 0 off, -1 from the environment
+ *   (BSMMA_AUTOTUNE=1 turns it on); cache_path: the file, or NULL for
+ *   BSMMA_AUTOTUNE_CACHE, else $XDG_CACHE_HOME/bsmma/autotune.txt, else
+ *   $HOME/.cache/bsmma/autotune.txt.  Reloads the cache.  Without a call the
+ *   environment decides at the first GEMM.  The file holds one line per class:
+ *   "grouped <T> <N> <K> <G> <width>" or "dense <M> <N> <K> <layout> <a_fmt> <b_fmt>
+ *   <variant>" (T, M rounded up to powers of two).
+ * bsmma_autotune_lookup -- the stored choice for a key (a line without its last
+ *   field), or -1.
+ */
+bsmma_status bsmma_autotune_configure(int enable, const char* cache_path);
+int bsmma_autotune_lookup(const char* key);
+
 /* Element type of the high-precision inputs of the quantisers. */
 typedef enum { BSMMA_BF16 = 0, BSMMA_F32 = 1 } bsmma_dtype;
 

@@ -9,13 +9,16 @@
 // Groupwise FP8 ("Add FlyDSL grouped groupwise FP8 GEMM for ROCm": quantize_fp8_group
 // and the per-group block layout of its scales): FP32 scale s = amax / 448 (1 for an
 // all-zero block) per 1x128 activation block or 128x128 weight block, codes
-// RNE-saturate(x / s) in E4M3, both divisions in FP32 (s never below 2^-149).
+// RNE-saturate(x / s) in E4M3, both divisions in FP32 (s never below 2^-149); the
+// per-value quotient comes from an exact FMA sequence on the block's reciprocal.
 //
 // Every kernel streams its input once from HBM with 16-byte loads and writes codes with
 // coalesced stores; scales are a small side stream.  Grids are a few CTAs per SM with
 // grid-stride loops.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <cstring>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -221,29 +224,133 @@ __device__ __forceinline__ float group_scale(float amax) {
   return fmaxf(__fdiv_rn(amax, 448.f), __uint_as_float(1u));
 }
 
-// E4M3 codes of eight values x / s (correctly rounded FP32 quotients).
-__device__ __forceinline__ uint2 e4m3_codes8(const float (&x)[8], float s) {
-  const uint32_t w0 = fp8x2<BSMMA_E4M3>(__fdiv_rn(x[0], s), __fdiv_rn(x[1], s)) |
-                      (fp8x2<BSMMA_E4M3>(__fdiv_rn(x[2], s), __fdiv_rn(x[3], s)) << 16);
-  const uint32_t w1 = fp8x2<BSMMA_E4M3>(__fdiv_rn(x[4], s), __fdiv_rn(x[5], s)) |
-                      (fp8x2<BSMMA_E4M3>(__fdiv_rn(x[6], s), __fdiv_rn(x[7], s)) << 16);
-  return make_uint2(w0, w1);
+// The correctly rounded FP32 quotient x / s from y = RN(1 / s) by FMA corrections
+// (P. Markstein, "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990; the division theorem in Muller et al.,
+// "Handbook of Floating-Point Arithmetic", ch. 4): if q is a faithful approximation of
+// x / s and y is within half an ulp of 1 / s, then r = x - s q is exact and
+// RN(q + r y) = RN(x / s).  q0 = RN(x y) is within 1.5 ulp, so one correction makes it
+// faithful and a second makes it exact.  The conditions hold wherever the code depends
+// on the quotient: for s in [2^-88, FLT_MAX] every |x / s| >= 2^-11 has a normal x
+// (>= 2^-99) and a remainder on a grid of at least 2^-146, so nothing underflows; a
+// smaller quotient gives a code of zero either way, whose sign is taken from x.
+constexpr float kFastDivMinScale = 0x1p-88f;
+
+__device__ __forceinline__ bool fast_div_ok(float s) {
+  return s >= kFastDivMinScale && s <= 3.40282347e38f;   // also false for NaN
+}
+
+// The sequence on a pair of values with packed FP32 operations (each lane rounds like
+// the scalar operation).  The sign of a zero quotient is restored by the caller.
+__device__ __forceinline__ float2 quotient2_rn(float2 x, float2 neg_s, float2 y) {
+  const float2 q0 = __fmul2_rn(x, y);
+  const float2 q1 = __ffma2_rn(__ffma2_rn(q0, neg_s, x), y, q0);
+  return __ffma2_rn(__ffma2_rn(q1, neg_s, x), y, q1);
+}
+
+// Sign bits of four FP32 values at bits 7, 15, 23 and 31 (one per code byte).
+__device__ __forceinline__ uint32_t sign_bytes4(float a, float b, float c, float d) {
+  const uint32_t ab = __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x0073);
+  const uint32_t cd = __byte_perm(__float_as_uint(c), __float_as_uint(d), 0x0073);
+  return __byte_perm(ab, cd, 0x5410) & 0x80808080u;
+}
+
+// E4M3 codes of eight values x / s, the quotients correctly rounded in FP32: by the FMA
+// sequence on pairs when fast_div_ok(s), with y = RN(1 / s), else by IEEE division.  Each
+// code's sign bit is then OR-ed in from x, which gives a quotient that vanished (or an
+// x of -0) the sign of x; a code of a negative quotient has that bit already.
+__device__ __forceinline__ uint2 e4m3_codes8(const float (&x)[8], float s, float y, bool fast) {
+  float q[8];
+  if (fast) {
+    const float2 ns2 = make_float2(-s, -s), y2 = make_float2(y, y);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 r = quotient2_rn(make_float2(x[2 * j], x[2 * j + 1]), ns2, y2);
+      q[2 * j] = r.x;
+      q[2 * j + 1] = r.y;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) q[j] = __fdiv_rn(x[j], s);
+  }
+  const uint32_t w0 = fp8x2<BSMMA_E4M3>(q[0], q[1]) | (fp8x2<BSMMA_E4M3>(q[2], q[3]) << 16);
+  const uint32_t w1 = fp8x2<BSMMA_E4M3>(q[4], q[5]) | (fp8x2<BSMMA_E4M3>(q[6], q[7]) << 16);
+  return make_uint2(w0 | sign_bytes4(x[0], x[1], x[2], x[3]),
+                    w1 | sign_bytes4(x[4], x[5], x[6], x[7]));
 }
 
 constexpr int kMaxGroups = 64;
 
-// Activations X[total_M][K] over 1x128 blocks.  A CTA takes 64 rows x one 128-K block:
-// sixteen threads share a row (eight consecutive values each, one 16-byte load), and
-// every thread owns four rows, all loaded before any is reduced.  Codes go out as
-// 8-byte stores; each row's scale to the per-group block layout.
+// Eight consecutive FP32 values from shared memory (BF16 widens exactly).
 template <bool F32>
-__global__ void __launch_bounds__(kThreads) group_quant_kernel(const void* x, int64_t total_M,
-                                                                int64_t K, const int64_t* m_sizes,
-                                                                int G, uint8_t* codes, float* sx,
-                                                                int* status) {
+__device__ __forceinline__ void lds8(const uint8_t* p, float (&v)[8]) {
+  if constexpr (F32) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 16);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+    const uint4 r = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[2 * j] = __uint_as_float(w[j] << 16);
+      v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  }
+}
+
+// Activations X[total_M][K] over 1x128 blocks.  A persistent CTA keeps a ring of
+// kXStages tiles of 64 rows x 128 values in shared memory, each filled by one tensor copy
+// issued by thread 0 (rows past total_M arrive as zeros and are not stored), and
+// quantises the oldest while the others stream in.  Four threads share a row: thread
+// `seg` of row `row` owns the 8-value chunks at columns seg*8 + 32k (k < 4), visited from
+// k = row & 1 on so that a warp's even and odd rows read opposite halves of the shared-
+// memory banks.  Per row: the 4-lane amax, the scale, its reciprocal and the group
+// lookup, spread over 32 values.  Codes go out as 8-byte stores (32 contiguous bytes per
+// row and chunk); each row's scale to the per-group block layout.
+constexpr int kXStages = 4;
+
+template <bool F32>
+struct XRing {
+  static constexpr int kRowBytes = 128 * (F32 ? 4 : 2);
+  static constexpr int kBytes = 64 * kRowBytes;               // one 64 x 128 tile
+  // 1 KB of slack puts the ring on a 1024-byte boundary (tensor copies need 128)
+  static constexpr int kSmem = 1024 + kXStages * kBytes + kXStages * 8;
+};
+
+template <bool F32>
+__global__ void __launch_bounds__(kThreads) group_quant_kernel(
+    const __grid_constant__ CUtensorMap tmX, int64_t total_M, int64_t K, const int64_t* m_sizes,
+    int G, uint8_t* codes, float* sx, int* status, uint64_t limit_ns) {
+  using R = XRing<F32>;
+  extern __shared__ __align__(16) uint8_t xring_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(xring_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + kXStages * R::kBytes);
   __shared__ int64_t start[kMaxGroups + 1];
   __shared__ int64_t size[kMaxGroups];
-  __shared__ int bad;
+  __shared__ int bad, landed;
+  // tile indices fit 32 bits (the entry point bounds total_M and K)
+  const int KB = static_cast<int>(K / 128);
+  const int tiles = static_cast<int>((total_M + 63) / 64) * KB;
+  const int mine = tiles > static_cast<int>(blockIdx.x)
+                       ? (tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                       : 0;
+  auto tile_of = [&](int it, int& rt, int& kb) {
+    const int t = static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x);
+    rt = t / KB;
+    kb = t - rt * KB;
+  };
+  // thread 0: the tile of iteration `it` into its slot
+  auto issue = [&](int it) {
+    if (it >= mine) return;
+    int rt, kb;
+    tile_of(it, rt, kb);
+    const int slot = it % kXStages;
+    mbar_arrive_expect_tx(&full[slot], R::kBytes);
+    tma_load_2d(&tmX, &full[slot], ring + slot * R::kBytes, kb * (F32 ? 128 : 64), rt * 64);
+  };
   if (threadIdx.x == 0) {
     int64_t row = 0;
     int b = 0;
@@ -258,92 +365,244 @@ __global__ void __launch_bounds__(kThreads) group_quant_kernel(const void* x, in
     start[G] = row;
     bad = b;
     if (b && blockIdx.x == 0) report_status(status, kDevBadMSizes);
+    if (!b && mine > 0) {
+      prefetch_tmap(&tmX);
+      for (int st = 0; st < kXStages; ++st) mbar_init(&full[st], 1);
+      fence_mbar_init();
+      for (int it = 0; it < kXStages; ++it) issue(it);
+    }
   }
   __syncthreads();
-  if (bad) return;   // uniform: nothing is written
-  const int seg = threadIdx.x & 15, rloc = threadIdx.x >> 4;   // rows rloc + 16i, i < 4
-  // tile indices fit 32 bits (the entry point bounds total_M and K)
-  const int KB = static_cast<int>(K / 128);
-  const int row_tiles = static_cast<int>((total_M + 63) / 64);
-  for (int t = blockIdx.x; t < row_tiles * KB; t += gridDim.x) {
-    const int rt = t / KB, kb = t - rt * KB;
-    float v[4][8] = {};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t r = static_cast<int64_t>(rt) * 64 + rloc + 16 * i;
-      if (r < total_M) load8<F32>(x, r * K + kb * 128 + seg * 8, v[i]);
+  if (bad) return;   // uniform: nothing is written, nothing was issued
+  static_assert(kThreads == 4 * 64, "four threads per row of a 64-row tile");
+  const int seg = threadIdx.x & 3, rloc = threadIdx.x >> 2;
+  const int rot = rloc & 1;
+  int it = 0;
+  for (; it < mine; ++it) {
+    const int slot = it % kXStages;
+    if (threadIdx.x == 0) {
+      volatile int no_abort = 0;
+      landed = mbar_wait(&full[slot], (it / kXStages) & 1, limit_ns, &no_abort, status) ? 1 : 0;
     }
+    __syncthreads();                      // the tile is visible to every thread
+    if (!landed) break;                   // uniform
+    const uint8_t* trow = ring + slot * R::kBytes + rloc * R::kRowBytes;
+    float v[4][8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t r = static_cast<int64_t>(rt) * 64 + rloc + 16 * i;
-      float amax = 0.f;
+    for (int k = 0; k < 4; ++k)
+      lds8<F32>(trow + (seg * 8 + 32 * ((k + rot) & 3)) * (F32 ? 4 : 2), v[k]);
+    __syncthreads();                      // the slot is read out
+    if (threadIdx.x == 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(it + kXStages);
+    }
+    int rt, kb;
+    tile_of(it, rt, kb);
+    const int64_t row0 = static_cast<int64_t>(rt) * 64;
+    const int64_t r = row0 + rloc;
+    float amax = 0.f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[i][j]));
+    for (int k = 0; k < 4; ++k)
 #pragma unroll
-      for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      if (r >= total_M) continue;     // whole half-warps (the row is shared by 16 threads)
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[k][j]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    if (r < total_M) {                    // whole 4-lane row groups
       const float s = group_scale(amax);
-      __stcs(reinterpret_cast<uint2*>(codes + r * K + kb * 128 + seg * 8), e4m3_codes8(v[i], s));
+      const bool fast = fast_div_ok(s);
+      const float y = fast ? __frcp_rn(s) : 0.f;
+      uint8_t* out = codes + r * K + kb * 128 + seg * 8;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        __stcs(reinterpret_cast<uint2*>(out + 32 * ((k + rot) & 3)), e4m3_codes8(v[k], s, y, fast));
       // the group owning row r: the last g with start[g] <= r (an empty group shares its
-      // start with the next one, so it is never the last), by a binary search every lane
-      // runs (no divergent scan)
-      int lo = 0, hi = G;
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (start[mid] <= r) lo = mid;
+      // start with the next one, so it is never the last); a binary search for the tile's
+      // first row, which every lane runs, then a walk past group ends
+      int g = 0, hi = G;
+      while (hi - g > 1) {
+        const int mid = (g + hi) >> 1;
+        if (start[mid] <= row0) g = mid;
         else hi = mid;
       }
-      if (seg == 0) sx[start[lo] * KB + (r - start[lo]) + static_cast<int64_t>(kb) * size[lo]] = s;
+      while (r >= start[g + 1]) ++g;    // start[G] = total_M > r ends the walk
+      if (seg == 0) sx[start[g] * KB + (r - start[g]) + static_cast<int64_t>(kb) * size[g]] = s;
     }
   }
+  // after a timeout, copies already issued must land before the CTA's memory is released
+  if (threadIdx.x == 0)
+    for (int j = it; j < it + kXStages && j < mine; ++j) {
+      volatile int no_abort = 0;
+      mbar_wait(&full[j % kXStages], (j / kXStages) & 1, limit_ns / 4 + 1, &no_abort, nullptr);
+    }
 }
 
-// Weights W[G][N][K] over 128x128 blocks.  A CTA of 512 threads takes one block:
-// thread t owns eight consecutive values of rows t/16 + 32i (i < 4), so each row
-// segment is read and written by 16 threads with 16-byte (8-byte) accesses.
+// Weights W[G][N][K] over 128x128 blocks.  A persistent CTA of 512 threads keeps a ring
+// of kWStages blocks in shared memory, each filled by one tensor copy issued by thread 0,
+// and quantises the oldest while the others stream in.
+// Thread t owns eight consecutive values of rows t/16 + 32i (i < 4) of a block.  Thread 0
+// alone waits on a block's barrier (bounded) and the CTA barrier hands the outcome to
+// every thread, so all leave the loop together.
 constexpr int kBlockThreads = 512;
+constexpr int kWStages = 3;
 
 template <bool F32>
-__global__ void __launch_bounds__(kBlockThreads) block_quant_kernel(const void* w, int64_t G,
-                                                                     int64_t N, int64_t K,
-                                                                     uint8_t* codes, float* sw) {
-  __shared__ float warp_amax[kBlockThreads / 32];
+struct WRing {
+  static constexpr int kRowBytes = 128 * (F32 ? 4 : 2);
+  static constexpr int kBytes = 128 * kRowBytes;              // one 128x128 block
+  // the ring starts on a 1024-byte boundary (a tensor copy's shared-memory destination must
+  // be 128-byte aligned), so 1 KB of slack in front of it
+  static constexpr int kSmem = 1024 + kWStages * kBytes + kWStages * 8;
+};
+
+// One 128x128 block of the weights' 3-D tensor map (32-bit words x N rows x G) into
+// shared memory, completing bytes on `bar`.
+__device__ __forceinline__ void tma_load_3d(const void* tmap, uint64_t* bar, void* dst,
+                                            int32_t c0, int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+template <bool F32>
+__global__ void __launch_bounds__(kBlockThreads) block_quant_kernel(
+    const __grid_constant__ CUtensorMap tmW, int64_t G, int64_t N, int64_t K, uint8_t* codes,
+    float* sw, int* status, uint64_t limit_ns) {
+  using R = WRing<F32>;
+  extern __shared__ __align__(16) uint8_t ring_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(ring_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + kWStages * R::kBytes);
+  __shared__ float warp_amax[2][kBlockThreads / 32];
+  __shared__ int landed;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // block indices fit 32 bits (the entry point bounds G * N/128 * K/128)
   const int NB = static_cast<int>(N / 128), KB = static_cast<int>(K / 128);
   const int seg = threadIdx.x & 15, r0 = threadIdx.x >> 4;
   const int blocks = static_cast<int>(G) * NB * KB;
-  for (int t = blockIdx.x; t < blocks; t += gridDim.x) {
-    const int g = t / (NB * KB), rem = t - g * NB * KB;
-    const int nb = rem / KB, kb = rem - nb * KB;
+  const int mine = blocks > static_cast<int>(blockIdx.x)
+                       ? (blocks - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                       : 0;
+  // block (g, nb, kb) of this CTA's iteration `it`
+  auto block_of = [&](int it, int& g, int& nb, int& kb) {
+    const int t = static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x);
+    g = t / (NB * KB);
+    const int rem = t - g * NB * KB;
+    nb = rem / KB;
+    kb = rem - nb * KB;
+    return t;
+  };
+  // thread 0: the block of iteration `it` into its slot
+  auto issue = [&](int it) {
+    if (it >= mine) return;
+    int g, nb, kb;
+    block_of(it, g, nb, kb);
+    const int slot = it % kWStages;
+    mbar_arrive_expect_tx(&full[slot], R::kBytes);
+    tma_load_3d(&tmW, &full[slot], ring + slot * R::kBytes, kb * (F32 ? 128 : 64), nb * 128, g);
+  };
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmW);
+    for (int st = 0; st < kWStages; ++st) mbar_init(&full[st], 1);
+    fence_mbar_init();
+    for (int it = 0; it < kWStages; ++it) issue(it);
+  }
+  int it = 0;
+  for (; it < mine; ++it) {
+    const int slot = it % kWStages;
+    if (threadIdx.x == 0) {
+      volatile int no_abort = 0;
+      landed = mbar_wait(&full[slot], (it / kWStages) & 1, limit_ns, &no_abort, status) ? 1 : 0;
+    }
+    __syncthreads();                      // the block is visible to every thread
+    if (!landed) break;                   // uniform
+    const uint8_t* blk = ring + slot * R::kBytes;
     float v[4][8];
     float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t n = static_cast<int64_t>(nb) * 128 + r0 + 32 * i;
-      load8<F32>(w, (g * N + n) * K + kb * 128 + seg * 8, v[i]);
-    }
+    for (int i = 0; i < 4; ++i) lds8<F32>(blk + (r0 + 32 * i) * R::kRowBytes + seg * (F32 ? 32 : 16), v[i]);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[i][j]));
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if (lane == 0) warp_amax[warp] = amax;
-    __syncthreads();
-    amax = warp_amax[0];
-#pragma unroll
-    for (int j = 1; j < kBlockThreads / 32; ++j) amax = fmaxf(amax, warp_amax[j]);
-    const float s = group_scale(amax);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t n = static_cast<int64_t>(nb) * 128 + r0 + 32 * i;
-      __stcs(reinterpret_cast<uint2*>(codes + (g * N + n) * K + kb * 128 + seg * 8),
-             e4m3_codes8(v[i], s));
+    if (lane == 0) warp_amax[it & 1][warp] = amax;
+    __syncthreads();                      // the slot is read out; all warp maxima are in
+    if (threadIdx.x == 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(it + kWStages);
     }
-    if (threadIdx.x == 0) sw[(static_cast<int64_t>(g) * NB + nb) * KB + kb] = s;
-    __syncthreads();   // warp_amax is reused by the next block
+    amax = warp_amax[it & 1][0];
+#pragma unroll
+    for (int j = 1; j < kBlockThreads / 32; ++j) amax = fmaxf(amax, warp_amax[it & 1][j]);
+    const float s = group_scale(amax);
+    const bool fast = fast_div_ok(s);
+    const float y = fast ? __frcp_rn(s) : 0.f;
+    int g, nb, kb;
+    const int t = block_of(it, g, nb, kb);
+    const int64_t o = (static_cast<int64_t>(g) * N + static_cast<int64_t>(nb) * 128) * K + kb * 128;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      __stcs(reinterpret_cast<uint2*>(codes + o + static_cast<int64_t>(r0 + 32 * i) * K + seg * 8),
+             e4m3_codes8(v[i], s, y, fast));
+    if (threadIdx.x == 0) sw[t] = s;
   }
+  // after a timeout, copies already issued must land before the CTA's memory is released
+  if (threadIdx.x == 0)
+    for (int j = it; j < it + kWStages && j < mine; ++j) {
+      volatile int no_abort = 0;
+      mbar_wait(&full[j % kWStages], (j / kWStages) & 1, limit_ns / 4 + 1, &no_abort, nullptr);
+    }
+}
+
+// A BF16 / FP32 tensor as a tensor map of 32-bit words (`rank` dimensions, innermost
+// first; `strides` in bytes for dimensions 1..rank-1), no swizzle, zero fill outside.
+bsmma_status encode_words(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                          const uint64_t* strides, const uint32_t* box) {
+  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static const Encode encode = []() -> Encode {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<Encode>(fn);
+  }();
+  if (!encode) return BSMMA_ERR_CUDA;
+  cuuint64_t d[3], st[2];
+  cuuint32_t b[3], e[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    if (i > 0) st[i - 1] = strides[i - 1];
+  }
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, static_cast<cuuint32_t>(rank),
+                            const_cast<void*>(base), d, st, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BSMMA_OK : BSMMA_ERR_INVALID_ARG;
+}
+
+// Resident CTAs per SM of a ring kernel (its ring takes much of shared memory); sets the
+// kernel's dynamic shared-memory limit on first use.  0 on failure.
+template <auto Kern>
+int ring_ctas_per_sm(int threads, int smem) {
+  static int n = -1;   // one per kernel; benign race: every thread computes the same value
+  if (n < 0) {
+    int k = 0;
+    if (cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, Kern, threads, smem) != cudaSuccess)
+      return 0;
+    n = k;
+  }
+  return n;
 }
 
 int grid_for(int64_t work, int per_sm, int sm_count) {
@@ -398,11 +657,29 @@ bsmma_status launch_group_quantize(const void* x, bool f32, int64_t total_M, int
   const DeviceInfo* dev = current_device(&st);
   if (!dev) return st;
   const int64_t work = ((total_M + 63) / 64) * (K / 128);
-  const int grid = grid_for(work, 8, dev->sm_count);
+  const int per_sm = f32 ? ring_ctas_per_sm<group_quant_kernel<true>>(kThreads, XRing<true>::kSmem)
+                         : ring_ctas_per_sm<group_quant_kernel<false>>(kThreads, XRing<false>::kSmem);
+  if (per_sm < 1) return BSMMA_ERR_CUDA;
+  // X[total_M][K] as 32-bit words: K/2 (BF16) or K (FP32) words x total_M rows, one
+  // 64 x 128-value tile per box.  An empty X has no tiles: the kernel only checks m_sizes
+  // and never reads the (zeroed) map.
+  CUtensorMap tm;
+  std::memset(&tm, 0, sizeof(tm));
+  if (total_M > 0) {
+    const uint64_t row_bytes = static_cast<uint64_t>(K) * (f32 ? 4 : 2);
+    const uint64_t dims[2] = {row_bytes / 4, static_cast<uint64_t>(total_M)};
+    const uint64_t strides[1] = {row_bytes};
+    const uint32_t box[2] = {f32 ? 128u : 64u, 64u};
+    st = encode_words(&tm, x, 2, dims, strides, box);
+    if (st != BSMMA_OK) return st;
+  }
+  const int grid = grid_for(work, per_sm, dev->sm_count);
   if (f32)
-    group_quant_kernel<true><<<grid, kThreads, 0, stream>>>(x, total_M, K, m_sizes, G, codes, scales, dev->status);
+    group_quant_kernel<true><<<grid, kThreads, XRing<true>::kSmem, stream>>>(
+        tm, total_M, K, m_sizes, G, codes, scales, dev->status, wait_limit_ns());
   else
-    group_quant_kernel<false><<<grid, kThreads, 0, stream>>>(x, total_M, K, m_sizes, G, codes, scales, dev->status);
+    group_quant_kernel<false><<<grid, kThreads, XRing<false>::kSmem, stream>>>(
+        tm, total_M, K, m_sizes, G, codes, scales, dev->status, wait_limit_ns());
   count_launches(1);
   return cuda_ok(cudaGetLastError());
 }
@@ -414,11 +691,25 @@ bsmma_status launch_block_quantize(const void* w, bool f32, int64_t G, int64_t N
   if (!dev) return st;
   const int64_t work = G * (N / 128) * (K / 128);
   if (work == 0) return BSMMA_OK;
-  const int grid = grid_for(work, 4, dev->sm_count);
+  const int per_sm = f32 ? ring_ctas_per_sm<block_quant_kernel<true>>(kBlockThreads, WRing<true>::kSmem)
+                         : ring_ctas_per_sm<block_quant_kernel<false>>(kBlockThreads, WRing<false>::kSmem);
+  if (per_sm < 1) return BSMMA_ERR_CUDA;
+  // W[G][N][K] as 32-bit words: K/2 (BF16) or K (FP32) words x N rows x G matrices,
+  // one 128x128-value block per box
+  CUtensorMap tm;
+  const uint64_t row_bytes = static_cast<uint64_t>(K) * (f32 ? 4 : 2);
+  const uint64_t dims[3] = {row_bytes / 4, static_cast<uint64_t>(N), static_cast<uint64_t>(G)};
+  const uint64_t strides[2] = {row_bytes, row_bytes * static_cast<uint64_t>(N)};
+  const uint32_t box[3] = {f32 ? 128u : 64u, 128u, 1u};
+  st = encode_words(&tm, w, 3, dims, strides, box);
+  if (st != BSMMA_OK) return st;
+  const int grid = grid_for(work, per_sm, dev->sm_count);
   if (f32)
-    block_quant_kernel<true><<<grid, kBlockThreads, 0, stream>>>(w, G, N, K, codes, scales);
+    block_quant_kernel<true><<<grid, kBlockThreads, WRing<true>::kSmem, stream>>>(
+        tm, G, N, K, codes, scales, dev->status, wait_limit_ns());
   else
-    block_quant_kernel<false><<<grid, kBlockThreads, 0, stream>>>(w, G, N, K, codes, scales);
+    block_quant_kernel<false><<<grid, kBlockThreads, WRing<false>::kSmem, stream>>>(
+        tm, G, N, K, codes, scales, dev->status, wait_limit_ns());
   count_launches(1);
   return cuda_ok(cudaGetLastError());
 }

@@ -145,17 +145,18 @@ def test_block_quantize_bit_exact(GNK, dtype):
     assert np.array_equal(scales.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
 
 
-def near_midpoint_blocks(seed, nblocks, block_len):
+def near_midpoint_blocks(seed, nblocks, block_len, log2_range=(-30, 30)):
     """nblocks blocks of block_len FP32 values whose quotients x / s land on, or within
     three units in the last place of, E4M3 rounding midpoints, each block with its own
-    random normal scale s (the block's first value is its amax)."""
-    g = np.random.default_rng([seed, nblocks, block_len])
+    random scale s = amax / 448, log2(amax / 448) uniform in log2_range (the block's
+    first value is its amax)."""
+    g = np.random.default_rng([seed, nblocks, block_len, 1000 + int(log2_range[0])])
     codes = torch.from_numpy(np.arange(127, dtype=np.uint8)).view(torch.float8_e4m3fn)
     vals = np.unique(codes.float().numpy())                          # 0, 2^-9, ..., 448
     mids = ((vals[1:] + vals[:-1]) / 2).astype(np.float32)           # 2^-10, ..., 432
     x = np.zeros((nblocks, block_len), dtype=np.float32)
     for j in range(nblocks):
-        amax = np.float32(448.0) * np.float32(2.0) ** np.float32(g.uniform(-30, 30))
+        amax = np.float32(np.float64(448.0) * 2.0 ** g.uniform(*log2_range))
         s = max(np.float32(amax / np.float32(448.0)), np.float32(2.0 ** -149))
         xs = (g.choice(mids, size=block_len - 1) * s).astype(np.float32)
         steps = g.integers(-3, 4, size=block_len - 1)
@@ -170,13 +171,40 @@ def near_midpoint_blocks(seed, nblocks, block_len):
 
 
 def test_group_quantize_near_boundaries():
-    """The quotient shortcut (a product with 1/s, exact division near E4M3 rounding
-    boundaries) gives the oracle's codes for quotients on and around every midpoint."""
+    """The quotient from the block's reciprocal and two FMA corrections gives the
+    oracle's codes for quotients on and around every E4M3 rounding midpoint."""
     x = near_midpoint_blocks(67, 2048, 128)
     ms = np.array([700, 0, 1348], dtype=np.int64)
     codes, scales = bs.fp8_group_quantize(torch.from_numpy(x).cuda(), torch.from_numpy(ms).cuda())
     torch.cuda.synchronize()
     ref_c, ref_s = oracle.fp8_group_quantize(x, ms)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+    assert np.array_equal(codes.cpu().numpy(), ref_c)
+
+
+# Scales across the whole FP32 range: subnormal (the 2^-149 floor), around 2^-88 where
+# the quotient switches between IEEE division and the FMA sequence, and up to amax near
+# FLT_MAX.
+SCALE_RANGES = [(-170.0, -120.0), (-95.0, -80.0), (-40.0, 40.0), (100.0, 118.9)]
+
+
+@pytest.mark.parametrize("log2_range", SCALE_RANGES, ids=lambda r: f"s2^{r[0]:g}..{r[1]:g}")
+def test_group_quantize_scale_extremes(log2_range):
+    x = near_midpoint_blocks(69, 1024, 128, log2_range)
+    ms = np.array([300, 724], dtype=np.int64)
+    codes, scales = bs.fp8_group_quantize(torch.from_numpy(x).cuda(), torch.from_numpy(ms).cuda())
+    torch.cuda.synchronize()
+    ref_c, ref_s = oracle.fp8_group_quantize(x, ms)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+    assert np.array_equal(codes.cpu().numpy(), ref_c)
+
+
+@pytest.mark.parametrize("log2_range", SCALE_RANGES, ids=lambda r: f"s2^{r[0]:g}..{r[1]:g}")
+def test_block_quantize_scale_extremes(log2_range):
+    w = near_midpoint_blocks(70, 8, 128 * 128, log2_range).reshape(1, 8 * 128, 128)
+    codes, scales = bs.fp8_block_quantize(torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    ref_c, ref_s = oracle.fp8_block_quantize(w)
     assert np.array_equal(scales.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
     assert np.array_equal(codes.cpu().numpy(), ref_c)
 

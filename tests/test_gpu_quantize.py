@@ -122,6 +122,32 @@ def test_group_quantize_bit_exact(sizes, K, dtype):
     assert np.array_equal(scales.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_group_quantize_multi_pass(dtype):
+    """Enough 64 x 128 tiles (250 x 9) that every persistent CTA wraps its ring of tile
+    slots several times; total_M is not a multiple of 64 and the groups are uneven."""
+    ms = np.array([4000, 37, 0, 9000, 2963], dtype=np.int64)
+    T, K = int(ms.sum()), 1152
+    x = make_input((71, T, K), T, K, dtype)
+    codes, scales = bs.fp8_group_quantize(x.contiguous().cuda(), torch.from_numpy(ms).cuda())
+    torch.cuda.synchronize()
+    assert bs.device_status() == 0
+    ref_c, ref_s = oracle.fp8_group_quantize(as_oracle_input(x), ms)
+    assert np.array_equal(codes.cpu().numpy(), ref_c)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+
+
+def test_group_quantize_empty_x_checks_sizes():
+    """total_M = 0: nothing to quantise, but m_sizes is still checked on the device."""
+    empty = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    bs.fp8_group_quantize(empty, torch.zeros(3, dtype=torch.int64, device="cuda"))
+    torch.cuda.synchronize()
+    assert bs.device_status() == 0
+    bs.fp8_group_quantize(empty, torch.tensor([1, -1, 0], dtype=torch.int64, device="cuda"))
+    torch.cuda.synchronize()
+    assert bs.device_status() == bs.STATUS.index("BSMMA_DEV_BAD_MSIZES")
+
+
 def test_group_quantize_bad_sizes_writes_nothing():
     x = make_input((64, 0), 20, 256, "bf16").cuda()
     codes = torch.full((20, 256), 0x5A, dtype=torch.uint8, device="cuda")
@@ -140,6 +166,19 @@ def test_block_quantize_bit_exact(GNK, dtype):
     w = make_input((65, G, N, K), G * N, K, dtype).reshape(G, N, K)
     codes, scales = bs.fp8_block_quantize(w.contiguous().cuda())
     torch.cuda.synchronize()
+    ref_c, ref_s = oracle.fp8_block_quantize(w.float().numpy())
+    assert np.array_equal(codes.cpu().numpy(), ref_c)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_block_quantize_multi_pass(dtype):
+    """38 x 32 blocks: every persistent CTA wraps its ring of block slots several times."""
+    G, N, K = 1, 38 * 128, 32 * 128
+    w = make_input((72, G, N, K), G * N, K, dtype).reshape(G, N, K)
+    codes, scales = bs.fp8_block_quantize(w.contiguous().cuda())
+    torch.cuda.synchronize()
+    assert bs.device_status() == 0
     ref_c, ref_s = oracle.fp8_block_quantize(w.float().numpy())
     assert np.array_equal(codes.cpu().numpy(), ref_c)
     assert np.array_equal(scales.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))

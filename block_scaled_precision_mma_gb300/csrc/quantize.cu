@@ -301,26 +301,33 @@ __device__ __forceinline__ void lds8(const uint8_t* p, float (&v)[8]) {
 }
 
 // Activations X[total_M][K] over 1x128 blocks.  A persistent CTA keeps a ring of
-// kXStages tiles of 64 rows x 128 values in shared memory, each filled by one tensor copy
-// issued by thread 0 (rows past total_M arrive as zeros and are not stored), and
-// quantises the oldest while the others stream in.  Four threads share a row: thread
-// `seg` of row `row` owns the 8-value chunks at columns seg*8 + 32k (k < 4), visited from
-// k = row & 1 on so that a warp's even and odd rows read opposite halves of the shared-
-// memory banks.  Per row: the 4-lane amax, the scale, its reciprocal and the group
-// lookup, spread over 32 values.  Codes go out as 8-byte stores (32 contiguous bytes per
-// row and chunk); each row's scale to the per-group block layout.
+// kXStages tiles of 64 rows x 128 values in shared memory.  Warp 8 produces: one tensor
+// copy per tile (rows past total_M arrive as zeros and are not stored), each slot reused
+// once its `empty` barrier has one arrival from every consumer warp.  Warps 0-7 consume:
+// warp w owns rows 8w .. 8w + 7 of every tile, waits on the tile's `full` barrier itself
+// and releases the slot as soon as its rows are in registers, so no CTA-wide barrier is
+// taken per tile.  Four threads share a row: thread `seg` of row `row` owns the 8-value
+// chunks at columns seg*8 + 32k (k < 4), visited from k = row & 1 on so that a warp's even
+// and odd rows read opposite halves of the shared-memory banks.  Per row: the 4-lane amax,
+// the scale, its reciprocal and the group lookup, spread over 32 values.  Codes go out as
+// 8-byte stores (32 contiguous bytes per row and chunk); each row's scale to the
+// per-group block layout.  Every wait is bounded; a timeout raises a CTA-wide abort flag
+// that ends the other warps' waits, and the producer waits (bounded) for its copies in
+// flight before it exits.
 constexpr int kXStages = 4;
+constexpr int kXConsumerWarps = 8;
+constexpr int kXThreads = (kXConsumerWarps + 1) * 32;
 
 template <bool F32>
 struct XRing {
   static constexpr int kRowBytes = 128 * (F32 ? 4 : 2);
   static constexpr int kBytes = 64 * kRowBytes;               // one 64 x 128 tile
   // 1 KB of slack puts the ring on a 1024-byte boundary (tensor copies need 128)
-  static constexpr int kSmem = 1024 + kXStages * kBytes + kXStages * 8;
+  static constexpr int kSmem = 1024 + kXStages * kBytes + 2 * kXStages * 8;
 };
 
 template <bool F32>
-__global__ void __launch_bounds__(kThreads) group_quant_kernel(
+__global__ void __launch_bounds__(kXThreads) group_quant_kernel(
     const __grid_constant__ CUtensorMap tmX, int64_t total_M, int64_t K, const int64_t* m_sizes,
     int G, uint8_t* codes, float* sx, int* status, uint64_t limit_ns) {
   using R = XRing<F32>;
@@ -328,9 +335,12 @@ __global__ void __launch_bounds__(kThreads) group_quant_kernel(
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(xring_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + kXStages * R::kBytes);
+  uint64_t* empty = full + kXStages;
   __shared__ int64_t start[kMaxGroups + 1];
   __shared__ int64_t size[kMaxGroups];
-  __shared__ int bad, landed;
+  __shared__ int bad;
+  __shared__ volatile int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // tile indices fit 32 bits (the entry point bounds total_M and K)
   const int KB = static_cast<int>(K / 128);
   const int tiles = static_cast<int>((total_M + 63) / 64) * KB;
@@ -341,15 +351,6 @@ __global__ void __launch_bounds__(kThreads) group_quant_kernel(
     const int t = static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x);
     rt = t / KB;
     kb = t - rt * KB;
-  };
-  // thread 0: the tile of iteration `it` into its slot
-  auto issue = [&](int it) {
-    if (it >= mine) return;
-    int rt, kb;
-    tile_of(it, rt, kb);
-    const int slot = it % kXStages;
-    mbar_arrive_expect_tx(&full[slot], R::kBytes);
-    tma_load_2d(&tmX, &full[slot], ring + slot * R::kBytes, kb * (F32 ? 128 : 64), rt * 64);
   };
   if (threadIdx.x == 0) {
     int64_t row = 0;
@@ -364,38 +365,55 @@ __global__ void __launch_bounds__(kThreads) group_quant_kernel(
     if (row != total_M) b = 1;
     start[G] = row;
     bad = b;
+    abort_flag = 0;
     if (b && blockIdx.x == 0) report_status(status, kDevBadMSizes);
     if (!b && mine > 0) {
-      prefetch_tmap(&tmX);
-      for (int st = 0; st < kXStages; ++st) mbar_init(&full[st], 1);
+      for (int st = 0; st < kXStages; ++st) {
+        mbar_init(&full[st], 1);
+        mbar_init(&empty[st], kXConsumerWarps);
+      }
       fence_mbar_init();
-      for (int it = 0; it < kXStages; ++it) issue(it);
     }
   }
   __syncthreads();
-  if (bad) return;   // uniform: nothing is written, nothing was issued
-  static_assert(kThreads == 4 * 64, "four threads per row of a 64-row tile");
-  const int seg = threadIdx.x & 3, rloc = threadIdx.x >> 2;
-  const int rot = rloc & 1;
-  int it = 0;
-  for (; it < mine; ++it) {
-    const int slot = it % kXStages;
-    if (threadIdx.x == 0) {
-      volatile int no_abort = 0;
-      landed = mbar_wait(&full[slot], (it / kXStages) & 1, limit_ns, &no_abort, status) ? 1 : 0;
+  if (bad || mine == 0) return;   // uniform: nothing is written, nothing was issued
+  if (warp == kXConsumerWarps) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tmap(&tmX);
+      int issued = 0;
+      for (int it = 0; it < mine; ++it) {
+        const int slot = it % kXStages;
+        if (it >= kXStages &&
+            !mbar_wait(&empty[slot], ((it / kXStages) - 1) & 1, limit_ns, &abort_flag, status))
+          break;
+        int rt, kb;
+        tile_of(it, rt, kb);
+        mbar_arrive_expect_tx(&full[slot], R::kBytes);
+        tma_load_2d(&tmX, &full[slot], ring + slot * R::kBytes, kb * (F32 ? 128 : 64), rt * 64);
+        issued = it + 1;
+      }
+      // copies still in flight must land before the CTA's memory is released
+      for (int j = issued > kXStages ? issued - kXStages : 0; j < issued; ++j) {
+        volatile int no_abort = 0;
+        mbar_wait(&full[j % kXStages], (j / kXStages) & 1, limit_ns / 4 + 1, &no_abort, nullptr);
+      }
     }
-    __syncthreads();                      // the tile is visible to every thread
-    if (!landed) break;                   // uniform
+    return;
+  }
+  // ------------------------------------------------------------------ consumers
+  const int seg = lane & 3, rloc = warp * 8 + (lane >> 2);
+  const int rot = rloc & 1;
+  for (int it = 0; it < mine; ++it) {
+    const int slot = it % kXStages;
+    if (!mbar_wait(&full[slot], (it / kXStages) & 1, limit_ns, &abort_flag, status)) break;
     const uint8_t* trow = ring + slot * R::kBytes + rloc * R::kRowBytes;
     float v[4][8];
 #pragma unroll
     for (int k = 0; k < 4; ++k)
       lds8<F32>(trow + (seg * 8 + 32 * ((k + rot) & 3)) * (F32 ? 4 : 2), v[k]);
-    __syncthreads();                      // the slot is read out
-    if (threadIdx.x == 0) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(it + kXStages);
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);   // this warp's rows are in registers
     int rt, kb;
     tile_of(it, rt, kb);
     const int64_t row0 = static_cast<int64_t>(rt) * 64;
@@ -428,12 +446,6 @@ __global__ void __launch_bounds__(kThreads) group_quant_kernel(
       if (seg == 0) sx[start[g] * KB + (r - start[g]) + static_cast<int64_t>(kb) * size[g]] = s;
     }
   }
-  // after a timeout, copies already issued must land before the CTA's memory is released
-  if (threadIdx.x == 0)
-    for (int j = it; j < it + kXStages && j < mine; ++j) {
-      volatile int no_abort = 0;
-      mbar_wait(&full[j % kXStages], (j / kXStages) & 1, limit_ns / 4 + 1, &no_abort, nullptr);
-    }
 }
 
 // Weights W[G][N][K] over 128x128 blocks.  A persistent CTA of 512 threads keeps a ring
@@ -657,8 +669,8 @@ bsmma_status launch_group_quantize(const void* x, bool f32, int64_t total_M, int
   const DeviceInfo* dev = current_device(&st);
   if (!dev) return st;
   const int64_t work = ((total_M + 63) / 64) * (K / 128);
-  const int per_sm = f32 ? ring_ctas_per_sm<group_quant_kernel<true>>(kThreads, XRing<true>::kSmem)
-                         : ring_ctas_per_sm<group_quant_kernel<false>>(kThreads, XRing<false>::kSmem);
+  const int per_sm = f32 ? ring_ctas_per_sm<group_quant_kernel<true>>(kXThreads, XRing<true>::kSmem)
+                         : ring_ctas_per_sm<group_quant_kernel<false>>(kXThreads, XRing<false>::kSmem);
   if (per_sm < 1) return BSMMA_ERR_CUDA;
   // X[total_M][K] as 32-bit words: K/2 (BF16) or K (FP32) words x total_M rows, one
   // 64 x 128-value tile per box.  An empty X has no tiles: the kernel only checks m_sizes
@@ -675,10 +687,10 @@ bsmma_status launch_group_quantize(const void* x, bool f32, int64_t total_M, int
   }
   const int grid = grid_for(work, per_sm, dev->sm_count);
   if (f32)
-    group_quant_kernel<true><<<grid, kThreads, XRing<true>::kSmem, stream>>>(
+    group_quant_kernel<true><<<grid, kXThreads, XRing<true>::kSmem, stream>>>(
         tm, total_M, K, m_sizes, G, codes, scales, dev->status, wait_limit_ns());
   else
-    group_quant_kernel<false><<<grid, kThreads, XRing<false>::kSmem, stream>>>(
+    group_quant_kernel<false><<<grid, kXThreads, XRing<false>::kSmem, stream>>>(
         tm, total_M, K, m_sizes, G, codes, scales, dev->status, wait_limit_ns());
   count_launches(1);
   return cuda_ok(cudaGetLastError());

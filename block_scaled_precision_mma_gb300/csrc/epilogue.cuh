@@ -17,14 +17,28 @@ struct Epilogue {
   int act;                     // 0 none, 1 ReLU, 2 GELU (erf form), 3 SiLU
 };
 
-__device__ __forceinline__ float activate(float v, int act) {
-  switch (act) {
-    case 1: return fmaxf(v, 0.f);
-    case 2: return 0.5f * v * (1.f + erff(v * 0.70710678118654752440f));   // x * Phi(x)
-    case 3: return __fdiv_rn(v, 1.f + expf(-v));                            // x * sigmoid(x)
-    default: return v;
-  }
+// GELU in its erf form, x * Phi(x) = x (1 + erf(x / sqrt 2)) / 2.  erf comes from
+// Abramowitz & Stegun, "Handbook of Mathematical Functions", formula 7.1.26: for u >= 0,
+// erfc(u) = (a1 t + a2 t^2 + ... + a5 t^5) e^(-u^2) + eps with t = 1 / (1 + p u) and
+// |eps| <= 1.5e-7.  With q = erfc(|x| / sqrt 2), 1 + erf(x / sqrt 2) is 2 - q for x >= 0
+// and q itself for x < 0, so negative inputs lose nothing to cancellation; the error in
+// the result stays below about |x| * 5e-7 (reciprocal and exponential by the fast
+// intrinsics; 2.8e-7 measured against erf in float32 over [-12, 12]).
+__device__ __forceinline__ float gelu_erf(float x) {
+  const float u = fabsf(x) * 0.70710678118654752440f;
+  const float t = __fdividef(1.f, fmaf(0.3275911f, u, 1.f));
+  float poly = 1.061405429f;
+  poly = fmaf(poly, t, -1.453152027f);
+  poly = fmaf(poly, t, 1.421413741f);
+  poly = fmaf(poly, t, -0.284496736f);
+  poly = fmaf(poly, t, 0.254829592f);
+  const float q = poly * t * __expf(-u * u);
+  return 0.5f * x * (x >= 0.f ? 2.f - q : q);
 }
+
+// x * sigmoid(x) = x / (1 + e^-x); for x below about -88 the denominator overflows and the
+// quotient is 0, the limit.
+__device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 
 // Eight accumulator values (FP32 bits) of columns col .. col+7 of one row -> out[0..7].
 // The bias is read with one 16-byte load (every lane of a warp reads the same columns,
@@ -43,9 +57,15 @@ __device__ __forceinline__ void store8(__nv_bfloat16* out, const uint32_t* r, in
       v[2 * j + 1] += __uint_as_float(w[j] & 0xFFFF0000u);
     }
   }
-  if (e.act) {
+  if (e.act == 1) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = activate(v[j], e.act);
+    for (int j = 0; j < 8; ++j) v[j] = fmaxf(v[j], 0.f);
+  } else if (e.act == 2) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = gelu_erf(v[j]);
+  } else if (e.act == 3) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = silu(v[j]);
   }
   st_global_v4_cs(out, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
                   pack_bf16x2(v[6], v[7]));

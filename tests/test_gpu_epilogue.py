@@ -96,3 +96,28 @@ def test_k_zero_gives_act_of_bias():
         torch.cuda.synchronize()
         ref = oracle.bias_act(np.zeros((M, N)), bias.float().numpy(), act)
         assert_close(D.float().cpu().numpy(), ref, f"K=0 {act}")
+
+
+def test_activation_tails():
+    """K = 0 gives D = act(bias) exactly, so a bias spanning +-120 probes each activation's
+    tails (GELU's erfc form for large negative inputs, SiLU's overflowing denominator)."""
+    M, N = 8, 1024
+    g = np.random.default_rng(73)
+    b = np.concatenate([np.linspace(-120.0, 120.0, N // 2), g.uniform(-12.0, 12.0, N // 2)])
+    bias = torch.from_numpy(b.astype(np.float32)).to(torch.bfloat16)
+    empty = torch.empty(0, dtype=torch.uint8, device="cuda")
+    for act in ACTS:
+        D = bs.mx_gemm(empty, empty, empty, empty, "NT", M=M, N=N, K=0, bias=bias.cuda(), act=act)
+        torch.cuda.synchronize()
+        ref = oracle.bias_act(np.zeros((M, N)), bias.float().numpy(), act)
+        assert_close(D.float().cpu().numpy(), ref, f"tails {act}")
+
+
+@pytest.mark.parametrize("act", ["gelu", "silu"])
+def test_large_negative_preactivations(act):
+    """A bias of -40 pushes most outputs far into the activations' negative tails."""
+    M, N, K = 256, 512, 256
+    c = synthetic.mx_operands((74, 0), M, N, K, "NT", "e4m3", "e4m3")
+    bias = torch.full((N,), -40.0).to(torch.bfloat16)
+    got, ref = run_case(c, bias, act)
+    assert_close(got, ref, f"negative tail {act}")

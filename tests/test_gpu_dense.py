@@ -72,6 +72,35 @@ def test_dense_persistent_many_tiles(layout, af, variant):
     check(c, rows=sample_rows(M, 96, 1))
 
 
+# single rows (decode-like), the narrowest N each layout allows (D rows are 16 bytes,
+# NN's B rows and TN's A rows 16 bytes of FP8) and one K block
+DEGENERATE = [
+    (1, 8, 32, "NT", "e4m3", "e4m3"),
+    (1, 8, 64, "NT", "e2m1", "e2m1"),
+    (1, 264, 1024, "NT", "e4m3", "e5m2"),
+    (3, 16, 96, "NN", "e4m3", "e5m2"),
+    (16, 16, 32, "TN", "e5m2", "e5m2"),
+    (129, 8, 160, "NT", "e5m2", "e4m3"),
+]
+
+
+@pytest.mark.parametrize("shape", DEGENERATE, ids=lambda s: "-".join(map(str, s)))
+def test_dense_degenerate(shape, variant):
+    M, N, K, layout, af, bf = shape
+    check(synthetic.mx_operands((58, M, N, K), M, N, K, layout, af, bf))
+
+
+def test_dense_empty_output():
+    """M = 0 or N = 0: nothing to compute, nothing launched, no error."""
+    for M, N in ((0, 64), (64, 0)):
+        c = synthetic.mx_operands((59, M, N), max(M, 1), max(N, 8), 64, "NT", "e4m3", "e4m3")
+        A, sA, B, sB = (to_dev(c[k]) for k in ("A", "sA", "B", "sB"))
+        D = bs.mx_gemm(A[:M], sA[:M], B[:N], sB[:N], "NT", M=M, N=N, K=64)
+        torch.cuda.synchronize()
+        assert tuple(D.shape) == (M, N)
+        assert bs.device_status() == 0
+
+
 def test_tiled_scales_match_plain():
     c = synthetic.mx_operands((2, 600), 384, 512, 512, "NT", "e4m3", "e4m3")
     a = run_dense(c)

@@ -189,7 +189,10 @@ typedef enum {
  * FP32 accumulation mx_gemm rounds directly.  Activation and bias are the follow-up
  * named in "[gfx1250] Add MXFP4 GEMM support to FlyDSL backend", Description (the
  * plain GEMM has neither); the activation set and the erf form of GELU are this
- * library's reading.
+ * library's reading.  Accuracy before the BF16 rounding: GELU's erf is evaluated by
+ * Abramowitz & Stegun formula 7.1.26 (erfc form for negative inputs), so the activation
+ * is within about 5e-7 |x| of the exact one; SiLU uses the fast exponential and divide
+ * (a few ulp).  Both are far below the BF16 output step.
  *   bias  BF16 [N] in device memory, 16-byte aligned, or NULL for none.
  *   act   a bsmma_activation.
  * Everything else, including preconditions and errors, is as for mx_gemm / mx_gemm_tiled.

@@ -21,6 +21,7 @@ runs are independent replicas (no collective on the data path).
 from __future__ import annotations
 
 import argparse
+import atexit
 import hashlib
 import json
 import os
@@ -131,7 +132,10 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """Samples nvidia-smi SM clocks and throttle reasons while running."""
+    """Samples nvidia-smi SM clocks and throttle reasons every 50 ms.  Started before the
+    warm-up (nvidia-smi's start-up can stall CUDA calls of this process for tens of ms, so
+    it must not fall inside the timed region); only samples that arrive inside the timed
+    window set by window() are summarised."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
@@ -139,9 +143,10 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []          # (arrival time, line)
+        self.t0 = self.t1 = None
 
-    def __enter__(self):
+    def start(self, settle_s: float = 5.0):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
@@ -149,26 +154,45 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            deadline = time.perf_counter() + settle_s
+            while not self.lines and time.perf_counter() < deadline and self.proc.poll() is None:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
+        if self.proc:
+            atexit.register(self.stop)   # also on an error before the timed region ends
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
-    def __exit__(self, *exc):
-        if self.proc:
+    def window(self, t0: float, t1: float):
+        self.t0, self.t1 = t0, t1
+
+    def stop(self):
+        if self.proc and self.proc.poll() is None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
 
+    def __enter__(self):
+        return self.start()
+
+    def __exit__(self, *exc):
+        self.stop()
+
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines = self.lines
+        if self.t0 is not None:
+            # a sample arrives up to one period after it was taken
+            inside = [(t, ln) for t, ln in lines if self.t0 <= t <= self.t1 + 0.06]
+            lines = inside if inside else lines
+        for _, ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 7:
                 continue
@@ -311,6 +335,7 @@ def run_ours(args):
             one_gemm(g, t, ev)
 
     mk = lambda: [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in gemms]
+    clk = ClockSampler(local).start()
     for _ in range(args.warmup):
         step(mk())
     torch.cuda.synchronize()
@@ -321,12 +346,15 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     n_launch0 = bs.launch_count()
-    with ClockSampler(local) as clk:
+    try:
         wall0 = time.perf_counter()
         for i in range(args.steps):
             step(all_events[i])
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
+    finally:
+        clk.stop()
+    clk.window(wall0, wall0 + wall)
     n_launch = bs.launch_count() - n_launch0
     st = bs.device_status()
     if st != 0:
@@ -579,6 +607,7 @@ def run_quantize(args):
             ev[1].record(stream)
 
     mk = lambda: [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in ops]
+    clk = ClockSampler(local).start()
     for _ in range(args.warmup):
         step(mk())
     torch.cuda.synchronize()
@@ -589,12 +618,15 @@ def run_quantize(args):
         dist.barrier()
     torch.cuda.synchronize()
     n0 = bs.launch_count()
-    with ClockSampler(local) as clk:
+    try:
         wall0 = time.perf_counter()
         for i in range(args.steps):
             step(all_events[i])
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
+    finally:
+        clk.stop()
+    clk.window(wall0, wall0 + wall)
     n_launch = bs.launch_count() - n0
     st = bs.device_status()
     if st != 0:

@@ -1,8 +1,8 @@
-"""CUDA-graph capture of every entry point that runs on the device: each call is captured
-once, then replayed after new inputs (and, for the grouped calls, a different m_sizes
-split of the same total_M) have been copied into the captured buffers.  Every replay is
-compared with the oracle on the new inputs, so nothing may have been read on the host or
-baked into the graph at capture time."""
+"""CUDA-graph capture of every entry point that runs on the device, and concurrent streams.
+Each call is captured once, then replayed after new inputs (and, for the grouped calls, a
+different m_sizes split of the same total_M) have been copied into the captured buffers.
+Every replay is compared with the oracle on the new inputs, so nothing may have been read
+on the host or baked into the graph at capture time."""
 import numpy as np
 import pytest
 import torch
@@ -123,3 +123,23 @@ def test_quantisers_replay_with_new_inputs():
         rc, rs = oracle.fp8_block_quantize(wh.float().numpy())
         assert np.array_equal(bq_c.cpu().numpy(), rc)
         assert np.array_equal(bq_s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+
+
+def test_mx_gemm_concurrent_streams():
+    """Two streams call mx_gemm at once with different operands: each stream relayouts
+    its scales into its own workspace, so neither result is disturbed by the other."""
+    M, N, K = 512, 1024, 1024
+    cs = [synthetic.mx_operands((93, i), M, N, K, "NT", "e4m3", "e4m3") for i in range(2)]
+    ops = [[to_dev(c[k]) for k in ("A", "sA", "B", "sB")] for c in cs]
+    outs = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in cs]
+    streams = [torch.cuda.Stream() for _ in cs]
+    torch.cuda.synchronize()
+    for _ in range(4):
+        for o, d, s in zip(ops, outs, streams):
+            with torch.cuda.stream(s):
+                bs.mx_gemm(*o, "NT", out=d)
+    torch.cuda.synchronize()
+    assert bs.device_status() == 0
+    for c, d in zip(cs, outs):
+        ref = oracle.mx_gemm(c["A"], c["sA"], c["B"], c["sB"], M, N, K, "NT")
+        assert_close(d.float().cpu().numpy(), ref, "concurrent streams")

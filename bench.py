@@ -858,8 +858,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
     ap.add_argument("--grouped-width", type=int, default=0, choices=[0, 128, 256],
                     help="grouped tile width: 0 automatic, 128 or 256 (tuning only)")
-    ap.add_argument("--dense-variant", type=int, default=0, choices=[0, 1, 2, 3],
-                    help="0 automatic, 1 single-CTA tiles, 2 CTA pairs, 3 SM-pair MMAs (tuning only)")
+    ap.add_argument("--dense-variant", type=int, default=0, choices=[0, 1, 3],
+                    help="0 automatic, 1 single-CTA tiles, 3 SM-pair MMAs (tuning only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     args = ap.parse_args()

@@ -230,7 +230,7 @@ def set_wait_limit_ns(ns: int):
 
 
 def set_dense_variant(variant: int):
-    """0 automatic, 1 single-CTA tiles, 2 CTA pairs sharing a multicast B tile."""
+    """0 automatic (SM-pair MMAs), 1 single-CTA tiles, 3 SM-pair MMAs."""
     _check(load().bsmma_set_dense_variant(int(variant)), "bsmma_set_dense_variant")
 
 

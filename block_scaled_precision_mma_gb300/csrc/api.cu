@@ -46,8 +46,12 @@ struct Workspace {
   cudaStream_t stream;
   void* ptr;
   int64_t bytes;
+  bool captured;   // handed to a kernel launch recorded into a CUDA graph
 };
 std::vector<Workspace> g_ws;
+// Buffers replaced by a larger one after a graph capture used them: a replay of that
+// graph still reads and writes them, so they stay allocated until the process exits.
+std::vector<void*> g_ws_kept;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -157,27 +161,34 @@ bsmma_status get_workspace(int64_t bytes, cudaStream_t stream, void** out) {
   Workspace* w = nullptr;
   for (auto& e : g_ws)
     if (e.device == dev && e.stream == stream) w = &e;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return BSMMA_ERR_CUDA;
+  const bool capturing = cap != cudaStreamCaptureStatusNone;
   if (w && w->bytes >= bytes) {
+    if (capturing) w->captured = true;
     *out = w->ptr;
     return BSMMA_OK;
   }
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return BSMMA_ERR_CUDA;
-  if (cap != cudaStreamCaptureStatusNone) return BSMMA_ERR_WORKSPACE;
+  if (capturing) return BSMMA_ERR_WORKSPACE;
   int64_t grow = bytes + bytes / 4 + 4096;
   void* p = nullptr;
   if (cudaMalloc(&p, static_cast<size_t>(grow)) != cudaSuccess) return BSMMA_ERR_CUDA;
   if (w) {
-    // earlier kernels on this stream may still read the old buffer
-    if (cudaStreamSynchronize(stream) != cudaSuccess) {
-      cudaFree(p);
-      return BSMMA_ERR_CUDA;
+    if (w->captured) {
+      g_ws_kept.push_back(w->ptr);   // a captured graph may still be replayed on it
+    } else {
+      // earlier kernels on this stream may still read the old buffer
+      if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaFree(p);
+        return BSMMA_ERR_CUDA;
+      }
+      cudaFree(w->ptr);
     }
-    cudaFree(w->ptr);
     w->ptr = p;
     w->bytes = grow;
+    w->captured = false;
   } else {
-    g_ws.push_back(Workspace{dev, stream, p, grow});
+    g_ws.push_back(Workspace{dev, stream, p, grow, false});
   }
   *out = p;
   return BSMMA_OK;
@@ -426,7 +437,7 @@ bsmma_status bsmma_set_wait_limit_ns(int64_t ns) {
 }
 
 bsmma_status bsmma_set_dense_variant(int variant) {
-  if (variant < 0 || variant > 3) return BSMMA_ERR_INVALID_ARG;
+  if (variant != 0 && variant != 1 && variant != 3) return BSMMA_ERR_INVALID_ARG;
   g_dense_variant = variant;
   return BSMMA_OK;
 }

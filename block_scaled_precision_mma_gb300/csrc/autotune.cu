@@ -5,7 +5,7 @@
 // gate, with a fixed choice when the gate is off; tuning never happens during graph
 // capture.  Here the shape class of the grouped GEMM is (nextPow2(total_M), N, K, G) and
 // the candidates are its two tile widths; the dense GEMM's class is (nextPow2(M), N, K,
-// layout, formats) and its candidates are the three kernel variants.
+// layout, formats) and its candidates are the SM-pair and the single-CTA kernels.
 //
 // The gate is BSMMA_AUTOTUNE=1 (or bsmma_autotune_configure); the cache file is
 // BSMMA_AUTOTUNE_CACHE, else $XDG_CACHE_HOME/bsmma/autotune.txt, else
@@ -107,6 +107,15 @@ int64_t next_pow2(int64_t v) {
   int64_t p = 1;
   while (p < v) p <<= 1;
   return v <= 0 ? 0 : p;
+}
+
+int autotune_cached(const std::string& key) {
+  Tuner& t = tuner();
+  std::lock_guard<std::mutex> g(t.mu);
+  t.ensure();
+  if (!t.enabled) return -1;
+  auto it = t.choices.find(key);
+  return it == t.choices.end() ? -1 : it->second;
 }
 
 int autotune_pick(const std::string& key, const std::vector<int>& candidates, int fallback,

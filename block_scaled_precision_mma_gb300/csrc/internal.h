@@ -24,7 +24,7 @@ struct DeviceInfo {
 const DeviceInfo* current_device(bsmma_status* err);
 
 uint64_t wait_limit_ns();
-int dense_variant();   // 0 automatic, 1 single CTAs, 2 CTA pairs, 3 SM-pair MMAs
+int dense_variant();   // 0 automatic, 1 single CTAs, 3 SM-pair MMAs
 int grouped_tile_width();   // 0 automatic, 128 or 256
 void count_launches(int n);
 
@@ -51,11 +51,13 @@ bsmma_status launch_wide_relayout(const uint8_t* sa, int64_t rows_a, uint8_t* ou
                                   int64_t kblocks, cudaStream_t stream);
 
 // Launchers (arguments already validated by the entry points).
-// bias: BF16 [N] or nullptr; act: bsmma_activation (0 = none).
+// bias: BF16 [N] or nullptr; act: bsmma_activation (0 = none).  may_tune: false keeps
+// the dense GEMM off the autotuner's timing runs (it then takes a stored choice, else
+// the SM-pair kernel).
 bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, const uint8_t* sfb,
                             void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
                             bsmma_fmt a_fmt, bsmma_fmt b_fmt, cudaStream_t stream,
-                            const void* bias = nullptr, int act = 0);
+                            const void* bias = nullptr, int act = 0, bool may_tune = true);
 bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B,
                                 const uint8_t* sfb, void* D, int64_t M, int64_t N, int64_t K,
                                 bsmma_layout layout, bsmma_fmt a_fmt, bsmma_fmt b_fmt,
@@ -77,6 +79,8 @@ bsmma_status launch_block_quantize(const void* w, bool f32, int64_t G, int64_t N
 // stream is not capturing -- the fastest of `candidates` timed with `launch`, else
 // `fallback`.
 int64_t next_pow2(int64_t v);
+// The stored choice for `key` when tuning is enabled, else -1; never times anything.
+int autotune_cached(const std::string& key);
 int autotune_pick(const std::string& key, const std::vector<int>& candidates, int fallback,
                   cudaStream_t stream, const std::function<bsmma_status(int)>& launch);
 

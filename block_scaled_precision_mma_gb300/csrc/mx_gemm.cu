@@ -15,10 +15,8 @@
 //   warps 2-9   epilogue: tcgen05.ld of the accumulator, release of tensor memory to
 //               the next tile, BF16 round-to-nearest-even, streaming 16-byte stores.
 // Tile 128 x 256, 128 bytes of K per stage (128 FP8 / 256 FP4 values), four MMAs per
-// stage.  As a CTA pair (2-CTA cluster) two vertically adjacent tiles share their B
-// tile: each CTA loads half of it and multicasts it to both.  Every wait is bounded;
-// a timed-out wait latches a status and every role unwinds to the common teardown,
-// which frees tensor memory.
+// stage.  Every wait is bounded; a timed-out wait latches a status and every role
+// unwinds to the common teardown, which frees tensor memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -37,7 +35,6 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfaCol = 256;   // 2 slots x 8 columns: row-scale chunks
 constexpr uint32_t kSfbCol = 288;   // 4 slots x 8 columns: column-scale blocks
 constexpr int kSmemLimit = 232448;  // 227 KB of dynamic shared memory per block
-constexpr bool kPairDefault = true;
 
 template <bool FP4>
 struct Cfg {
@@ -65,25 +62,19 @@ struct DenseParams {
   uint64_t limit_ns;
 };
 
-// Scheduling unit u -> output tile (mt, nt).  Single CTAs take one tile per unit;
-// a CTA pair takes two vertically adjacent tiles that share their B tile.  Units
-// walk the output in bands of kBandRows tile rows, along N inside a band, so that
-// the CTAs running at the same time touch a compact block of A and B that stays in L2.
+// Scheduling unit u -> output tile (mt, nt).  Units walk the output in bands of
+// kBandRows tile rows, along N inside a band, so that the CTAs running at the same
+// time touch a compact block of A and B that stays in L2.
 constexpr int kBandRows = 16;
 
-template <bool PAIR>
-__device__ __forceinline__ void unit_tile(const DenseParams& p, int u, uint32_t rank, int& mt,
-                                          int& nt) {
-  const int rows = PAIR ? (p.num_m_tiles + 1) >> 1 : p.num_m_tiles;   // unit rows
-  const int band = PAIR ? kBandRows / 2 : kBandRows;
-  const int per_band = band * p.num_n_tiles;
+__device__ __forceinline__ void unit_tile(const DenseParams& p, int u, int& mt, int& nt) {
+  const int per_band = kBandRows * p.num_n_tiles;
   const int b = u / per_band;
-  const int r0 = b * band;
-  const int h = rows - r0 < band ? rows - r0 : band;
+  const int r0 = b * kBandRows;
+  const int h = p.num_m_tiles - r0 < kBandRows ? p.num_m_tiles - r0 : kBandRows;
   const int v = u - b * per_band;
-  const int ur = r0 + v % h;
+  mt = r0 + v % h;
   nt = v / h;
-  mt = PAIR ? ur * 2 + static_cast<int>(rank) : ur;
 }
 
 // A ring position: slot index and the parity of its current phase.
@@ -107,7 +98,7 @@ __device__ __forceinline__ void tc_cp_wide(uint32_t taddr, uint64_t sdesc) {
 // 3+3+2+2 warps, so a thread may hold at most 16384 / (3 * 32) = 170 registers.
 // EPI: the output stage adds a bias and / or applies an activation (a separate
 // instantiation, so the plain GEMM's registers and code are unchanged).
-template <bool FP4, bool A_MN, bool B_MN, bool PAIR, bool EPI>
+template <bool FP4, bool A_MN, bool B_MN, bool EPI>
 __global__ void __maxnreg__(168)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSFA,
@@ -133,12 +124,10 @@ __global__ void __maxnreg__(168)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-  constexpr uint16_t kPairMask = 3;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], PAIR ? 2 : 1);   // a pair frees a stage only when both MMAs are done
+      mbar_init(&empty[s], 1);
     }
     for (int s = 0; s < C::kSfaSlots; ++s) {
       mbar_init(&sfa_full[s], 1);
@@ -164,13 +153,11 @@ __global__ void __maxnreg__(168)
   }
   tc_fence_before();
   __syncthreads();
-  if (PAIR) cluster_sync();   // the peer's barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total_units = PAIR ? ((p.num_m_tiles + 1) >> 1) * p.num_n_tiles
-                               : p.num_m_tiles * p.num_n_tiles;
-  const int first_unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int unit_stride = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int total_units = p.num_m_tiles * p.num_n_tiles;
+  const int first_unit = static_cast<int>(blockIdx.x);
+  const int unit_stride = static_cast<int>(gridDim.x);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -180,7 +167,7 @@ __global__ void __maxnreg__(168)
       bool ok = true;
       for (int u = first_unit; ok && u < total_units; u += unit_stride) {
         int mt, nt;
-        unit_tile<PAIR>(p, u, rank, mt, nt);
+        unit_tile(p, u, mt, nt);
         for (int ks = 0; ks < p.num_k_stages; ++ks) {
           if (!mbar_wait(&empty[st.slot], st.phase ^ 1, p.limit_ns, abort_flag, p.status)) {
             ok = false;
@@ -193,16 +180,7 @@ __global__ void __maxnreg__(168)
           uint8_t* b_dst = sB + st.slot * C::kBBytes;
           if (A_MN) tma_load_2d(&tmA, &full[st.slot], a_dst, mt * kBM, ks * 128);
           else      tma_load_2d(&tmA, &full[st.slot], a_dst, ks * 128, mt * kBM);
-          if (PAIR) {
-            // this CTA's 128-row half of the B tile, to both CTAs
-            const int r = static_cast<int>(rank);
-            if (B_MN)
-              tma_load_2d_mc(&tmB, &full[st.slot], b_dst + r * 16384, nt * kBN + r * 128,
-                             ks * 128, kPairMask);
-            else
-              tma_load_2d_mc(&tmB, &full[st.slot], b_dst + r * 16384, ks * 128,
-                             nt * kBN + r * 128, kPairMask);
-          } else if (B_MN) {
+          if (B_MN) {
             tma_load_2d(&tmB, &full[st.slot], b_dst, nt * kBN, ks * 128);
             tma_load_2d(&tmB, &full[st.slot], b_dst + 16384, nt * kBN + 128, ks * 128);
           } else {
@@ -300,8 +278,7 @@ __global__ void __maxnreg__(168)
               mma_mxf8f6f4(tmem, ad, bd, p.idesc | idesc_sf_id(j, j), sfa_t + 4 * sub, sfb_t[0], acc);
             }
           }
-          if (PAIR) tc_commit_mc(&empty[st.slot], kPairMask);
-          else tc_commit(&empty[st.slot]);
+          tc_commit(&empty[st.slot]);
           st.advance(C::kStages);
           if (sub == C::kStagesPerChunk - 1 || ks == p.num_k_stages - 1) ++chunk;
         }
@@ -321,7 +298,7 @@ __global__ void __maxnreg__(168)
     int local = 0;
     for (int u = first_unit; u < total_units; u += unit_stride, ++local) {
       int mt, nt;
-      unit_tile<PAIR>(p, u, rank, mt, nt);
+      unit_tile(p, u, mt, nt);
       if (!mbar_wait(acc_full, local & 1, p.limit_ns, abort_flag, p.status)) break;
       tc_fence_after();
       uint32_t r[kChunks][32];
@@ -363,64 +340,26 @@ __global__ void __maxnreg__(168)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  // neither CTA of a pair leaves while its peer may still signal its barriers
-  if (PAIR) cluster_sync();
 }
 
-template <bool FP4, bool A_MN, bool B_MN, bool PAIR, bool EPI>
+template <bool FP4, bool A_MN, bool B_MN, bool EPI>
 bsmma_status launch_dense(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                           const CUtensorMap& tsb, const DenseParams& p, int sm_count,
                           cudaStream_t stream) {
   using C = Cfg<FP4>;
-  auto kern = mx_gemm_kernel<FP4, A_MN, B_MN, PAIR, EPI>;
-  static int max_clusters = -1;   // benign race: every thread computes the same value
-  if (max_clusters < 0) {
+  auto kern = mx_gemm_kernel<FP4, A_MN, B_MN, EPI>;
+  static bool attr_set = false;   // benign race: setting the attribute twice is harmless
+  if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
       return BSMMA_ERR_CUDA;
-    int n = sm_count;
-    if (PAIR) {
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 2;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.gridDim = dim3(2 * sm_count, 1, 1);
-      cfg.blockDim = dim3(kThreads, 1, 1);
-      cfg.dynamicSmemBytes = C::kSmemBytes;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1)
-        return BSMMA_ERR_CUDA;
-    }
-    max_clusters = n;
+    attr_set = true;
   }
-  const int64_t units = PAIR ? static_cast<int64_t>((p.num_m_tiles + 1) / 2) * p.num_n_tiles
-                             : static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
-  const int64_t slots = PAIR ? max_clusters : sm_count;   // co-resident CTAs (pairs)
-  const int grid = static_cast<int>((units < slots ? units : slots) * (PAIR ? 2 : 1));
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = PAIR ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, p);
+  const int64_t units = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
+  const int grid = static_cast<int>(units < sm_count ? units : sm_count);
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(ta, tb, tsa, tsb, p);
   count_launches(1);
-  return cuda_ok(e == cudaSuccess ? cudaGetLastError() : e);
-}
-
-// One CTA per 128x256 tile (variant 1) or CTA pairs sharing a multicast B tile (2).
-bool use_pair(int num_m_tiles, int v) {
-  if (v == 1) return false;
-  return kPairDefault && num_m_tiles >= 1;
+  return cuda_ok(cudaGetLastError());
 }
 
 }  // namespace
@@ -435,19 +374,24 @@ bsmma_status launch_mx_gemm_variant(const void* A, const uint8_t* sfa, const voi
 bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, const uint8_t* sfb,
                             void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
                             bsmma_fmt a_fmt, bsmma_fmt b_fmt, cudaStream_t stream,
-                            const void* bias, int act) {
-  // SM-pair MMAs unless a one-CTA variant is asked for, or (opt-in) tuning per
-  // (nextPow2(M), N, K, layout, formats) picks another
+                            const void* bias, int act, bool may_tune) {
+  // SM-pair MMAs unless the one-CTA variant is asked for, or (opt-in) tuning per
+  // (nextPow2(M), N, K, layout, formats) picks it
   int variant = dense_variant();
   if (variant == 0) {
     const std::string key = "dense " + std::to_string(next_pow2(M)) + " " + std::to_string(N) +
                             " " + std::to_string(K) + " " + std::to_string(static_cast<int>(layout)) +
                             " " + std::to_string(static_cast<int>(a_fmt)) + " " +
                             std::to_string(static_cast<int>(b_fmt));
-    variant = autotune_pick(key, {3, 2, 1}, 3, stream, [&](int v) {
-      return launch_mx_gemm_variant(A, sfa, B, sfb, D, M, N, K, layout, a_fmt, b_fmt, stream, bias,
-                                    act, v);
-    });
+    if (may_tune) {
+      variant = autotune_pick(key, {3, 1}, 3, stream, [&](int v) {
+        return launch_mx_gemm_variant(A, sfa, B, sfb, D, M, N, K, layout, a_fmt, b_fmt, stream,
+                                      bias, act, v);
+      });
+    } else {
+      const int cached = autotune_cached(key);
+      variant = cached == 1 || cached == 3 ? cached : 3;
+    }
   }
   return launch_mx_gemm_variant(A, sfa, B, sfb, D, M, N, K, layout, a_fmt, b_fmt, stream, bias,
                                 act, variant);
@@ -469,12 +413,11 @@ bsmma_status launch_mx_gemm_variant(const void* A, const uint8_t* sfa, const voi
   const int64_t kq = (kblocks + 7) / 8;          // row-scale chunks per 128 rows
   const int64_t kgp = 2 * ((kblocks + 7) / 8);   // column-scale blocks per 256 columns
   const int num_m_tiles = static_cast<int>((M + kBM - 1) / kBM);
-  const bool pair = use_pair(num_m_tiles, variant);
   CUtensorMap ta, tb, tsa, tsb;
   if (layout == BSMMA_TN) st = encode_tmap_u8(&ta, A, M, K, M, 128, 128);
   else st = encode_tmap_u8(&ta, A, kbytes, M, kbytes, 128, 128);
   if (st != BSMMA_OK) return st;
-  if (layout == BSMMA_NT) st = encode_tmap_u8(&tb, B, kbytes, N, kbytes, 128, pair ? 128 : kBN);
+  if (layout == BSMMA_NT) st = encode_tmap_u8(&tb, B, kbytes, N, kbytes, 128, kBN);
   else st = encode_tmap_u8(&tb, B, N, K, N, 128, 128);
   if (st != BSMMA_OK) return st;
   // both scale layouts viewed as rows of 1 KB ([*][256 words]): a row-scale chunk is 4
@@ -503,22 +446,14 @@ bsmma_status launch_mx_gemm_variant(const void* A, const uint8_t* sfa, const voi
   p.limit_ns = wait_limit_ns();
   const int sms = dev->sm_count;
   const bool epi = bias != nullptr || act != 0;
-#define BSMMA_DENSE(F, A, B, P)                                                  \
-  (epi ? launch_dense<F, A, B, P, true>(ta, tb, tsa, tsb, p, sms, stream)        \
-       : launch_dense<F, A, B, P, false>(ta, tb, tsa, tsb, p, sms, stream))
-  if (pair) {
-    if (fp4) return BSMMA_DENSE(true, false, false, true);
-    switch (layout) {
-      case BSMMA_NT: return BSMMA_DENSE(false, false, false, true);
-      case BSMMA_NN: return BSMMA_DENSE(false, false, true, true);
-      default:       return BSMMA_DENSE(false, true, true, true);
-    }
-  }
-  if (fp4) return BSMMA_DENSE(true, false, false, false);
+#define BSMMA_DENSE(F, A, B)                                                     \
+  (epi ? launch_dense<F, A, B, true>(ta, tb, tsa, tsb, p, sms, stream)           \
+       : launch_dense<F, A, B, false>(ta, tb, tsa, tsb, p, sms, stream))
+  if (fp4) return BSMMA_DENSE(true, false, false);
   switch (layout) {
-    case BSMMA_NT: return BSMMA_DENSE(false, false, false, false);
-    case BSMMA_NN: return BSMMA_DENSE(false, false, true, false);
-    default:       return BSMMA_DENSE(false, true, true, false);
+    case BSMMA_NT: return BSMMA_DENSE(false, false, false);
+    case BSMMA_NN: return BSMMA_DENSE(false, false, true);
+    default:       return BSMMA_DENSE(false, true, true);
   }
 #undef BSMMA_DENSE
 }

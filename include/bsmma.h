@@ -82,10 +82,16 @@ typedef enum { BSMMA_SCALES_A = 0, BSMMA_SCALES_B = 1 } bsmma_scale_role;
  * M == 0 or N == 0 is a no-op; K == 0 writes D = 0.
  *
  * The scales are first rearranged (mx_scale_relayout, both roles in one launch) into
- * a library-owned device workspace kept per (device, stream), which grows when needed: growing
- * synchronises `stream` once, and returns BSMMA_ERR_WORKSPACE if the stream is
- * being captured (call bsmma_reserve_workspace before capture).  Calls on the
- * same stream are ordered; calls on different streams use different workspaces.
+ * a library-owned device workspace kept per (device, stream), which grows when needed.
+ * Growing returns BSMMA_ERR_WORKSPACE if the stream is being captured (call
+ * bsmma_reserve_workspace before capture).  Otherwise it allocates a larger buffer
+ * and, if no CUDA graph captured a call that used the old buffer, synchronises
+ * `stream` once and frees the old one; a buffer that a captured graph uses is kept
+ * until the process exits, so replaying that graph stays valid after growth.  Calls
+ * on the same stream are ordered; calls on different streams use different
+ * workspaces.  The workspace is keyed by the stream handle: let a stream's pending
+ * mx_gemm work finish before destroying the stream, since a stream created later
+ * may get the same handle and with it the same workspace.
  * Two kernel launches per call (relayout, GEMM).
  */
 bsmma_status mx_gemm(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
@@ -125,7 +131,9 @@ bsmma_status mx_gemm_tiled(const void* A, const uint8_t* sA_tiled, const void* B
  * (cudaGetSymbolAddress) and caches it; make that first call before any stream
  * capture.  All calls on a device share the one array and overwrite it completely,
  * so calls that can overlap on the GPU (different streams without ordering between
- * them) race with each other; order them on one stream.
+ * them) race with each other; order them on one stream.  It never runs the
+ * autotuner's timing runs (they create events and synchronise): with tuning enabled
+ * it takes the stored choice for the shape class, else the SM-pair kernel.
  */
 #define BSMMA_NOALLOC_SCRATCH_BYTES (16ll << 20)
 bsmma_status mx_gemm_noalloc(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
@@ -156,7 +164,11 @@ bsmma_status grouped_fp8_gemm(const uint8_t* A, const float* sA, const uint8_t* 
 /*
  * mx_scale_relayout -- rearranges plain E8M0 scales s_plain [rows][kblocks] into the
  * tiled layout the GEMM kernels copy into tensor memory (128 lanes x 32 bytes per
- * copy).  Byte (lane l, column c, byte b) of a block sits at
+ * copy).  Source: "[gfx1250] Add MXFP4 GEMM support to FlyDSL backend", Description
+ * (the GEMM takes plain scales and rearranges them into the hardware's preferred
+ * order inside the backend; a caller that keeps static weight scales can do it once,
+ * here, and call mx_gemm_tiled).  The target layout is this library's own, made for
+ * the sm_103a tensor-memory copy; the pages fix only that plain scales go in.  Byte (lane l, column c, byte b) of a block sits at
  * (l/8)*256 + (c/4)*128 + (l%8)*16 + (c%4)*4 + b.
  *   role BSMMA_SCALES_A: one 4096-byte chunk per 128 rows and 8 K-blocks, chunk
  *     (rb, kq) at (rb*KQ + kq)*4096, RB = 2*ceil(rows/256) row blocks,
@@ -172,7 +184,9 @@ bsmma_status grouped_fp8_gemm(const uint8_t* A, const float* sA, const uint8_t* 
 bsmma_status mx_scale_relayout(const uint8_t* s_plain, int64_t rows, int64_t kblocks,
                                bsmma_scale_role role, uint8_t* s_tiled, bsmma_stream stream);
 
-/* Size in bytes of the tiled layout of [rows][kblocks] scales of the given role. */
+/* Size in bytes of the tiled layout of [rows][kblocks] scales of the given role
+ * (the buffer mx_scale_relayout fills; same source as mx_scale_relayout).  Returns 0
+ * for an unknown role or an empty tensor. */
 int64_t mx_scale_tiled_bytes(int64_t rows, int64_t kblocks, bsmma_scale_role role);
 
 /* Activation of the fused epilogue (mx_gemm_bias_act). */
@@ -214,7 +228,7 @@ bsmma_status mx_gemm_tiled_bias_act(const void* A, const uint8_t* sA_tiled, cons
  * graph capture.
  *   Shape classes and candidates: grouped_fp8_gemm per (nextPow2(total_M), N, K, G),
  *   tile widths 256 and 128 (when N % 256 == 0); the dense GEMMs per (nextPow2(M), N, K,
- *   layout, a_fmt, b_fmt), the SM-pair, CTA-pair and single-CTA kernels (3, 2, 1).
+ *   layout, a_fmt, b_fmt), the SM-pair and single-CTA kernels (3, 1).
  *   The first call of a new class on a non-capturing stream runs each candidate twice
  *   and waits for it (it synchronises that stream); later calls, and calls in any
  *   process that reads the same cache file, use the stored choice.  A variant or width
@@ -292,7 +306,9 @@ bsmma_status fp8_block_quantize(const void* w, bsmma_dtype w_dtype, int64_t G, i
                                 int64_t K, uint8_t* codes, float* scales, bsmma_stream stream);
 
 /* Grows the current (device, stream) scale workspace to at least `bytes`
- * (call before capturing mx_gemm into a CUDA graph). */
+ * (call before capturing mx_gemm into a CUDA graph).  The stream argument is this
+ * library's addition to the boundary: workspaces are kept per stream, so the one
+ * that a later capture on `stream` will use is the one reserved. */
 bsmma_status bsmma_reserve_workspace(int64_t bytes, bsmma_stream stream);
 
 /* Synchronises `stream`, then returns and clears the current device's latched
@@ -303,10 +319,10 @@ bsmma_status bsmma_device_status(bsmma_stream stream);
 bsmma_status bsmma_set_wait_limit_ns(int64_t ns);
 
 /* Selects the dense kernel variant for later mx_gemm / mx_gemm_tiled calls:
- * 0 automatic (default: SM-pair MMAs), 1 one CTA per 128x256 tile, 2 CTA pairs (2-CTA
- * clusters computing two vertically adjacent tiles that share one multicast B tile),
- * 3 SM-pair MMAs (2-CTA clusters issuing one 256x256 MMA over both SMs).  All
- * variants compute the same result; this is a tuning and testing control. */
+ * 0 automatic (default: SM-pair MMAs), 1 one CTA per 128x256 tile, 3 SM-pair MMAs
+ * (2-CTA clusters issuing one 256x256 MMA over both SMs); any other value returns
+ * BSMMA_ERR_INVALID_ARG.  Both variants compute the same result; this is a tuning and
+ * testing control. */
 bsmma_status bsmma_set_dense_variant(int variant);
 
 /* Selects the grouped kernel's tile width for later grouped_fp8_gemm calls: 0

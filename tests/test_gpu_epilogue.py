@@ -22,7 +22,7 @@ def _lib():
     torch.cuda.init()
 
 
-@pytest.fixture(params=[1, 2, 3], ids=["single", "cta_pair", "sm_pair"])
+@pytest.fixture(params=[1, 3], ids=["single", "sm_pair"])
 def variant(request):
     bs.set_dense_variant(request.param)
     yield request.param

@@ -1,8 +1,9 @@
-"""CUDA-graph capture of every entry point that runs on the device, and concurrent streams.
-Each call is captured once, then replayed after new inputs (and, for the grouped calls, a
-different m_sizes split of the same total_M) have been copied into the captured buffers.
-Every replay is compared with the oracle on the new inputs, so nothing may have been read
-on the host or baked into the graph at capture time."""
+"""CUDA-graph capture of mx_gemm, grouped_fp8_gemm and the three quantisers, and
+concurrent streams.  Each call is captured once, then replayed after new inputs (and, for
+the grouped calls, a different m_sizes split of the same total_M) have been copied into the
+captured buffers.  Every replay is compared with the oracle on the new inputs, so nothing
+may have been read on the host or baked into the graph at capture time.  A captured
+mx_gemm is also replayed after a larger uncaptured call has grown its stream's workspace."""
 import numpy as np
 import pytest
 import torch
@@ -68,6 +69,40 @@ def test_mx_gemm_replays_with_new_operands():
         assert bs.device_status() == 0
         ref = oracle.mx_gemm(c["A"], c["sA"], c["B"], c["sB"], M, N, K, "NT", "e4m3", "e5m2")
         assert_close(D.float().cpu().numpy(), ref, "mx_gemm replay")
+
+
+def test_mx_gemm_replay_after_workspace_growth():
+    """A graph keeps the workspace address it was captured with.  A later, larger call on
+    the same stream grows the workspace; the captured buffer must stay allocated, so the
+    replay still computes the right result."""
+    s = torch.cuda.Stream()          # a stream of its own: its workspace starts empty
+    M, N, K = 256, 384, 256
+    c1 = synthetic.mx_operands((94, 1), M, N, K, "NT", "e4m3", "e4m3")
+    c2 = synthetic.mx_operands((94, 2), M, N, K, "NT", "e4m3", "e4m3")
+    ops = [to_dev(c1[k]) for k in ("A", "sA", "B", "sB")]
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        bs.mx_gemm(*ops, "NT", out=D)        # sizes the workspace for this shape only
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        bs.mx_gemm(*ops, "NT", out=D)
+    big = synthetic.mx_operands((94, 3), 2048, 2048, 2048, "NT", "e4m3", "e4m3")
+    big_ops = [to_dev(big[k]) for k in ("A", "sA", "B", "sB")]
+    with torch.cuda.stream(s):
+        Dbig = bs.mx_gemm(*big_ops, "NT")    # grows the stream's workspace
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 700, 2047])
+    ref = oracle.mx_gemm(big["A"], big["sA"], big["B"], big["sB"], 2048, 2048, 2048, "NT", rows=rows)
+    assert_close(Dbig.float().cpu().numpy()[rows], ref, "large call after capture")
+    for c in (c2, c1):
+        refill(ops, [c[k] for k in ("A", "sA", "B", "sB")])
+        g.replay()
+        torch.cuda.synchronize()
+        assert bs.device_status() == 0
+        ref = oracle.mx_gemm(c["A"], c["sA"], c["B"], c["sB"], M, N, K, "NT")
+        assert_close(D.float().cpu().numpy(), ref, "replay after workspace growth")
 
 
 def test_grouped_replays_with_new_split():

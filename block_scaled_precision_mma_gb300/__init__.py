@@ -26,7 +26,8 @@ import torch
 
 from .build import LIB_PATH, build
 
-__all__ = ["mx_gemm", "mx_gemm_tiled", "mx_gemm_noalloc", "grouped_fp8_gemm", "mx_scale_relayout",
+__all__ = ["mx_gemm", "mx_gemm_tiled", "mx_gemm_noalloc", "grouped_fp8_gemm", "grouped_fp8_pack_weights",
+           "mx_scale_relayout",
            "mx_quantize", "fp8_group_quantize", "fp8_block_quantize", "autotune_configure",
            "autotune_lookup",
            "mx_scale_tiled_bytes", "device_status", "reserve_workspace", "set_wait_limit_ns",
@@ -68,6 +69,8 @@ def load(path: str | None = None):
         lib.mx_gemm_tiled.argtypes = [p, p, p, p, p, i64, i64, i64, i32, i32, i32, p]
         lib.mx_gemm_noalloc.argtypes = [p, p, p, p, p, i64, i64, i64, i32, i32, i32, p]
         lib.grouped_fp8_gemm.argtypes = [p, p, p, p, p, p, i64, i32, i64, i64, p]
+        lib.grouped_fp8_gemm_packed.argtypes = [p, p, p, p, p, p, i64, i32, i64, i64, p]
+        lib.grouped_fp8_pack_weights.argtypes = [p, i64, i64, i64, p, p]
         lib.mx_scale_relayout.argtypes = [p, i64, i64, i32, p, p]
         lib.mx_scale_tiled_bytes.argtypes = [i64, i64, i32]
         lib.mx_scale_tiled_bytes.restype = i64
@@ -90,6 +93,7 @@ def load(path: str | None = None):
         lib.fp8_group_quantize.argtypes = [p, i32, i64, i64, p, i32, p, p, p]
         lib.fp8_block_quantize.argtypes = [p, i32, i64, i64, i64, p, p, p]
         for name in ("mx_gemm", "mx_gemm_tiled", "mx_gemm_noalloc", "grouped_fp8_gemm",
+                     "grouped_fp8_gemm_packed", "grouped_fp8_pack_weights",
                      "mx_scale_relayout",
                      "bsmma_reserve_workspace", "bsmma_device_status", "bsmma_set_wait_limit_ns",
                      "bsmma_set_dense_variant", "bsmma_set_grouped_tile_width",
@@ -181,11 +185,23 @@ def mx_gemm_tiled(A, sA_tiled, B, sB_tiled, layout="NT", a_fmt="e4m3", b_fmt="e4
                    tiled=True, bias=bias, act=act)
 
 
-def grouped_fp8_gemm(X, sX, W, sW, m_sizes, out=None, stream=None):
+def grouped_fp8_pack_weights(W, out=None, stream=None):
+    """W [G, N, K] E4M3 codes -> the packed layout of ``grouped_fp8_gemm(..., packed=True)``
+    (same shape and size; see ``grouped_fp8_pack_weights`` in bsmma.h)."""
+    G, N, K = W.shape
+    if out is None:
+        out = torch.empty_like(W)
+    _check(load().grouped_fp8_pack_weights(_ptr(W), G, N, K, _ptr(out), _stream(stream)),
+           "grouped_fp8_pack_weights")
+    return out
+
+
+def grouped_fp8_gemm(X, sX, W, sW, m_sizes, out=None, stream=None, packed=False):
     """Grouped groupwise FP8 GEMM (see ``grouped_fp8_gemm`` in bsmma.h).
 
-    X [total_M, K] E4M3 codes, sX float32 per-group block layout, W [G, N, K] E4M3,
-    sW float32 [G, N/128, K/128], m_sizes int64 [G] on the device.
+    X [total_M, K] E4M3 codes, sX float32 per-group block layout, W [G, N, K] E4M3 (or,
+    with ``packed=True``, the output of grouped_fp8_pack_weights), sW float32
+    [G, N/128, K/128], m_sizes int64 [G] on the device.
     """
     total_M, K = X.shape
     G, N, _ = W.shape
@@ -193,10 +209,11 @@ def grouped_fp8_gemm(X, sX, W, sW, m_sizes, out=None, stream=None):
         raise ValueError("m_sizes must be a 1-D int64 tensor of length G")
     if out is None:
         out = torch.empty((total_M, N), dtype=torch.bfloat16, device=W.device)
-    _check(load().grouped_fp8_gemm(_ptr(X) if total_M else None, _ptr(sX) if total_M else None,
-                                   _ptr(W), _ptr(sW), _ptr(out) if total_M else None,
-                                   _ptr(m_sizes), total_M, G, N, K, _stream(stream)),
-           "grouped_fp8_gemm")
+    fn = load().grouped_fp8_gemm_packed if packed else load().grouped_fp8_gemm
+    _check(fn(_ptr(X) if total_M else None, _ptr(sX) if total_M else None,
+              _ptr(W), _ptr(sW), _ptr(out) if total_M else None,
+              _ptr(m_sizes), total_M, G, N, K, _stream(stream)),
+           "grouped_fp8_gemm_packed" if packed else "grouped_fp8_gemm")
     return out
 
 

@@ -351,9 +351,10 @@ bsmma_status mx_gemm_bias_act(const void* A, const uint8_t* sA, const void* B, c
                         static_cast<int>(act));
 }
 
-bsmma_status grouped_fp8_gemm(const uint8_t* A, const float* sA, const uint8_t* B,
-                              const float* sB, void* D, const int64_t* m_sizes, int64_t total_M,
-                              int G, int64_t N, int64_t K, bsmma_stream stream) {
+namespace {
+bsmma_status check_grouped(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                           const void* D, const int64_t* m_sizes, int64_t total_M, int G,
+                           int64_t N, int64_t K) {
   if (G < 1 || G > 64 || total_M < 0 || N <= 0 || K <= 0) return BSMMA_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % 128 != 0) return BSMMA_ERR_INVALID_ARG;
   if (!B || !sB || !m_sizes) return BSMMA_ERR_INVALID_ARG;
@@ -363,8 +364,37 @@ bsmma_status grouped_fp8_gemm(const uint8_t* A, const float* sA, const uint8_t* 
     return BSMMA_ERR_MISALIGNED;
   if (total_M >= INT32_MAX || static_cast<int64_t>(G) * N >= INT32_MAX || K > kMaxStride)
     return BSMMA_ERR_INVALID_ARG;
+  return BSMMA_OK;
+}
+}  // namespace
+
+bsmma_status grouped_fp8_gemm(const uint8_t* A, const float* sA, const uint8_t* B,
+                              const float* sB, void* D, const int64_t* m_sizes, int64_t total_M,
+                              int G, int64_t N, int64_t K, bsmma_stream stream) {
+  const bsmma_status st = check_grouped(A, sA, B, sB, D, m_sizes, total_M, G, N, K);
+  if (st != BSMMA_OK) return st;
   return launch_grouped(A, sA, B, sB, D, m_sizes, total_M, G, N, K,
                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+bsmma_status grouped_fp8_gemm_packed(const uint8_t* A, const float* sA, const uint8_t* B_packed,
+                                     const float* sB, void* D, const int64_t* m_sizes,
+                                     int64_t total_M, int G, int64_t N, int64_t K,
+                                     bsmma_stream stream) {
+  const bsmma_status st = check_grouped(A, sA, B_packed, sB, D, m_sizes, total_M, G, N, K);
+  if (st != BSMMA_OK) return st;
+  return launch_grouped(A, sA, B_packed, sB, D, m_sizes, total_M, G, N, K,
+                        reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+bsmma_status grouped_fp8_pack_weights(const uint8_t* W, int64_t G, int64_t N, int64_t K,
+                                      uint8_t* W_packed, bsmma_stream stream) {
+  if (G < 0 || N < 0 || K < 0 || N % 128 != 0 || K % 128 != 0) return BSMMA_ERR_INVALID_ARG;
+  if (G == 0 || N == 0 || K == 0) return BSMMA_OK;
+  if (!W || !W_packed) return BSMMA_ERR_INVALID_ARG;
+  if (!aligned16(W) || !aligned16(W_packed)) return BSMMA_ERR_MISALIGNED;
+  if (W == W_packed) return BSMMA_ERR_INVALID_ARG;   // not in place
+  return launch_pack_weights(W, G, N, K, W_packed, reinterpret_cast<cudaStream_t>(stream));
 }
 
 bsmma_status mx_quantize(const void* x, bsmma_dtype x_dtype, int64_t rows, int64_t cols,

@@ -62,6 +62,7 @@ struct GCfg {
 struct GroupedParams {
   const float* sX;
   const float* sW;
+  const uint8_t* Wp;    // packed weights (grouped_fp8_pack_weights layout), or null
   __nv_bfloat16* D;
   const int64_t* m_sizes;
   int64_t total_M, N;
@@ -105,7 +106,10 @@ __device__ __forceinline__ int find_group(const GroupTable& gt, int G, int mt) {
 // 12 warps (three warpgroups) share an SM's four register-file quarters (16384
 // registers each) three to a quarter, so a thread launches with at most
 // 16384 / (3 * 32) = 170 registers (168 allocated); the warpgroups then rebalance.
-template <int BN>
+// PACKED: W comes from the packed layout, one contiguous bulk copy per stage (the
+// weight tile is stored exactly as the 128-byte-swizzled shared-memory image the MMA
+// reads); otherwise a 2-D tensor copy from W [G*N][K].
+template <int BN, bool PACKED>
 __global__ void __launch_bounds__(384, 1)
     grouped_fp8_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                        const GroupedParams p) {
@@ -204,7 +208,13 @@ __global__ void __launch_bounds__(384, 1)
             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
             uint8_t* dst = ring + stage * kStageBytes;
             tma_load_2d(&tmX, &full[stage], dst, kb * kBK, row0);
-            tma_load_2d(&tmW, &full[stage], dst + kATileBytes, kb * kBK, wrow0);
+            if constexpr (PACKED)
+              bulk_load(dst + kATileBytes,
+                        p.Wp + ((static_cast<int64_t>(g) * KB + kb) * (p.N / 128) + nt * (BN / 128)) *
+                                   (128 * kBK),
+                        C::kBTileBytes, &full[stage]);
+            else
+              tma_load_2d(&tmW, &full[stage], dst + kATileBytes, kb * kBK, wrow0);
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1;
@@ -400,7 +410,7 @@ __global__ void __launch_bounds__(384, 1)
   named_barrier_sync(1, C::kThreads);
 }
 
-template <int BN>
+template <int BN, bool PACKED>
 bsmma_status launch_grouped_bn(const CUtensorMap& tx, const CUtensorMap& tw, GroupedParams p,
                                int64_t total_M, int G, int sm_count, cudaStream_t stream) {
   using C = GCfg<BN>;
@@ -411,12 +421,12 @@ bsmma_status launch_grouped_bn(const CUtensorMap& tx, const CUtensorMap& tw, Gro
   if (grid < 1) grid = 1;
   static bool attr_set = false;   // benign race: setting the attribute twice is harmless
   if (!attr_set) {
-    if (cudaFuncSetAttribute(grouped_fp8_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(grouped_fp8_kernel<BN, PACKED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return BSMMA_ERR_CUDA;
     attr_set = true;
   }
-  grouped_fp8_kernel<BN><<<static_cast<int>(grid), C::kThreads, C::kSmemBytes, stream>>>(tx, tw, p);
+  grouped_fp8_kernel<BN, PACKED><<<static_cast<int>(grid), C::kThreads, C::kSmemBytes, stream>>>(tx, tw, p);
   count_launches(1);
   return cuda_ok(cudaGetLastError());
 }
@@ -426,13 +436,47 @@ bsmma_status launch_grouped_bn(const CUtensorMap& tx, const CUtensorMap& tw, Gro
 namespace {
 bsmma_status launch_grouped_width(const uint8_t* X, const float* sX, const uint8_t* W,
                                   const float* sW, void* D, const int64_t* m_sizes, int64_t total_M,
-                                  int G, int64_t N, int64_t K, int bn, const DeviceInfo* dev,
-                                  cudaStream_t stream);
+                                  int G, int64_t N, int64_t K, int bn, bool packed,
+                                  const DeviceInfo* dev, cudaStream_t stream);
+
+// Packed weight layout: for group g, 128-K block kb and 128-row block nb of W, one
+// 16 KB block at ((g*KB + kb)*NB + nb) * 16384 holding rows nb*128 .. nb*128+127, 128
+// bytes of K each, with the 16-byte pieces of row r stored in the order that the
+// 128-byte swizzle of a shared-memory tile uses (piece c at position c ^ (r % 8)).  Two
+// neighbouring 128-row blocks of one K block are contiguous, so a 128- or 256-row tile
+// is one contiguous copy whose bytes land in shared memory exactly as the MMA reads them.
+__global__ void pack_weights_kernel(const uint4* __restrict__ W, uint4* __restrict__ Wp, int64_t G,
+                                    int64_t N, int64_t K) {
+  const int64_t pieces_per_row = K / 16;
+  const int64_t total = G * N * pieces_per_row;
+  const int64_t KB = K / 128, NB = N / 128;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = i / pieces_per_row;          // g*N + n
+    const int64_t piece = i - row * pieces_per_row;  // 16-byte piece of the row
+    const int64_t g = row / N, n = row - g * N;
+    const int64_t kb = piece / 8, c = piece % 8;
+    const int64_t nb = n / 128, r = n % 128;
+    const int64_t dst = ((g * KB + kb) * NB + nb) * 1024 + r * 8 + (c ^ (r % 8));
+    Wp[dst] = W[i];
+  }
+}
 }  // namespace
+
+bsmma_status launch_pack_weights(const uint8_t* W, int64_t G, int64_t N, int64_t K, uint8_t* Wp,
+                                 cudaStream_t stream) {
+  bsmma_status st;
+  const DeviceInfo* dev = current_device(&st);
+  if (!dev) return st;
+  pack_weights_kernel<<<dev->sm_count * 8, 256, 0, stream>>>(
+      reinterpret_cast<const uint4*>(W), reinterpret_cast<uint4*>(Wp), G, N, K);
+  count_launches(1);
+  return cuda_ok(cudaGetLastError());
+}
 
 bsmma_status launch_grouped(const uint8_t* X, const float* sX, const uint8_t* W, const float* sW,
                             void* D, const int64_t* m_sizes, int64_t total_M, int G, int64_t N,
-                            int64_t K, cudaStream_t stream) {
+                            int64_t K, cudaStream_t stream, bool packed) {
   bsmma_status st;
   const DeviceInfo* dev = current_device(&st);
   if (!dev) return st;
@@ -449,20 +493,22 @@ bsmma_status launch_grouped(const uint8_t* X, const float* sX, const uint8_t* W,
   int bn = (wide || force_wide) ? 256 : 128;
   if (grouped_tile_width() == 0 && N % 256 == 0) {
     // opt-in autotuning per (nextPow2(total_M), N, K, G)
-    const std::string key = "grouped " + std::to_string(next_pow2(total_M)) + " " +
-                            std::to_string(N) + " " + std::to_string(K) + " " + std::to_string(G);
+    const std::string key = std::string(packed ? "grouped_packed " : "grouped ") +
+                            std::to_string(next_pow2(total_M)) + " " + std::to_string(N) + " " +
+                            std::to_string(K) + " " + std::to_string(G);
     bn = autotune_pick(key, {256, 128}, bn, stream, [&](int c) {
-      return launch_grouped_width(X, sX, W, sW, D, m_sizes, total_M, G, N, K, c, dev, stream);
+      return launch_grouped_width(X, sX, W, sW, D, m_sizes, total_M, G, N, K, c, packed, dev,
+                                  stream);
     });
   }
-  return launch_grouped_width(X, sX, W, sW, D, m_sizes, total_M, G, N, K, bn, dev, stream);
+  return launch_grouped_width(X, sX, W, sW, D, m_sizes, total_M, G, N, K, bn, packed, dev, stream);
 }
 
 namespace {
 bsmma_status launch_grouped_width(const uint8_t* X, const float* sX, const uint8_t* W,
                                   const float* sW, void* D, const int64_t* m_sizes, int64_t total_M,
-                                  int G, int64_t N, int64_t K, int bn, const DeviceInfo* dev,
-                                  cudaStream_t stream) {
+                                  int G, int64_t N, int64_t K, int bn, bool packed,
+                                  const DeviceInfo* dev, cudaStream_t stream) {
   bsmma_status st;
   CUtensorMap tx, tw;
   // With no rows there is no X tile to load; W's address stands in for the map.
@@ -474,6 +520,7 @@ bsmma_status launch_grouped_width(const uint8_t* X, const float* sX, const uint8
   GroupedParams p;
   p.sX = sX;
   p.sW = sW;
+  p.Wp = packed ? W : nullptr;
   p.D = static_cast<__nv_bfloat16*>(D);
   p.m_sizes = m_sizes;
   p.total_M = total_M;
@@ -482,8 +529,12 @@ bsmma_status launch_grouped_width(const uint8_t* X, const float* sX, const uint8
   p.num_kb = static_cast<int>(K / kBK);
   p.status = dev->status;
   p.limit_ns = wait_limit_ns();
-  if (bn == 256) return launch_grouped_bn<256>(tx, tw, p, total_M, G, dev->sm_count, stream);
-  return launch_grouped_bn<128>(tx, tw, p, total_M, G, dev->sm_count, stream);
+  if (packed) {
+    if (bn == 256) return launch_grouped_bn<256, true>(tx, tw, p, total_M, G, dev->sm_count, stream);
+    return launch_grouped_bn<128, true>(tx, tw, p, total_M, G, dev->sm_count, stream);
+  }
+  if (bn == 256) return launch_grouped_bn<256, false>(tx, tw, p, total_M, G, dev->sm_count, stream);
+  return launch_grouped_bn<128, false>(tx, tw, p, total_M, G, dev->sm_count, stream);
 }
 }  // namespace
 

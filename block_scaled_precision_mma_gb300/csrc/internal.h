@@ -62,9 +62,12 @@ bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B
                                 const uint8_t* sfb, void* D, int64_t M, int64_t N, int64_t K,
                                 bsmma_layout layout, bsmma_fmt a_fmt, bsmma_fmt b_fmt,
                                 cudaStream_t stream, const void* bias = nullptr, int act = 0);
+// packed: W is in the grouped_fp8_pack_weights layout.
 bsmma_status launch_grouped(const uint8_t* X, const float* sX, const uint8_t* W, const float* sW,
                             void* D, const int64_t* m_sizes, int64_t total_M, int G, int64_t N,
-                            int64_t K, cudaStream_t stream);
+                            int64_t K, cudaStream_t stream, bool packed = false);
+bsmma_status launch_pack_weights(const uint8_t* W, int64_t G, int64_t N, int64_t K, uint8_t* Wp,
+                                 cudaStream_t stream);
 
 // Quantisers (arguments already validated by the entry points).
 bsmma_status launch_mx_quantize(const void* x, bool f32, int64_t rows, int64_t cols, bsmma_fmt fmt,

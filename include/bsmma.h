@@ -162,6 +162,30 @@ bsmma_status grouped_fp8_gemm(const uint8_t* A, const float* sA, const uint8_t* 
                               int G, int64_t N, int64_t K, bsmma_stream stream);
 
 /*
+ * grouped_fp8_pack_weights / grouped_fp8_gemm_packed -- the grouped GEMM with weights
+ * rearranged once ahead of time, as the pages' preshuffled sibling op rearranges its
+ * weights at load time ("Add FlyDSL grouped groupwise FP8 GEMM for ROCm", introduction
+ * and Performance: the _preshuffle variant).  The layout is this library's own, made
+ * for sm_103a: each 128-row x 128-K tile of W is one contiguous 16 KB block that holds
+ * the tile exactly as the MMA reads it from shared memory, so a kernel stage loads its
+ * weight tile with one bulk copy.
+ *   grouped_fp8_pack_weights: W [G][N][K] E4M3 codes -> W_packed, G*N*K bytes, where
+ *     the tile (g, 128-K block kb, 128-row block nb) starts at byte
+ *     ((g*(K/128) + kb)*(N/128) + nb) * 16384, row r of the tile (W row nb*128 + r) at
+ *     r*128 bytes into it, and the 16-byte piece c of that row (K offsets kb*128 + 16c ..
+ *     +15) at position c ^ (r % 8) of the row.  Not in place (W != W_packed).  One launch.
+ *   grouped_fp8_gemm_packed: grouped_fp8_gemm with B = W_packed; every other argument,
+ *     the result, preconditions and errors as for grouped_fp8_gemm.
+ * Preconditions: N % 128 == 0, K % 128 == 0, G >= 0, 16-byte-aligned W and W_packed.
+ */
+bsmma_status grouped_fp8_pack_weights(const uint8_t* W, int64_t G, int64_t N, int64_t K,
+                                      uint8_t* W_packed, bsmma_stream stream);
+bsmma_status grouped_fp8_gemm_packed(const uint8_t* A, const float* sA, const uint8_t* B_packed,
+                                     const float* sB, void* D, const int64_t* m_sizes,
+                                     int64_t total_M, int G, int64_t N, int64_t K,
+                                     bsmma_stream stream);
+
+/*
  * mx_scale_relayout -- rearranges plain E8M0 scales s_plain [rows][kblocks] into the
  * tiled layout the GEMM kernels copy into tensor memory (128 lanes x 32 bytes per
  * copy).  Source: "[gfx1250] Add MXFP4 GEMM support to FlyDSL backend", Description

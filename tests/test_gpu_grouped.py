@@ -22,21 +22,31 @@ def _lib():
     torch.cuda.init()
 
 
-@pytest.fixture(params=[128, 256], ids=["bn128", "bn256"])
+PACKED = False   # run_grouped packs W and calls the packed entry point
+
+
+@pytest.fixture(params=[(128, False), (256, False), (128, True), (256, True)],
+                ids=["bn128", "bn256", "bn128_packed", "bn256_packed"])
 def gwidth(request):
-    """Runs the test with 128- and 256-column grouped tiles."""
-    bs.set_grouped_tile_width(request.param)
-    yield request.param
+    """Runs the test with 128- and 256-column grouped tiles, on plain and on packed
+    weights."""
+    global PACKED
+    width, PACKED = request.param
+    bs.set_grouped_tile_width(width)
+    yield width
     bs.set_grouped_tile_width(0)
+    PACKED = False
 
 
 def run_grouped(c, guard=True):
     ms = np.asarray(c["m_sizes"], dtype=np.int64)
     T, N = int(ms.sum()), c["N"]
     X, sX, W, sW, m = (to_dev(c[k]) for k in ("X", "sX", "W", "sW", "m_sizes"))
+    if PACKED:
+        W = bs.grouped_fp8_pack_weights(W)
     buf, out = guarded_out(max(T, 1), N)
     out = out[:T] if T else None
-    D = bs.grouped_fp8_gemm(X, sX, W, sW, m, out=out)
+    D = bs.grouped_fp8_gemm(X, sX, W, sW, m, out=out, packed=PACKED)
     torch.cuda.synchronize()
     st = bs.device_status()
     assert st == 0, bs.status_string(st)
@@ -101,6 +111,36 @@ def test_grouped_deterministic():
     ms = synthetic.gen_m_sizes(1024, 1)
     c = synthetic.grouped_operands((40, 78), ms, 512, 768)
     assert np.array_equal(run_grouped(c), run_grouped(c))
+
+
+def packed_layout(W):
+    """The packed weight layout written out from its definition: tile (g, kb, nb) at
+    ((g*KB + kb)*NB + nb)*16384, row r at r*128, 16-byte piece c at position c ^ (r % 8)."""
+    G, N, K = W.shape
+    KB, NB = K // 128, N // 128
+    t = W.reshape(G, NB, 128, KB, 8, 16)                  # g, nb, r, kb, c, byte
+    out = np.empty((G, KB, NB, 128, 8, 16), dtype=np.uint8)
+    for r in range(128):
+        perm = np.arange(8) ^ (r % 8)                    # piece c goes to position perm[c]
+        dst = np.empty((G, KB, NB, 8, 16), dtype=np.uint8)
+        dst[:, :, :, perm, :] = t[:, :, r, :, :, :].transpose(0, 2, 1, 3, 4)
+        out[:, :, :, r] = dst
+    return out.reshape(-1)
+
+
+def test_pack_weights_layout():
+    rng = np.random.default_rng(42)
+    W = rng.integers(0, 256, size=(3, 384, 640), dtype=np.uint8)
+    got = bs.grouped_fp8_pack_weights(to_dev(W))
+    torch.cuda.synchronize()
+    assert bs.device_status() == 0
+    assert np.array_equal(got.cpu().numpy().reshape(-1), packed_layout(W))
+
+
+def test_pack_weights_rejects_in_place():
+    W = torch.zeros((1, 128, 128), dtype=torch.uint8, device="cuda")
+    with pytest.raises(bs.BsmmaError):
+        bs.grouped_fp8_pack_weights(W, out=W)
 
 
 def test_grouped_empty_total():

@@ -40,11 +40,11 @@ __device__ __forceinline__ float gelu_erf(float x) {
 // quotient is 0, the limit.
 __device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 
-// Eight accumulator values (FP32 bits) of columns col .. col+7 of one row -> out[0..7].
-// The bias is read with one 16-byte load (every lane of a warp reads the same columns,
-// so the load is a broadcast).
-__device__ __forceinline__ void store8(__nv_bfloat16* out, const uint32_t* r, int64_t col,
-                                       const Epilogue& e) {
+// Eight accumulator values (FP32 bits) of columns col .. col+7 of one row -> eight BF16
+// results packed two per word.  The bias is read with one 16-byte load (every lane of a
+// warp reads the same columns, so the load is a broadcast).
+__device__ __forceinline__ void apply8(const uint32_t* r, int64_t col, const Epilogue& e,
+                                       uint32_t (&o)[4]) {
   float v[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[j]);
@@ -67,8 +67,18 @@ __device__ __forceinline__ void store8(__nv_bfloat16* out, const uint32_t* r, in
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = silu(v[j]);
   }
-  st_global_v4_cs(out, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                  pack_bf16x2(v[6], v[7]));
+  o[0] = pack_bf16x2(v[0], v[1]);
+  o[1] = pack_bf16x2(v[2], v[3]);
+  o[2] = pack_bf16x2(v[4], v[5]);
+  o[3] = pack_bf16x2(v[6], v[7]);
+}
+
+// Same, stored to out[0..7] with one streaming 16-byte store.
+__device__ __forceinline__ void store8(__nv_bfloat16* out, const uint32_t* r, int64_t col,
+                                       const Epilogue& e) {
+  uint32_t o[4];
+  apply8(r, col, e, o);
+  st_global_v4_cs(out, o[0], o[1], o[2], o[3]);
 }
 
 }  // namespace bsmma

@@ -12,8 +12,12 @@
 //                       leader CTA's stage barrier;
 //   leader,    warp 1   lane 0 copies the scales into both CTAs' tensor memory and
 //                       issues the pair MMAs; commits release the stage in both CTAs;
-//   both CTAs, warps 2-9  epilogue of the CTA's 128 accumulator rows, then an arrive on
-//                       the leader's accumulator barrier.
+//   both CTAs, warps 2-9  epilogue of the CTA's 128 accumulator rows: tensor memory ->
+//                       registers, an arrive on the leader's accumulator barrier (the next
+//                       unit's MMAs may start), then (FP8) BF16 pieces of 32 rows x 32
+//                       columns through a 2 KB shared-memory buffer per warp to TMA
+//                       tensor stores, or (FP4, whose five stages leave no room for the
+//                       buffers) 16-byte stores from registers.
 // Every wait is bounded; on a timeout each role unwinds to the common teardown.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -44,9 +48,12 @@ struct Cfg2 {
   static constexpr int kSfbBytes = kKgPerStage * kSfbRepl * 1024;
   static constexpr int kChunkBytes = 4096;                // row-scale chunk, in the stage that loads it
   static constexpr int kStageBytes = kABytes + kBBytes + kSfbBytes + kChunkBytes;
-  static constexpr int kStages0 = (kSmemLimit - 2048) / kStageBytes;
+  // output staging: 2 KB (32 x 32 BF16) per epilogue warp, when it leaves five stages
+  static constexpr bool kStaged = !FP4;
+  static constexpr int kOutBytes = kStaged ? 8 * 2048 : 0;
+  static constexpr int kStages0 = (kSmemLimit - 2048 - kOutBytes) / kStageBytes;
   static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kOutBytes + 256;
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
 };
 
@@ -151,7 +158,8 @@ template <bool FP4, bool A_MN, bool B_MN, bool EPI>
 __global__ void __maxnreg__(168)
     mx_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmSFA,
-                       const __grid_constant__ CUtensorMap tmSFB, const Pair2Params p) {
+                       const __grid_constant__ CUtensorMap tmSFB,
+                       const __grid_constant__ CUtensorMap tmD, const Pair2Params p) {
   using C = Cfg2<FP4>;
   constexpr int kSfbRepl = C::kSfbRepl;
   extern __shared__ uint8_t smem_raw[];
@@ -161,7 +169,8 @@ __global__ void __maxnreg__(168)
   uint8_t* sB = sA + C::kStages * C::kABytes;
   uint8_t* sSFB = sB + C::kStages * C::kBBytes;
   uint8_t* sSFA = sSFB + C::kStages * C::kSfbBytes;        // one chunk slot per stage
-  uint64_t* full = reinterpret_cast<uint64_t*>(sSFA + C::kStages * C::kChunkBytes);
+  uint8_t* sOut = sSFA + C::kStages * C::kChunkBytes;       // output staging (FP8)
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + C::kOutBytes);
   uint64_t* empty = full + C::kStages;
   uint64_t* acc_full = empty + C::kStages;
   uint64_t* acc_empty = acc_full + 1;
@@ -187,6 +196,7 @@ __global__ void __maxnreg__(168)
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmSFA);
     prefetch_tmap(&tmSFB);
+    if (C::kStaged) prefetch_tmap(&tmD);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, kTmemCols);
@@ -339,7 +349,49 @@ __global__ void __maxnreg__(168)
       if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
       const int64_t row = static_cast<int64_t>(mt) * 128 + q * 32 + lane;
       const int64_t col0 = static_cast<int64_t>(nt) * 256 + h * kCols;
-      if (row < p.M) {
+      if constexpr (C::kStaged) {
+        // 32 x 32 pieces: lane = row; the piece's 16-byte groups of 8 columns go to the
+        // buffer in the 64-byte swizzle the tensor map names (group v of row r at
+        // position v ^ ((r / 2) % 4)), so the 32 lanes' writes hit distinct banks.
+        const int64_t row0 = static_cast<int64_t>(mt) * 128 + q * 32;
+        uint8_t* stg = sOut + (warp - 2) * 2048;
+        if (row0 < p.M) {
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) {
+            if (col0 + c * 32 >= p.N) break;   // warp-uniform
+            uint32_t o[4][4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int64_t col = col0 + c * 32 + v * 8;
+              if constexpr (EPI) {
+                if (col < p.N) {
+                  apply8(&r[c][v * 8], col, p.epi, o[v]);
+                  continue;
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                o[v][j] = pack_bf16x2(__uint_as_float(r[c][v * 8 + 2 * j]),
+                                      __uint_as_float(r[c][v * 8 + 2 * j + 1]));
+            }
+            if (lane == 0) bulk_wait_group_read<0>();   // the previous piece has been read
+            __syncwarp();
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint32_t a = smem_u32(stg + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16));
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(o[v][0]),
+                           "r"(o[v][1]), "r"(o[v][2]), "r"(o[v][3])
+                           : "memory");
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmD, stg, static_cast<int32_t>(col0 + c * 32), static_cast<int32_t>(row0));
+              bulk_commit_group();
+            }
+          }
+        }
+      } else if (row < p.M) {
         __nv_bfloat16* out = p.D + row * p.N + col0;
 #pragma unroll
         for (int c = 0; c < kChunks; ++c)
@@ -359,6 +411,9 @@ __global__ void __maxnreg__(168)
           }
       }
     }
+    // every tensor store of this warp has finished reading and writing before the
+    // buffers (and the block) go away
+    if (C::kStaged && lane == 0) bulk_wait_group<0>();
   }
   __syncthreads();
   cluster_sync();   // both CTAs are done with tensor memory and with each other's barriers
@@ -372,7 +427,8 @@ __global__ void __maxnreg__(168)
 
 template <bool FP4, bool A_MN, bool B_MN, bool EPI>
 bsmma_status launch_2sm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
-                        const CUtensorMap& tsb, const Pair2Params& p, cudaStream_t stream) {
+                        const CUtensorMap& tsb, const CUtensorMap& td, const Pair2Params& p,
+                        cudaStream_t stream) {
   using C = Cfg2<FP4>;
   auto kern = mx_gemm_2sm_kernel<FP4, A_MN, B_MN, EPI>;
   static int max_clusters = -1;   // benign race: every thread computes the same value
@@ -413,7 +469,7 @@ bsmma_status launch_2sm(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, td, p);
   count_launches(1);
   return cuda_ok(e == cudaSuccess ? cudaGetLastError() : e);
 }
@@ -432,7 +488,9 @@ bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B
   const int64_t kblocks = K / 32;
   const int64_t kq = (kblocks + 7) / 8;                   // row-scale chunks per 128 rows
   const int64_t kgp = 2 * ((kblocks + 7) / 8);            // column-scale blocks per 256 columns
-  CUtensorMap ta, tb, tsa, tsb;
+  CUtensorMap ta, tb, tsa, tsb, td;
+  st = encode_tmap_bf16_out(&td, D, static_cast<uint64_t>(N), static_cast<uint64_t>(M), 32, 32);
+  if (st != BSMMA_OK) return st;
   if (layout == BSMMA_TN) st = encode_tmap_u8(&ta, A, M, K, M, 128, 128);
   else st = encode_tmap_u8(&ta, A, kbytes, M, kbytes, 128, 128);
   if (st != BSMMA_OK) return st;
@@ -465,8 +523,8 @@ bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B
   p.limit_ns = wait_limit_ns();
   const bool epi = bias != nullptr || act != 0;
 #define BSMMA_2SM(F, A, B)                                                       \
-  (epi ? launch_2sm<F, A, B, true>(ta, tb, tsa, tsb, p, stream)                  \
-       : launch_2sm<F, A, B, false>(ta, tb, tsa, tsb, p, stream))
+  (epi ? launch_2sm<F, A, B, true>(ta, tb, tsa, tsb, td, p, stream)              \
+       : launch_2sm<F, A, B, false>(ta, tb, tsa, tsb, td, p, stream))
   if (fp4) return BSMMA_2SM(true, false, false);
   switch (layout) {
     case BSMMA_NT: return BSMMA_2SM(false, false, false);

@@ -49,6 +49,15 @@ struct Workspace {
   bool captured;   // handed to a kernel launch recorded into a CUDA graph
 };
 std::vector<Workspace> g_ws;
+// The dense kernel's split workspace of one (device, stream): a fixed size per device, its
+// arrival counters zero between launches.
+struct SplitWorkspace {
+  int device;
+  cudaStream_t stream;
+  void* ptr;
+  int64_t counter_bytes;
+};
+std::vector<SplitWorkspace> g_sws;
 // Buffers replaced by a larger one after a graph capture used them: a replay of that
 // graph still reads and writes them, so they stay allocated until the process exits.
 std::vector<void*> g_ws_kept;
@@ -222,6 +231,35 @@ bsmma_status get_workspace(int64_t bytes, cudaStream_t stream, void** out) {
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
+
+bsmma_status split_workspace(cudaStream_t stream, float** part, int** arrivals) {
+  bsmma_status st;
+  const DeviceInfo* dev = current_device(&st);
+  if (!dev) return st;
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& e : g_sws)
+    if (e.device == dev->device && e.stream == stream) {
+      *arrivals = static_cast<int*>(e.ptr);
+      *part = reinterpret_cast<float*>(static_cast<uint8_t*>(e.ptr) + e.counter_bytes);
+      return BSMMA_OK;
+    }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return BSMMA_ERR_CUDA;
+  if (cap != cudaStreamCaptureStatusNone) return BSMMA_ERR_WORKSPACE;
+  const int64_t sms = dev->sm_count;
+  const int64_t counter_bytes = align_up(sms * 4, 256);
+  const int64_t bytes = counter_bytes + 2 * sms * 128 * 256 * 4;
+  void* p = nullptr;
+  if (cudaMalloc(&p, static_cast<size_t>(bytes)) != cudaSuccess) return BSMMA_ERR_CUDA;
+  if (cudaMemsetAsync(p, 0, static_cast<size_t>(counter_bytes), stream) != cudaSuccess) {
+    cudaFree(p);
+    return BSMMA_ERR_CUDA;
+  }
+  g_sws.push_back(SplitWorkspace{dev->device, stream, p, counter_bytes});
+  *arrivals = static_cast<int*>(p);
+  *part = reinterpret_cast<float*>(static_cast<uint8_t*>(p) + counter_bytes);
+  return BSMMA_OK;
+}
 
 bsmma_status validate_dense(const void* A, const void* sA, const void* B, const void* sB,
                             const void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
@@ -471,7 +509,11 @@ bsmma_status fp8_block_quantize(const void* w, bsmma_dtype w_dtype, int64_t G, i
 bsmma_status bsmma_reserve_workspace(int64_t bytes, bsmma_stream stream) {
   if (bytes < 0) return BSMMA_ERR_INVALID_ARG;
   void* p = nullptr;
-  return get_workspace(bytes, reinterpret_cast<cudaStream_t>(stream), &p);
+  bsmma_status st = get_workspace(bytes, reinterpret_cast<cudaStream_t>(stream), &p);
+  if (st != BSMMA_OK) return st;
+  float* part = nullptr;
+  int* arrivals = nullptr;
+  return split_workspace(reinterpret_cast<cudaStream_t>(stream), &part, &arrivals);
 }
 
 bsmma_status bsmma_device_status(bsmma_stream stream) {
@@ -484,6 +526,15 @@ bsmma_status bsmma_device_status(bsmma_stream stream) {
   if (cudaMemcpy(&v, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
       cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
     return BSMMA_ERR_CUDA;
+  if (v == BSMMA_DEV_TIMEOUT) {
+    // a dense launch that gave up may have left split-unit arrival counts behind
+    if (cudaDeviceSynchronize() != cudaSuccess) return BSMMA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (auto& e : g_sws)
+      if (e.device == dev->device &&
+          cudaMemset(e.ptr, 0, static_cast<size_t>(e.counter_bytes)) != cudaSuccess)
+        return BSMMA_ERR_CUDA;
+  }
   return static_cast<bsmma_status>(v);
 }
 

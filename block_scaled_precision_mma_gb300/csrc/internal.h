@@ -55,18 +55,25 @@ bsmma_status launch_wide_relayout(const uint8_t* sa, int64_t rows_a, uint8_t* ou
                                   const uint8_t* sb, int64_t rows_b, uint8_t* out_b,
                                   int64_t kblocks, cudaStream_t stream);
 
+// The dense SM-pair kernel's split workspace for (current device, stream): arrival
+// counters [#SMs] (zero between launches) and partial-sum slots [2 * #SMs][128 x 256 FP32].
+// Allocated, its counters zeroed, by the first call on a stream, which must not be
+// captured (BSMMA_ERR_WORKSPACE otherwise); a fixed size per device.
+bsmma_status split_workspace(cudaStream_t stream, float** part, int** arrivals);
+
 // Launchers (arguments already validated by the entry points).
-// bias: BF16 [N] or nullptr; act: bsmma_activation (0 = none).  may_tune: false keeps
-// the dense GEMM off the autotuner's timing runs (it then takes a stored choice, else
-// the SM-pair kernel).
+// bias: BF16 [N] or nullptr; act: bsmma_activation (0 = none).  may_allocate: false keeps
+// the dense GEMM off the autotuner's timing runs (it then takes a stored choice, else the
+// SM-pair kernel) and off the split workspace (units are not split).
 bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, const uint8_t* sfb,
                             void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
                             bsmma_fmt a_fmt, bsmma_fmt b_fmt, cudaStream_t stream,
-                            const void* bias = nullptr, int act = 0, bool may_tune = true);
+                            const void* bias = nullptr, int act = 0, bool may_allocate = true);
 bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B,
                                 const uint8_t* sfb, void* D, int64_t M, int64_t N, int64_t K,
                                 bsmma_layout layout, bsmma_fmt a_fmt, bsmma_fmt b_fmt,
-                                cudaStream_t stream, const void* bias = nullptr, int act = 0);
+                                cudaStream_t stream, const void* bias = nullptr, int act = 0,
+                                bool may_split = true);
 // packed: W is in the grouped_fp8_pack_weights layout.
 bsmma_status launch_grouped(const uint8_t* X, const float* sX, const uint8_t* W, const float* sW,
                             void* D, const int64_t* m_sizes, int64_t total_M, int G, int64_t N,

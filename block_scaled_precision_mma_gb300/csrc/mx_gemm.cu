@@ -368,13 +368,14 @@ namespace {
 bsmma_status launch_mx_gemm_variant(const void* A, const uint8_t* sfa, const void* B,
                                     const uint8_t* sfb, void* D, int64_t M, int64_t N, int64_t K,
                                     bsmma_layout layout, bsmma_fmt a_fmt, bsmma_fmt b_fmt,
-                                    cudaStream_t stream, const void* bias, int act, int variant);
+                                    cudaStream_t stream, const void* bias, int act, int variant,
+                                    bool may_split);
 }  // namespace
 
 bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, const uint8_t* sfb,
                             void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,
                             bsmma_fmt a_fmt, bsmma_fmt b_fmt, cudaStream_t stream,
-                            const void* bias, int act, bool may_tune) {
+                            const void* bias, int act, bool may_allocate) {
   // SM-pair MMAs unless the one-CTA variant is asked for, or (opt-in) tuning per
   // (nextPow2(M), N, K, layout, formats) picks it
   int variant = dense_variant();
@@ -383,10 +384,10 @@ bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, co
                             " " + std::to_string(K) + " " + std::to_string(static_cast<int>(layout)) +
                             " " + std::to_string(static_cast<int>(a_fmt)) + " " +
                             std::to_string(static_cast<int>(b_fmt));
-    if (may_tune) {
+    if (may_allocate) {
       variant = autotune_pick(key, {3, 1}, 3, stream, [&](int v) {
         return launch_mx_gemm_variant(A, sfa, B, sfb, D, M, N, K, layout, a_fmt, b_fmt, stream,
-                                      bias, act, v);
+                                      bias, act, v, true);
       });
     } else {
       const int cached = autotune_cached(key);
@@ -394,16 +395,18 @@ bsmma_status launch_mx_gemm(const void* A, const uint8_t* sfa, const void* B, co
     }
   }
   return launch_mx_gemm_variant(A, sfa, B, sfb, D, M, N, K, layout, a_fmt, b_fmt, stream, bias,
-                                act, variant);
+                                act, variant, may_allocate);
 }
 
 namespace {
 bsmma_status launch_mx_gemm_variant(const void* A, const uint8_t* sfa, const void* B,
                                     const uint8_t* sfb, void* D, int64_t M, int64_t N, int64_t K,
                                     bsmma_layout layout, bsmma_fmt a_fmt, bsmma_fmt b_fmt,
-                                    cudaStream_t stream, const void* bias, int act, int variant) {
+                                    cudaStream_t stream, const void* bias, int act, int variant,
+                                    bool may_split) {
   if (variant == 3)
-    return launch_mx_gemm_2sm(A, sfa, B, sfb, D, M, N, K, layout, a_fmt, b_fmt, stream, bias, act);
+    return launch_mx_gemm_2sm(A, sfa, B, sfb, D, M, N, K, layout, a_fmt, b_fmt, stream, bias, act,
+                              may_split);
   bsmma_status st;
   const DeviceInfo* dev = current_device(&st);
   if (!dev) return st;

@@ -12,6 +12,12 @@
 //                       leader CTA's stage barrier;
 //   leader,    warp 1   lane 0 copies the scales into both CTAs' tensor memory and
 //                       issues the pair MMAs; commits release the stage in both CTAs;
+// Work split: whole 256 x 256 units go round robin over the clusters; when the last wave
+// would leave clusters idle, the k-stages of its leftover units are shared out in equal
+// contiguous ranges instead (stream-K), and a unit whose stages fall to several clusters
+// is finished by the last of them to arrive: each writes its FP32 partial sums to a
+// workspace slot and counts itself in, and the last one adds the slots in stage order
+// (the same order whoever arrives last) before its output stage.
 //   both CTAs, warps 2-9  epilogue of the CTA's 128 accumulator rows: tensor memory ->
 //                       registers, an arrive on the leader's accumulator barrier (the next
 //                       unit's MMAs may start), then (FP8) BF16 pieces of 32 rows x 32
@@ -53,12 +59,14 @@ struct Cfg2 {
   static constexpr int kOutBytes = kStaged ? 8 * 2048 : 0;
   static constexpr int kStages0 = (kSmemLimit - 2048 - kOutBytes) / kStageBytes;
   static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kOutBytes + 256;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kOutBytes + 512;
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
 };
 
 struct Pair2Params {
   __nv_bfloat16* D;
+  float* part;          // split-unit partial sums [clusters][2][2 CTAs][128 x 256], or null
+  int* arrivals;        // [2 * leftover units] CTAs counted in per split unit (zero between launches)
   Epilogue epi;         // optional bias and activation
   int64_t M, N;
   int sfa_kq;           // row-scale chunks per 128-row block
@@ -139,6 +147,82 @@ __device__ __forceinline__ void mma_mxf4_pair(uint32_t d, uint64_t a, uint64_t b
       : "memory");
 }
 
+// A range shorter than this many stage granules is not worth splitting a unit for.
+constexpr int kMinGranules = 8;
+// The extra time of a split range (pipeline start, partial sums written and added), in
+// k-stages of the unit's own MMA time.
+constexpr int kSplitCostStages = 40;
+
+// The clusters' share of the units: units [0, t_dp) whole and round robin; the P clusters
+// with a stream-K range share W granules (a granule: the stages one row-scale chunk
+// covers) of units [t_dp, units), gpu granules per unit.
+struct DSched {
+  int units, KS, gran, gpu, t_dp, P, W;
+};
+__device__ __forceinline__ DSched make_dsched(int units, int KS, int gran, int clusters,
+                                              bool can_split) {
+  DSched s;
+  s.units = units;
+  s.KS = KS;
+  s.gran = gran;
+  s.gpu = (KS + gran - 1) / gran;
+  s.t_dp = units;
+  s.P = 0;
+  s.W = 0;
+  const int rem = units % clusters;
+  // Worth it only when the split tail, rem / clusters of a unit's KS stages plus a fixed
+  // cost, beats the last wave's one unit: a split range pays for its own pipeline start
+  // and for writing and summing partial sums, about kSplitCostStages stages' time as
+  // measured (8192^3 FP8, KS 64, 36 leftover units of 76: 2.5% slower; 4096x4096x14336,
+  // KS 112, 28 of 76: 3.3% faster; FP4 8192^3, KS 32: 4.9% slower).
+  if (can_split && rem != 0 &&
+      static_cast<int64_t>(rem) * KS <= static_cast<int64_t>(clusters) * (KS - kSplitCostStages)) {
+    const int64_t W = static_cast<int64_t>(rem) * s.gpu;
+    int64_t P = W / kMinGranules;
+    if (P > clusters) P = clusters;
+    if (P > rem && W < INT32_MAX) {   // only when it puts more clusters to work
+      s.t_dp = units - rem;
+      s.P = static_cast<int>(P);
+      s.W = static_cast<int>(W);
+    }
+  }
+  return s;
+}
+__device__ __forceinline__ int dsk_begin(const DSched& s, int c) {
+  return static_cast<int>(static_cast<int64_t>(c) * s.W / s.P);
+}
+__device__ __forceinline__ int dsk_owner(const DSched& s, int it) {
+  return static_cast<int>((static_cast<int64_t>(it + 1) * s.P - 1) / s.W);
+}
+// Work item of a warp: unit u, stages [ks0, ks1).  The position (next whole unit, next
+// granule, end) lives in shared memory, one copy per warp, so it costs no registers.
+__device__ __forceinline__ void dwork_init(const DSched& s, volatile int* st, int c) {
+  st[0] = c;
+  st[1] = c < s.P ? dsk_begin(s, c) : 0;
+  st[2] = c < s.P ? dsk_begin(s, c + 1) : 0;
+}
+__device__ __forceinline__ bool dwork_next(const DSched& s, volatile int* st, int clusters, int& u,
+                                           int& ks0, int& ks1) {
+  const int dp = st[0];
+  if (dp < s.t_dp) {
+    u = dp;
+    ks0 = 0;
+    ks1 = s.KS;
+    st[0] = dp + clusters;
+    return true;
+  }
+  const int it = st[1], end = st[2];
+  if (it >= end) return false;
+  const int v = it / s.gpu;
+  const int g0 = it - v * s.gpu;
+  const int g1 = s.gpu - g0 <= end - it ? s.gpu : g0 + (end - it);
+  st[1] = it + (g1 - g0);
+  u = s.t_dp + v;
+  ks0 = g0 * s.gran;
+  ks1 = g1 * s.gran < s.KS ? g1 * s.gran : s.KS;
+  return true;
+}
+
 // Unit u -> (256-row unit row ur, 256-column tile nt), banded along N for L2 reuse.
 __device__ __forceinline__ void unit_tile2(const Pair2Params& p, int u, int& ur, int& nt) {
   const int per_band = kBandUnits * p.num_n_tiles;
@@ -177,6 +261,9 @@ __global__ void __maxnreg__(168)
   uint64_t* drain = acc_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = abort_flag + 1;           // this CTA finishes the current split unit
+  DSched& sched = *reinterpret_cast<DSched*>(const_cast<int*>(abort_flag + 2));
+  volatile int* work_state = abort_flag + 2 + (sizeof(DSched) + 3) / 4;   // [10 warps][4]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -191,6 +278,8 @@ __global__ void __maxnreg__(168)
     mbar_init(acc_empty, 2 * kEpiWarps);   // used in the leader: epilogues of both CTAs
     mbar_init(drain, 1);
     *abort_flag = 0;
+    sched = make_dsched(p.num_unit_rows * p.num_n_tiles, p.num_k_stages, C::kStagesPerChunk,
+                        static_cast<int>(gridDim.x >> 1), p.part != nullptr);
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
@@ -207,9 +296,9 @@ __global__ void __maxnreg__(168)
   cluster_sync();   // both CTAs' barriers initialised and tensor memory allocated
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total_units = p.num_unit_rows * p.num_n_tiles;
-  const int first_unit = static_cast<int>(blockIdx.x >> 1);
-  const int unit_stride = static_cast<int>(gridDim.x >> 1);
+  const int cluster_id = static_cast<int>(blockIdx.x >> 1);
+  const int clusters = static_cast<int>(gridDim.x >> 1);
+  volatile int* wst = work_state + warp * 4;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -217,12 +306,14 @@ __global__ void __maxnreg__(168)
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_parity = 0;
       bool ok = true;
-      for (int u = first_unit; ok && u < total_units; u += unit_stride) {
+      dwork_init(sched, wst, cluster_id);
+      int u, ks0, ks1;
+      while (ok && dwork_next(sched, wst, clusters, u, ks0, ks1)) {
         int ur, nt;
         unit_tile2(p, u, ur, nt);
         const int mt = ur * 2 + static_cast<int>(rank);          // this CTA's 128 rows of A
         const int nb = nt * 2 + static_cast<int>(rank);          // this CTA's 128 rows of B
-        for (int ks = 0; ks < p.num_k_stages; ++ks) {
+        for (int ks = ks0; ks < ks1; ++ks) {
           if (!mbar_wait(&empty[stage], phase ^ 1, p.limit_ns, abort_flag, p.status)) {
             ok = false;
             break;
@@ -268,10 +359,12 @@ __global__ void __maxnreg__(168)
       uint32_t phase = 0, kiter = 0, chunk = 0;
       bool ok = true;
       int local = 0;
-      for (int u = first_unit; ok && u < total_units; u += unit_stride, ++local) {
+      dwork_init(sched, wst, cluster_id);
+      int u, ks0, ks1;
+      for (; ok && dwork_next(sched, wst, clusters, u, ks0, ks1); ++local) {
         if (!mbar_wait(acc_empty, (local & 1) ^ 1, p.limit_ns, abort_flag, p.status)) break;
         tc_fence_after();
-        for (int ks = 0; ks < p.num_k_stages; ++ks) {
+        for (int ks = ks0; ks < ks1; ++ks) {
           if (!mbar_wait(&full[stage], phase, p.limit_ns, abort_flag, p.status)) {
             ok = false;
             break;
@@ -297,7 +390,7 @@ __global__ void __maxnreg__(168)
                                      : make_sdesc(a_base + j * 32, 16, 1024, kSwizzle128B);
             const uint64_t bd = B_MN ? make_sdesc(b_base + j * 4096, 16384, 1024, kSwizzle128B)
                                      : make_sdesc(b_base + j * 32, 16, 1024, kSwizzle128B);
-            const uint32_t acc = (ks | j) != 0;
+            const uint32_t acc = ks != ks0 || j != 0;
             if (FP4) {
               const int g = j >> 1;                                   // K group within the stage
               const uint32_t sfid = (j & 1) * 2;
@@ -310,7 +403,7 @@ __global__ void __maxnreg__(168)
           }
           tc_commit_pair(&empty[stage], kPairMask);
           ++kiter;
-          if (sub == C::kStagesPerChunk - 1 || ks == p.num_k_stages - 1) ++chunk;
+          if (sub == C::kStagesPerChunk - 1 || ks == ks1 - 1) ++chunk;
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1;
@@ -331,7 +424,9 @@ __global__ void __maxnreg__(168)
     const int h = (warp - 2) >> 2;
     const uint32_t acc_empty_leader = map_to_cta(smem_u32(acc_empty), 0);
     int local = 0;
-    for (int u = first_unit; u < total_units; u += unit_stride, ++local) {
+    dwork_init(sched, wst, cluster_id);
+    int u, ks0, ks1;
+    for (; dwork_next(sched, wst, clusters, u, ks0, ks1); ++local) {
       int ur, nt;
       unit_tile2(p, u, ur, nt);
       const int mt = ur * 2 + static_cast<int>(rank);
@@ -348,67 +443,121 @@ __global__ void __maxnreg__(168)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
       const int64_t row = static_cast<int64_t>(mt) * 128 + q * 32 + lane;
+      const int64_t row0 = static_cast<int64_t>(mt) * 128 + q * 32;
       const int64_t col0 = static_cast<int64_t>(nt) * 256 + h * kCols;
-      if constexpr (C::kStaged) {
-        // 32 x 32 pieces: lane = row; the piece's 16-byte groups of 8 columns go to the
-        // buffer in the 64-byte swizzle the tensor map names (group v of row r at
-        // position v ^ ((r / 2) % 4)), so the 32 lanes' writes hit distinct banks.
-        const int64_t row0 = static_cast<int64_t>(mt) * 128 + q * 32;
-        uint8_t* stg = sOut + (warp - 2) * 2048;
-        if (row0 < p.M) {
+      uint8_t* stg = sOut + (warp - 2) * 2048;
+      // Output of the 32-column piece c of this warp's 32 rows x 128 columns (vals: 32
+      // FP32 values of this lane's row).  FP8: BF16 through the warp's buffer to a TMA
+      // tensor store -- lane = row, the 16-byte group v of 8 columns at position
+      // v ^ ((r / 2) % 4), the tensor map's 64-byte swizzle, so the lanes hit distinct
+      // banks.  FP4: 16-byte stores from registers.
+      auto store_piece = [&](int c, const uint32_t* vals) {
+        if constexpr (C::kStaged) {
+          if (row0 >= p.M || col0 + c * 32 >= p.N) return;   // warp-uniform
+          uint32_t o[4][4];
 #pragma unroll
-          for (int c = 0; c < kChunks; ++c) {
-            if (col0 + c * 32 >= p.N) break;   // warp-uniform
-            uint32_t o[4][4];
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const int64_t col = col0 + c * 32 + v * 8;
-              if constexpr (EPI) {
-                if (col < p.N) {
-                  apply8(&r[c][v * 8], col, p.epi, o[v]);
-                  continue;
-                }
+          for (int g = 0; g < 4; ++g) {
+            const int64_t col = col0 + c * 32 + g * 8;
+            if constexpr (EPI) {
+              if (col < p.N) {
+                apply8(vals + g * 8, col, p.epi, o[g]);
+                continue;
               }
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                o[v][j] = pack_bf16x2(__uint_as_float(r[c][v * 8 + 2 * j]),
-                                      __uint_as_float(r[c][v * 8 + 2 * j + 1]));
             }
-            if (lane == 0) bulk_wait_group_read<0>();   // the previous piece has been read
-            __syncwarp();
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const uint32_t a = smem_u32(stg + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16));
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(o[v][0]),
-                           "r"(o[v][1]), "r"(o[v][2]), "r"(o[v][3])
-                           : "memory");
-            }
-            fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tmD, stg, static_cast<int32_t>(col0 + c * 32), static_cast<int32_t>(row0));
-              bulk_commit_group();
+            for (int j = 0; j < 4; ++j)
+              o[g][j] = pack_bf16x2(__uint_as_float(vals[g * 8 + 2 * j]),
+                                    __uint_as_float(vals[g * 8 + 2 * j + 1]));
+          }
+          if (lane == 0) bulk_wait_group_read<0>();   // the previous piece has been read
+          __syncwarp();
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint32_t a = smem_u32(stg + lane * 64 + ((g ^ ((lane >> 1) & 3)) * 16));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(o[g][0]),
+                         "r"(o[g][1]), "r"(o[g][2]), "r"(o[g][3])
+                         : "memory");
+          }
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmD, stg, static_cast<int32_t>(col0 + c * 32), static_cast<int32_t>(row0));
+            bulk_commit_group();
+          }
+        } else {
+          if (row >= p.M) return;
+          __nv_bfloat16* out = p.D + row * p.N + col0;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int o = c * 32 + g * 8;
+            if (col0 + o < p.N) {
+              if constexpr (EPI)
+                store8(out + o, vals + g * 8, col0 + o, p.epi);
+              else
+                st_global_v4_cs(out + o,
+                                pack_bf16x2(__uint_as_float(vals[g * 8 + 0]), __uint_as_float(vals[g * 8 + 1])),
+                                pack_bf16x2(__uint_as_float(vals[g * 8 + 2]), __uint_as_float(vals[g * 8 + 3])),
+                                pack_bf16x2(__uint_as_float(vals[g * 8 + 4]), __uint_as_float(vals[g * 8 + 5])),
+                                pack_bf16x2(__uint_as_float(vals[g * 8 + 6]), __uint_as_float(vals[g * 8 + 7])));
             }
           }
         }
-      } else if (row < p.M) {
-        __nv_bfloat16* out = p.D + row * p.N + col0;
+      };
+      if (ks0 == 0 && ks1 == p.num_k_stages) {
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c)
+        for (int c = 0; c < kChunks; ++c) store_piece(c, r[c]);
+        continue;
+      }
+      // A split unit.  Slot layout, chosen so that a warp's 32 lanes write and read 512
+      // contiguous bytes: [warp (quarter, half)][32-column piece][4-column group][lane];
+      // the slot of cluster c for this unit is (c, its first or last unit, this CTA's half).
+      const int v = u - sched.t_dp;
+      float4* const part = reinterpret_cast<float4*>(p.part) + (q * 2 + h) * (kChunks * 8 * 32) + lane;
+      auto slot_of = [&](int c) -> float4* {
+        const int which = dsk_begin(sched, c) / sched.gpu == v ? 0 : 1;
+        return part + static_cast<uint32_t>((c * 2 + which) * 2 + static_cast<int>(rank)) * (128 * 256 / 4);
+      };
+      float4* mine = slot_of(cluster_id);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int o = c * 32 + v * 8;
-            if (col0 + o < p.N) {
-              if constexpr (EPI)
-                store8(out + o, &r[c][v * 8], col0 + o, p.epi);
-              else
-                st_global_v4_cs(out + o,
-                                pack_bf16x2(__uint_as_float(r[c][v * 8 + 0]), __uint_as_float(r[c][v * 8 + 1])),
-                                pack_bf16x2(__uint_as_float(r[c][v * 8 + 2]), __uint_as_float(r[c][v * 8 + 3])),
-                                pack_bf16x2(__uint_as_float(r[c][v * 8 + 4]), __uint_as_float(r[c][v * 8 + 5])),
-                                pack_bf16x2(__uint_as_float(r[c][v * 8 + 6]), __uint_as_float(r[c][v * 8 + 7])));
-            }
+      for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          __stcg(mine + (c * 8 + j) * 32,
+                 make_float4(__uint_as_float(r[c][4 * j]), __uint_as_float(r[c][4 * j + 1]),
+                             __uint_as_float(r[c][4 * j + 2]), __uint_as_float(r[c][4 * j + 3])));
+      __threadfence();
+      named_barrier_sync(2, kEpiWarps * 32);
+      if (threadIdx.x == 64) {
+        const int nseg = dsk_owner(sched, (v + 1) * sched.gpu - 1) - dsk_owner(sched, v * sched.gpu) + 1;
+        const int arrived = atomicAdd(&p.arrivals[v * 2 + rank], 1) + 1;
+        const int last = arrived == nseg;
+        if (last) p.arrivals[v * 2 + rank] = 0;   // every contributor has counted itself in
+        *last_flag = last;
+      }
+      named_barrier_sync(2, kEpiWarps * 32);
+      if (!*last_flag) continue;
+      __threadfence();
+      // the last to arrive: every contributor's slot summed in stage order, a 32-column
+      // piece at a time, and stored
+      const int c_lo = dsk_owner(sched, v * sched.gpu);
+      const int c_hi = dsk_owner(sched, (v + 1) * sched.gpu - 1);
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        uint32_t sum[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sum[i] = 0u;
+        for (int cc = c_lo; cc <= c_hi; ++cc) {
+          const float4* src = slot_of(cc) + c * 8 * 32;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 x = __ldcg(src + j * 32);
+            sum[4 * j] = __float_as_uint(__uint_as_float(sum[4 * j]) + x.x);
+            sum[4 * j + 1] = __float_as_uint(__uint_as_float(sum[4 * j + 1]) + x.y);
+            sum[4 * j + 2] = __float_as_uint(__uint_as_float(sum[4 * j + 2]) + x.z);
+            sum[4 * j + 3] = __float_as_uint(__uint_as_float(sum[4 * j + 3]) + x.w);
           }
+        }
+        store_piece(c, sum);
       }
     }
     // every tensor store of this warp has finished reading and writing before the
@@ -479,7 +628,7 @@ bsmma_status launch_2sm(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
 bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B,
                                 const uint8_t* sfb, void* D, int64_t M, int64_t N, int64_t K,
                                 bsmma_layout layout, bsmma_fmt a_fmt, bsmma_fmt b_fmt,
-                                cudaStream_t stream, const void* bias, int act) {
+                                cudaStream_t stream, const void* bias, int act, bool may_split) {
   bsmma_status st;
   const DeviceInfo* dev = current_device(&st);
   if (!dev) return st;
@@ -505,6 +654,12 @@ bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B
                          fp4 ? 8 : 4);
   if (st != BSMMA_OK) return st;
   Pair2Params p;
+  p.part = nullptr;
+  p.arrivals = nullptr;
+  if (may_split) {
+    st = split_workspace(stream, &p.part, &p.arrivals);
+    if (st != BSMMA_OK) return st;
+  }
   p.D = static_cast<__nv_bfloat16*>(D);
   p.epi.bias = static_cast<const __nv_bfloat16*>(bias);
   p.epi.act = act;

@@ -66,9 +66,10 @@ bsmma_status mx_gemm_noalloc(const void* A, const uint8_t* sA, const void* B, co
   // previous call's contents never leak into this one
   st = launch_wide_relayout(sA, M, scratch, sB, N, scratch + bytes_a, K / 32, s);
   if (st != BSMMA_OK) return st;
-  // no tuning runs here: they would create events and synchronise the stream
+  // no tuning runs (they would create events and synchronise the stream) and no split
+  // units (their workspace is allocated on first use)
   return launch_mx_gemm(A, scratch, B, scratch + bytes_a, D, M, N, K, layout, a_fmt, b_fmt, s,
-                        nullptr, 0, /*may_tune=*/false);
+                        nullptr, 0, /*may_allocate=*/false);
 }
 
 }  // extern "C"

@@ -92,6 +92,13 @@ typedef enum { BSMMA_SCALES_A = 0, BSMMA_SCALES_B = 1 } bsmma_scale_role;
  * workspaces.  The workspace is keyed by the stream handle: let a stream's pending
  * mx_gemm work finish before destroying the stream, since a stream created later
  * may get the same handle and with it the same workspace.
+ * When the last wave of 256 x 256 output units would leave most SM pairs idle, the
+ * kernel splits those units' K range over the idle pairs and the last pair to finish
+ * a unit adds the others' FP32 partial sums, in K order (the result does not depend on
+ * which pair finishes last).  The partial sums live in a second per-(device, stream)
+ * workspace of fixed size (two 128 KB slots per SM), allocated, its counters zeroed,
+ * by the stream's first dense call; that first call must not be captured (it returns
+ * BSMMA_ERR_WORKSPACE then; bsmma_reserve_workspace allocates it too).
  * Two kernel launches per call (relayout, GEMM).
  */
 bsmma_status mx_gemm(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
@@ -103,7 +110,8 @@ bsmma_status mx_gemm(const void* A, const uint8_t* sA, const void* B, const uint
  * mx_scale_relayout: sA_tiled with role BSMMA_SCALES_A for the M rows
  * (mx_scale_tiled_bytes(M, K/32, BSMMA_SCALES_A) bytes), sB_tiled with role
  * BSMMA_SCALES_B for the N rows.  Lets callers relayout static weight scales once.
- * One kernel launch; allocates nothing.
+ * One kernel launch.  It allocates nothing but the fixed-size split workspace of
+ * mx_gemm, on the stream's first dense call.
  */
 bsmma_status mx_gemm_tiled(const void* A, const uint8_t* sA_tiled, const void* B,
                            const uint8_t* sB_tiled, void* D, int64_t M, int64_t N, int64_t K,
@@ -131,7 +139,8 @@ bsmma_status mx_gemm_tiled(const void* A, const uint8_t* sA_tiled, const void* B
  * (cudaGetSymbolAddress) and caches it; make that first call before any stream
  * capture.  All calls on a device share the one array and overwrite it completely,
  * so calls that can overlap on the GPU (different streams without ordering between
- * them) race with each other; order them on one stream.  It never runs the
+ * them) race with each other; order them on one stream.  It never splits output units
+ * (their workspace is allocated on first use), and it never runs the
  * autotuner's timing runs (they create events and synchronise): with tuning enabled
  * it takes the stored choice for the shape class, else the SM-pair kernel.
  */
@@ -329,10 +338,12 @@ bsmma_status fp8_group_quantize(const void* x, bsmma_dtype x_dtype, int64_t tota
 bsmma_status fp8_block_quantize(const void* w, bsmma_dtype w_dtype, int64_t G, int64_t N,
                                 int64_t K, uint8_t* codes, float* scales, bsmma_stream stream);
 
-/* Grows the current (device, stream) scale workspace to at least `bytes`
- * (call before capturing mx_gemm into a CUDA graph).  The stream argument is this
- * library's addition to the boundary: workspaces are kept per stream, so the one
- * that a later capture on `stream` will use is the one reserved. */
+/* Grows the current (device, stream) scale workspace to at least `bytes` and allocates
+ * the stream's split workspace if it has none (call before capturing mx_gemm or
+ * mx_gemm_tiled into a CUDA graph).  The stream argument is this library's addition to
+ * the boundary: workspaces are kept per stream, so the ones that a later capture on
+ * `stream` will use are the ones reserved.  After bsmma_device_status has returned
+ * BSMMA_DEV_TIMEOUT, the split workspaces' counters are cleared before it returns. */
 bsmma_status bsmma_reserve_workspace(int64_t bytes, bsmma_stream stream);
 
 /* Synchronises `stream`, then returns and clears the current device's latched

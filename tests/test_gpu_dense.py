@@ -56,6 +56,36 @@ SMALL = [
 ]
 
 
+# Few output units with a long K: the SM-pair kernel splits their k-stages over more
+# clusters than there are units, and the last cluster to finish a unit adds the others'
+# partial sums (the work split's reduction), for every format, layout and a ragged edge.
+SPLIT = [
+    (512, 512, 8192, "NT", "e4m3", "e4m3"),
+    (300, 776, 6144, "NT", "e4m3", "e5m2"),
+    (512, 768, 4096, "NN", "e4m3", "e4m3"),
+    (528, 512, 4096, "TN", "e5m2", "e4m3"),
+    (512, 512, 8192, "NT", "e2m1", "e2m1"),
+    (256, 256, 16384, "NT", "e4m3", "e4m3"),
+]
+
+
+@pytest.mark.parametrize("shape", SPLIT, ids=lambda s: "-".join(map(str, s)))
+def test_dense_split_units(shape):
+    M, N, K, layout, af, bf = shape
+    c = synthetic.mx_operands((61, M + N), M, N, K, layout, af, bf)
+    check(c)
+    check(c, tiled=True)
+
+
+def test_dense_split_units_deterministic():
+    """The split units' partial sums are added in stage order whoever arrives last, so
+    repeated calls give the same bits."""
+    c = synthetic.mx_operands((62, 0), 512, 512, 8192, "NT", "e4m3", "e4m3")
+    a = run_dense(c)
+    for _ in range(3):
+        assert np.array_equal(run_dense(c), a)
+
+
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: "-".join(map(str, s)))
 def test_dense_small(shape, variant):
     M, N, K, layout, af, bf = shape

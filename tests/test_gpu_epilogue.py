@@ -73,6 +73,16 @@ def test_bias_act_every_kernel_variant(variant, act):
     assert_close(got, ref, f"variant {variant} {act}")
 
 
+def test_bias_act_on_split_units():
+    """Few units with a long K: the split units' summed partials go through the fused
+    output stage."""
+    M, N, K = 512, 768, 8192
+    c = synthetic.mx_operands((73, 0), M, N, K, "NT", "e4m3", "e4m3")
+    bias = make_bias((73,), N)
+    got, ref = run_case(c, bias, "gelu", tiled=False)
+    assert_close(got, ref, "split units, bias + GELU")
+
+
 def test_empty_stage_is_mx_gemm_bit_for_bit():
     M, N, K = 256, 384, 512
     c = synthetic.mx_operands((72, 0), M, N, K, "NT", "e4m3", "e4m3")

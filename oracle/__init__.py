@@ -14,6 +14,9 @@ this module compiles it with gcc and exposes numpy-friendly wrappers:
 * :func:`grouped_fp8_gemm` -- grouped groupwise FP8 GEMM with per-1x128 activation
   scales in the per-group block layout and per-128x128 weight scales ("Add FlyDSL
   grouped groupwise FP8 GEMM for ROCm", introduction and the scale-layout fix).
+* :func:`grouped_bf16_gemm` -- grouped BF16 GEMM with no scales, D[r] = X[r] . W[g(r)]^T
+  over uneven and empty groups ("PyTorch on AMD GPUs gains a FlyDSL backend",
+  Interpretation: the BF16 grouped-GEMM cases).
 * :func:`wide_scale_relayout` / :func:`wide_scale_bytes` -- the integer
   permutations (with padding) of plain E8M0 scales into the tiled layouts the GEMM
   kernels copy into tensor memory, for the scales of op(A) (role 0) and op(B)
@@ -77,6 +80,8 @@ def bind(path: str):
     lib.oracle_mx_gemm.restype = i32
     lib.oracle_grouped_fp8_gemm.argtypes = [p, p, p, p, p, i32, i64, i64, i64, p, i64, p, i32]
     lib.oracle_grouped_fp8_gemm.restype = i32
+    lib.oracle_grouped_bf16_gemm.argtypes = [p, p, p, i32, i64, i64, i64, p, i64, p, i32]
+    lib.oracle_grouped_bf16_gemm.restype = i32
     lib.oracle_wide_scale_bytes.argtypes = [i64, i64, i32]
     lib.oracle_wide_scale_bytes.restype = i64
     lib.oracle_wide_scale_relayout.argtypes = [p, i64, i64, i32, p]
@@ -167,6 +172,27 @@ def grouped_fp8_gemm(X, sX, W, sW, m_sizes, N, K, rows=None, nthreads=None,
                                          _ptr(D), _threads(nthreads))
     if rc != 0:
         raise ValueError("oracle_grouped_fp8_gemm: bad arguments")
+    return D
+
+
+def grouped_bf16_gemm(X, W, m_sizes, N, K, rows=None, nthreads=None, lib=None) -> np.ndarray:
+    """FP64 D[rows, N] of the grouped BF16 GEMM: D[r] = X[r] . W[g(r)]^T.
+
+    X [total_M, K] and W [G, N, K] are BF16 bit patterns (uint16), m_sizes int64 [G].
+    """
+    X = np.ascontiguousarray(X, dtype=np.uint16)
+    W = np.ascontiguousarray(W, dtype=np.uint16)
+    ms = np.ascontiguousarray(m_sizes, dtype=np.int64)
+    G = ms.size
+    total_M = X.shape[0] if X.ndim == 2 else X.size // max(K, 1)
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nrows = total_M if r is None else r.size
+    D = np.zeros((nrows, N), dtype=np.float64)
+    rc = _load(lib).oracle_grouped_bf16_gemm(_ptr(X), _ptr(W), _ptr(ms), G, total_M, N, K,
+                                             None if r is None else _ptr(r), nrows, _ptr(D),
+                                             _threads(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_grouped_bf16_gemm: bad arguments")
     return D
 
 

@@ -24,6 +24,11 @@
  *                      * sum_{k in block kb} e4m3(X[r][k]) * e4m3(W[g][n][k])
  *     with sX(g,l,kb) = sA[M_start_g*(K/128) + l + kb*m_g]  (per-group blocks).
  *
+ *   grouped BF16 ("PyTorch on AMD GPUs gains a FlyDSL backend", Interpretation:
+ *   grouped GEMM over uneven and empty groups, BF16 cases):
+ *
+ *     for row r of group g:  D[r][n] = sum_k bf16(X[r][k]) * bf16(W[g][n][k])
+ *
  * Decoding is by 256-entry (16 for E2M1) tables built from the format
  * definitions (OCP E4M3FN, E5M2, E2M1, E8M0).  Every operand row is decoded
  * once into an FP64 buffer, then plain sequential dot products are taken.
@@ -283,6 +288,97 @@ int oracle_grouped_fp8_gemm(const uint8_t* X, const float* sX, const uint8_t* W,
   free(jobs);
   free(Xdec);
   free(meta);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Grouped BF16 GEMM ("PyTorch on AMD GPUs gains a FlyDSL backend",          */
+/* Interpretation: grouped GEMM over uneven and empty expert groups, BF16    */
+/* cases).  The plain reading: for row r of group g,                         */
+/*   D[r][n] = sum_k bf16(X[r][k]) * bf16(W[g][n][k])                         */
+/* with no scales.  BF16 is decoded from its bit fields (1 sign, 8 exponent  */
+/* bits with bias 127, 7 mantissa bits).                                     */
+/* ------------------------------------------------------------------------ */
+static double bf16_value(uint16_t c) {
+  int s = c >> 15, e = (c >> 7) & 255, m = c & 127;
+  double v;
+  if (e == 255) v = (m == 0) ? INFINITY : NAN;
+  else if (e == 0) v = ldexp((double)m, -133);             /* m/128 * 2^(1-127) */
+  else v = ldexp(128.0 + m, e - 134);                       /* (1+m/128) * 2^(e-127) */
+  return s ? -v : v;
+}
+
+typedef struct {
+  const uint16_t* W;
+  const double* Xdec;                    /* [nrows][K] decoded sampled rows of X */
+  int64_t N, K, nrows;
+  const int64_t* grp_of;
+  int G;
+  double* D;
+  int64_t n0, n1;
+} grouped_bf16_job;
+
+static void* grouped_bf16_worker(void* p) {
+  grouped_bf16_job* j = (grouped_bf16_job*)p;
+  double* wrow = (double*)malloc(sizeof(double) * (size_t)(j->K > 0 ? j->K : 1));
+  for (int g = 0; g < j->G; ++g) {
+    int any = 0;
+    for (int64_t r = 0; r < j->nrows; ++r) any |= (j->grp_of[r] == g);
+    if (!any) continue;
+    for (int64_t n = j->n0; n < j->n1; ++n) {
+      const uint16_t* w = j->W + ((int64_t)g * j->N + n) * j->K;
+      for (int64_t k = 0; k < j->K; ++k) wrow[k] = bf16_value(w[k]);
+      for (int64_t r = 0; r < j->nrows; ++r) {
+        if (j->grp_of[r] != g) continue;
+        const double* xrow = j->Xdec + r * j->K;
+        double acc = 0.0;
+        for (int64_t k = 0; k < j->K; ++k) acc += xrow[k] * wrow[k];
+        j->D[r * j->N + n] = acc;
+      }
+    }
+  }
+  free(wrow);
+  return 0;
+}
+
+/*
+ * X [total_M][K] BF16 bit patterns, W [G][N][K] BF16 bit patterns, m_sizes [G]
+ * int64 (host).  Output rows `rows` (global row ids; NULL = all total_M rows) into
+ * D[nrows][N].  Returns 0, or -1 on bad arguments (negative size, sum != total_M,
+ * row id out of range).
+ */
+int oracle_grouped_bf16_gemm(const uint16_t* X, const uint16_t* W, const int64_t* m_sizes, int G,
+                             int64_t total_M, int64_t N, int64_t K, const int64_t* rows,
+                             int64_t nrows, double* D, int nthreads) {
+  if (G < 1 || N < 0 || K < 0) return -1;
+  int64_t sum = 0;
+  for (int g = 0; g < G; ++g) { if (m_sizes[g] < 0) return -1; sum += m_sizes[g]; }
+  if (sum != total_M) return -1;
+  if (rows == NULL) nrows = total_M;
+  if (nrows == 0 || N == 0) return 0;
+  int64_t* grp_of = (int64_t*)malloc(sizeof(int64_t) * (size_t)nrows);
+  double* Xdec = (double*)malloc(sizeof(double) * (size_t)(nrows * (K > 0 ? K : 1)));
+  for (int64_t r = 0; r < nrows; ++r) {
+    int64_t row = rows ? rows[r] : r;
+    if (row < 0 || row >= total_M) { free(grp_of); free(Xdec); return -1; }
+    int64_t start = 0;
+    int g = 0;
+    while (row >= start + m_sizes[g]) { start += m_sizes[g]; ++g; }
+    grp_of[r] = g;
+    for (int64_t k = 0; k < K; ++k) Xdec[r * K + k] = bf16_value(X[row * K + k]);
+  }
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > N) nthreads = (int)N;
+  grouped_bf16_job* jobs = (grouped_bf16_job*)malloc(sizeof(grouped_bf16_job) * (size_t)nthreads);
+  for (int t = 0; t < nthreads; ++t) {
+    grouped_bf16_job j = {W, Xdec, N, K, nrows, grp_of, G, D, N * t / nthreads,
+                          N * (t + 1) / nthreads};
+    jobs[t] = j;
+  }
+  run_parallel(jobs, sizeof(grouped_bf16_job), nthreads, grouped_bf16_worker);
+  free(jobs);
+  free(Xdec);
+  free(grp_of);
   return 0;
 }
 

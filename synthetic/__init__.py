@@ -19,6 +19,8 @@ Recipes
 * m_sizes (G = 8): two distinct empty groups; the other six share total_M by a
   multinomial draw over Dirichlet(1) weights; redrawn until at least one size is
   not a multiple of 128.
+* BF16 operands (grouped BF16 config): seeded N(0,1) float32 values truncated to
+  their top 16 bits (the BF16 bit pattern, rounding toward zero), no scales.
 * Seeds: ``numpy.random.default_rng([cfg, case, operand])`` (PCG64).
 
 The E4M3/E5M2 roundings use PyTorch's float8 casts (round-to-nearest-even) on
@@ -183,6 +185,19 @@ def grouped_operands(key, m_sizes, N, K):
     sX = to_group_block_layout(sx, m_sizes)
     return dict(X=X, sX=sX, W=W, sW=sw, m_sizes=m_sizes, N=N, K=K, x_val=x, w_val=w,
                 sx_rowmajor=sx)
+
+
+def grouped_bf16_operands(key, m_sizes, N, K):
+    """Seeded grouped BF16 operands: X [total_M, K] and W [G, N, K] as BF16 bit
+    patterns (uint16), from N(0,1) float32 values truncated to 16 bits."""
+    m_sizes = np.asarray(m_sizes, dtype=np.int64)
+    G = m_sizes.size
+    total_M = int(m_sizes.sum())
+    x = normal((*key, 0), (total_M, K))
+    w = normal((*key, 1), (G, N, K))
+    X = (x.view(np.uint32) >> 16).astype(np.uint16)
+    W = (w.view(np.uint32) >> 16).astype(np.uint16)
+    return dict(X=X, W=W, m_sizes=m_sizes, N=N, K=K)
 
 
 def to_group_block_layout(s_rows: np.ndarray, m_sizes) -> np.ndarray:

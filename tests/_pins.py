@@ -287,6 +287,83 @@ def pin_grouped_probes(lib=None):
         assert np.array_equal(got, expect), sizes
 
 
+# ---------------------------------------------------------------- grouped BF16
+def bf16_decode(bits: np.ndarray) -> np.ndarray:
+    """BF16 bit patterns -> float64 through PyTorch's bfloat16 dtype."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def random_finite_bf16(g: np.random.Generator, shape) -> np.ndarray:
+    """Uniform BF16 bit patterns over every finite code (subnormals and zeros included)."""
+    c = g.integers(0, 1 << 16, size=shape, dtype=np.uint32).astype(np.uint16)
+    inf_nan = (c & 0x7F80) == 0x7F80
+    return np.where(inf_nan, c & 0x807F, c).astype(np.uint16)
+
+
+def pin_grouped_bf16_decode_points(lib=None):
+    """Closed-form BF16 values through a 1x1x1 product with W = 1.0."""
+    points = {0x3F80: 1.0, 0xC000: -2.0, 0x4049: 3.140625, 0x0080: 2.0 ** -126,
+              0x0001: 2.0 ** -133, 0x807F: -127 * 2.0 ** -133, 0x7F7F: (2 - 2.0 ** -7) * 2.0 ** 127,
+              0x3C00: 2.0 ** -7, 0x0000: 0.0, 0x8000: 0.0, 0x4380: 256.0}
+    codes = np.array(list(points), dtype=np.uint16)
+    ms = np.array([codes.size], dtype=np.int64)
+    W = np.array([[[0x3F80]]], dtype=np.uint16)
+    got = oracle.grouped_bf16_gemm(codes.reshape(-1, 1), W, ms, 1, 1, lib=lib)
+    assert np.array_equal(got[:, 0], np.array(list(points.values()))), got[:, 0]
+
+
+def pin_grouped_bf16_vs_torch(lib=None):
+    """Random finite BF16 codes over uneven and empty groups against per-group float64
+    matmuls of PyTorch-decoded values (FP64 summation-order differences only)."""
+    g = np.random.default_rng([43, 0])
+    for sizes, N, K in (([0, 37, 5, 0, 1, 90], 24, 40), ([13], 7, 3), ([0, 0, 4, 0], 5, 129)):
+        ms = np.array(sizes, dtype=np.int64)
+        T, G = int(ms.sum()), ms.size
+        # random exponents over the whole finite range, squeezed so products stay finite
+        X = random_finite_bf16(g, (T, K))
+        W = random_finite_bf16(g, (G, N, K))
+        X = (X & 0x807F) | (((g.integers(100, 154, size=X.shape)) << 7).astype(np.uint16))
+        W[..., ::2] = (W[..., ::2] & 0x807F) | (g.integers(0, 4, size=W[..., ::2].shape) << 7).astype(np.uint16)
+        got = oracle.grouped_bf16_gemm(X, W, ms, N, K, lib=lib)
+        xd, wd = bf16_decode(X), bf16_decode(W)
+        ref = np.zeros((T, N))
+        bound = np.zeros((T, N))
+        start = 0
+        for gi, m in enumerate(sizes):
+            ref[start:start + m] = xd[start:start + m] @ wd[gi].T
+            bound[start:start + m] = np.abs(xd[start:start + m]) @ np.abs(wd[gi]).T
+            start += m
+        assert got.shape == (T, N)
+        assert np.all(np.abs(got - ref) <= 4 * K * 2.0 ** -53 * bound), sizes
+
+
+def pin_grouped_bf16_probes(lib=None):
+    """Exact index probes: D[r, n] = ((l mod 256) + 1) * 2^g from a single hot K
+    column, and D[r, n] = (n mod 8 + 1) * 2^(n/128 mod 8) from another."""
+    one = 0x3F80
+    for sizes in ([3, 0, 300, 1, 0, 129, 2, 5], [260], [0, 0, 0, 7]):
+        ms = np.array(sizes, dtype=np.int64)
+        G, T, N, K = ms.size, int(ms.sum()), 1024, 72
+        X = np.zeros((T, K), dtype=np.uint16)
+        W = np.zeros((G, N, K), dtype=np.uint16)
+        expect = np.zeros((T, N))
+        start = 0
+        n = np.arange(N)
+        colval = (n % 8 + 1) * 2.0 ** ((n // 128) % 8)
+        W[:, :, 70] = torch.from_numpy(colval.astype(np.float32)).bfloat16().view(torch.int16).numpy().view(np.uint16)
+        for gi, m in enumerate(sizes):
+            loc = np.arange(m)
+            rv = ((loc % 256) + 1).astype(np.float32)
+            X[start:start + m, 5] = torch.from_numpy(rv).bfloat16().view(torch.int16).numpy().view(np.uint16)
+            X[start:start + m, 70] = one
+            W[gi, :, 5] = torch.tensor([2.0 ** gi]).bfloat16().view(torch.int16).numpy().view(np.uint16)[0]
+            expect[start:start + m] = rv[:, None] * 2.0 ** gi + colval[None, :]
+            start += m
+        got = oracle.grouped_bf16_gemm(X, W, ms, N, K, lib=lib)
+        assert np.array_equal(got, expect), sizes
+
+
 # ---------------------------------------------------------------- relayout
 def load_wide_positions():
     out = []
@@ -522,4 +599,5 @@ def pin_bias_act(lib=None):
 ALL_PINS = [pin_decode_points, pin_decode_vs_torch, pin_dense_bruteforce, pin_dense_unit_scales,
             pin_dense_pow2, pin_dense_layouts, pin_grouped_concat, pin_grouped_g1_transpose,
             pin_grouped_probes, pin_wide_relayout, pin_quant_closed_form, pin_quant_vs_independent,
-            pin_quant_roundtrip, pin_quant_error_bound, pin_group_quant, pin_bias_act]
+            pin_quant_roundtrip, pin_quant_error_bound, pin_group_quant, pin_bias_act,
+            pin_grouped_bf16_decode_points, pin_grouped_bf16_vs_torch, pin_grouped_bf16_probes]

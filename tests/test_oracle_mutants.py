@@ -49,6 +49,15 @@ MUTANTS = [
     ("gelu_tanh_scale", "0.5 * v * (1.0 + erf(v / sqrt(2.0)))", "0.5 * v * (1.0 + erf(v / 2.0))"),
     ("silu_sign", "v = v / (1.0 + exp(-v));", "v = v / (1.0 + exp(v));"),
     ("relu_leaky", "v = v > 0.0 ? v : 0.0;", "v = v > 0.0 ? v : 0.01 * v;"),
+    ("bf16_exponent_bias", "v = ldexp(128.0 + m, e - 134);", "v = ldexp(128.0 + m, e - 133);"),
+    ("bf16_subnormal_scale", "v = ldexp((double)m, -133);", "v = ldexp((double)m, -132);"),
+    ("bf16_exponent_field", "e = (c >> 7) & 255, m = c & 127;", "e = (c >> 8) & 255, m = c & 127;"),
+    ("bf16_sign_dropped", "  return s ? -v : v;\n}", "  return v;\n}"),
+    ("bf16_row_group", "    grp_of[r] = g;\n", "    grp_of[r] = g > 0 ? g - 1 : 0;\n"),
+    ("bf16_w_transposed", "const uint16_t* w = j->W + ((int64_t)g * j->N + n) * j->K;",
+     "const uint16_t* w = j->W + (int64_t)g * j->N * j->K + n;"),
+    ("bf16_k_tail_dropped", "for (int64_t k = 0; k < j->K; ++k) acc += xrow[k] * wrow[k];",
+     "for (int64_t k = 0; k + 1 < j->K; ++k) acc += xrow[k] * wrow[k];"),
     ("block_sw_kmajor", "sw[(g * (N / 128) + nb) * (K / 128) + kb] = s;", "sw[(g * (K / 128) + kb) * (N / 128) + nb] = s;"),
 ]
 

@@ -93,3 +93,18 @@ def test_grouped_quantisation_error_matches_pages():
         start += m
     resid = np.abs(got - ref).max() / np.abs(ref).max()
     assert 0.005 < resid < 0.08, resid
+
+
+def test_grouped_bf16_recipe():
+    """BF16 operands are the N(0,1) inputs truncated toward zero to 16 bits: finite,
+    within one BF16 step of the value, never larger in magnitude."""
+    ms = np.array([0, 5, 0, 9], dtype=np.int64)
+    c = synthetic.grouped_bf16_operands((50, 1), ms, 16, 24)
+    assert c["X"].shape == (14, 24) and c["W"].shape == (4, 16, 24)
+    assert c["X"].dtype == np.uint16 and c["W"].dtype == np.uint16
+    from tests._pins import bf16_decode
+    x = synthetic.normal((50, 1, 0), (14, 24)).astype(np.float64)
+    xd = bf16_decode(c["X"])
+    assert np.all(np.isfinite(xd))
+    assert np.all(np.abs(xd) <= np.abs(x)) and np.all(np.sign(xd) == np.sign(x))
+    assert np.all(np.abs(x - xd) <= 2.0 ** -7 * np.abs(x))

@@ -9,7 +9,8 @@ Inputs are seeded N(0,1) values quantised per 32-wide K block (E8M0 scale
 MiB write) before every GEMM, outside the timed events.
 
 Other workloads (``--workload``): mxfp4_dense (8192^3 and 1024x14336x4096),
-grouped_fp8 (G=8, totM 128/1024/16384 x three (N,K)), linear_triple (fwd/dgrad/
+grouped_fp8 (G=8, totM 128/1024/16384 x three (N,K)), grouped_bf16 (the same shapes
+in BF16 without scales), linear_triple (fwd/dgrad/
 wgrad of X[8192,4096], W[14336,4096], dY[8192,14336]), mxfp8_256 (256^3),
 mxfp8_bias_gelu (the default GEMMs with a fused bias + GELU output stage), and
 quantize (the quantisers that make the operands, in GB/s against HBM bandwidth).
@@ -38,7 +39,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MX/FP8 GEMM TFLOPS (2MNK/s) and % of GB300 block-scaled tensor peak"
 FALLBACK_BF16_TFLOPS = 1900.0        # used only when MEASURED_PEAKS.json is absent
-NOMINAL_RATIO = {"fp8": 4.5 / 2.25, "fp4": 13.5 / 2.25}
+NOMINAL_RATIO = {"fp8": 4.5 / 2.25, "fp4": 13.5 / 2.25, "bf16": 1.0}
 
 
 # ----------------------------------------------------------------------------- workloads
@@ -72,6 +73,11 @@ def workload_spec(name: str):
         for g in out:
             g["packed"] = True
         return out
+    if name == "grouped_bf16":
+        out = workload_spec("grouped_fp8")
+        for g in out:
+            g["kind"] = "grouped_bf16"
+        return out
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -89,17 +95,20 @@ WORKLOAD_TEXT = {
     "grouped_fp8_packed": "the grouped_fp8 GEMMs on weights packed once outside the timed region "
                           "(grouped_fp8_pack_weights: each 128x128 weight tile one contiguous "
                           "block), as the pages' preshuffled grouped op packs at load time",
+    "grouped_bf16": "grouped BF16 (no scales), the grouped_fp8 shapes: G=8, totM in "
+                    "{128,1024,16384} x (N,K) in {(2048,7168),(7168,2304),(16384,6656)}; seeded "
+                    "uneven m_sizes with 2 empty groups; FP32 accumulation, BF16 out",
 }
 
 
 def describe(g) -> str:
-    if g["kind"] == "grouped":
-        return f'grouped G=8 totM={g["T"]} N={g["N"]} K={g["K"]}'
+    if g["kind"].startswith("grouped"):
+        return f'{g["kind"]} G=8 totM={g["T"]} N={g["N"]} K={g["K"]}'
     return f'{g["M"]}x{g["N"]}x{g["K"]} {g.get("layout", "")} {g.get("a", "")}x{g.get("b", "")}'
 
 
 def flops_of(g) -> float:
-    if g["kind"] == "grouped":
+    if g["kind"].startswith("grouped"):
         return 2.0 * g["T"] * g["N"] * g["K"]
     return 2.0 * g["M"] * g["N"] * g["K"]
 
@@ -109,6 +118,8 @@ def grouped_bytes(g, m_sizes) -> float:
     groups, X and its scales, D, m_sizes."""
     T, N, K = g["T"], g["N"], g["K"]
     live = int(sum(1 for m in m_sizes if m > 0))
+    if g["kind"] == "grouped_bf16":      # BF16 X and W, no scales
+        return live * N * K * 2 + T * K * 2 + 2 * T * N + 8 * len(m_sizes)
     return (live * (N * K + 4 * N * K / 128 ** 2) + T * K + 4 * T * K / 128 + 2 * T * N
             + 8 * len(m_sizes))
 
@@ -131,6 +142,8 @@ def make_inputs(g):
         g.update(M=c["M"], N=c["N"], K=c["K"])
         return c
     ms = synthetic.gen_m_sizes(g["T"], g["case"])
+    if g["kind"] == "grouped_bf16":
+        return synthetic.grouped_bf16_operands((5, g["case"]), ms, g["N"], g["K"])
     return synthetic.grouped_operands((4, g["case"]), ms, g["N"], g["K"])
 
 
@@ -255,7 +268,8 @@ def reduce_max(values, dist):
 # The sources each workload's dominant kernel is built from (the traffic record is
 # valid only while they are unchanged).
 KERNEL_SOURCES = {
-    "grouped_fp8": ("grouped_gemm.cu", "ptx.cuh", "internal.h"),
+    "grouped_fp8": ("grouped_gemm.cu", "grouped_sched.cuh", "ptx.cuh", "internal.h"),
+    "grouped_bf16": ("grouped_bf16.cu", "grouped_sched.cuh", "ptx.cuh", "internal.h"),
     "quantize": ("quantize.cu", "ptx.cuh", "internal.h"),
     "dense": ("mx_gemm_2sm.cu", "mx_gemm.cu", "ptx.cuh", "internal.h"),
 }
@@ -305,7 +319,15 @@ def run_ours(args):
     gemms = []
     for g in spec:
         c = make_inputs(g)
-        if g["kind"] == "grouped":
+        if g["kind"] == "grouped_bf16":
+            def bf16(a):
+                return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+            t = {"X": bf16(c["X"]).to(dev), "W": bf16(c["W"]).to(dev),
+                 "m_sizes": torch.from_numpy(c["m_sizes"]).to(dev)}
+            t["D"] = torch.empty((g["T"], g["N"]), dtype=torch.bfloat16, device=dev)
+            host = {"X": bf16(c["X"]).pin_memory(), "W": bf16(c["W"]).pin_memory(),
+                    "m_sizes": torch.from_numpy(c["m_sizes"]).pin_memory()}
+        elif g["kind"] == "grouped":
             t = {k: torch.from_numpy(np.ascontiguousarray(c[k])).to(dev)
                  for k in ("X", "sX", "W", "sW", "m_sizes")}
             t["D"] = torch.empty((g["T"], g["N"]), dtype=torch.bfloat16, device=dev)
@@ -339,7 +361,10 @@ def run_ours(args):
     def one_gemm(g, t, ev):
         """Relayout (a2) + GEMM (a3-a6); events: [start, after relayout, end]."""
         ev[0].record(stream)
-        if g["kind"] == "grouped":
+        if g["kind"] == "grouped_bf16":
+            ev[1].record(stream)
+            bs.grouped_bf16_gemm(t["X"], t["W"], t["m_sizes"], out=t["D"])
+        elif g["kind"] == "grouped":
             ev[1].record(stream)
             bs.grouped_fp8_gemm(t["X"], t["sX"], t["W"], t["sW"], t["m_sizes"], out=t["D"],
                                     packed=g.get("packed", False))
@@ -408,14 +433,17 @@ def run_ours(args):
             with torch.cuda.stream(h2d_stream):
                 if recorded[i]:
                     h2d_stream.wait_event(comp_done[i])     # the last step's GEMM i read its inputs
-                keys = ("X", "sX", "W", "sW", "m_sizes") if g["kind"] == "grouped" else ("A", "sA", "B", "sB")
+                keys = {"grouped": ("X", "sX", "W", "sW", "m_sizes"), "grouped_bf16": ("X", "W", "m_sizes")
+                        }.get(g["kind"], ("A", "sA", "B", "sB"))
                 for k in keys:
                     t[k].copy_(h[k], non_blocking=True)
                 h2d_done[i].record(h2d_stream)
             stream.wait_event(h2d_done[i])
             if recorded[i]:
                 stream.wait_event(d2h_done[i])              # the last step's result i is on the host
-            if g["kind"] == "grouped":
+            if g["kind"] == "grouped_bf16":
+                bs.grouped_bf16_gemm(t["X"], t["W"], t["m_sizes"], out=t["D"])
+            elif g["kind"] == "grouped":
                 bs.grouped_fp8_gemm(t["X"], t["sX"], t["W"], t["sW"], t["m_sizes"], out=t["D"],
                                     packed=g.get("packed", False))
             else:
@@ -455,7 +483,9 @@ def run_ours(args):
 
     bf16_peak, _, peak_src = measured_peaks()
     is_fp4 = args.workload == "mxfp4_dense"
-    peak = bf16_peak * NOMINAL_RATIO["fp4" if is_fp4 else "fp8"]
+    is_bf16 = args.workload == "grouped_bf16"
+    kind = "fp4" if is_fp4 else "bf16" if is_bf16 else "fp8"
+    peak = bf16_peak * NOMINAL_RATIO[kind]
     # the dominant launch: the GEMM of the step with the most flops
     dom = max(range(len(gemms)), key=lambda j: flops_of(gemms[j][0]))
     dom_g = gemms[dom][0]
@@ -464,6 +494,8 @@ def run_ours(args):
     value = ws * step_flops / (ms_per_step * 1e-3) / 1e12
     if args.workload.startswith("grouped_fp8"):
         kernel = "grouped_fp8_kernel"
+    elif is_bf16:
+        kernel = "grouped_bf16_kernel"
     else:
         kernel = "mx_gemm_2sm_kernel" if args.dense_variant in (0, 3) else "mx_gemm_kernel"
     line = {
@@ -477,8 +509,10 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "mxfp4(e2m1)+e8m0->f32acc" if is_fp4 else "mxfp8(e4m3/e5m2)+e8m0->f32acc",
-        "data": "synthetic (seeded N(0,1), MX-quantised)",
+        "dtype": {"fp4": "mxfp4(e2m1)+e8m0->f32acc", "bf16": "bf16->f32acc",
+                  "fp8": "mxfp8(e4m3/e5m2)+e8m0->f32acc"}[kind],
+        "data": "synthetic (seeded N(0,1) truncated to BF16)" if is_bf16
+                else "synthetic (seeded N(0,1), MX-quantised)",
         "config": {"workload": args.workload + ": " + WORKLOAD_TEXT[args.workload],
                    "l2": "flushed before every GEMM by a 256 MiB write outside the timed events",
                    "parallelism": f"replicas x{ws}",
@@ -489,21 +523,21 @@ def run_ours(args):
                      "launch": describe(dom_g),
                      "achieved": round(achieved, 1),
                      "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "peak_source": f"{peak_src} bf16 dense x nominal "
-                                    f"{'fp4' if is_fp4 else 'fp8'}/bf16 ratio, burst",
+                     "peak_source": f"{peak_src} bf16 dense, burst" if is_bf16 else
+                                    f"{peak_src} bf16 dense x nominal {kind}/bf16 ratio, burst",
                      "traffic": recorded_traffic(args.workload),
                      "all_gemm_kernels_achieved": round(step_achieved, 1)},
         "e2e": None if args.no_e2e else {
             "value": round(ws * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "api": "mx_gemm / grouped_fp8_gemm with host->device copies of every input "
+            "api": "mx_gemm / grouped_fp8_gemm / grouped_bf16_gemm with host->device copies of every input "
                    "and device->host copy of D inside the timed region; the copies run on two "
                    "copy streams, overlapping the neighbouring GEMMs' compute"},
         "gpu_launches": int(n_launch),
         "clocks": clk.summary(),
         "wall_s_timed": round(wall, 3),
     }
-    if args.workload.startswith("grouped_fp8"):
+    if args.workload.startswith("grouped"):
         # each shape against its own bound: compute at the FP8 peak or its algorithmic
         # bytes at the measured HBM copy bandwidth, whichever takes longer
         _, hbm_peak, _ = measured_peaks()
@@ -817,12 +851,16 @@ def time_oracle_sample(spec, rows_per_gemm: int, inputs_cache: dict, nthreads: i
         if i not in inputs_cache:
             inputs_cache[i] = make_inputs(dict(g))
         c = inputs_cache[i]
-        if g["kind"] == "grouped":
+        if g["kind"].startswith("grouped"):
             T = int(np.asarray(c["m_sizes"]).sum())
             rows = np.random.default_rng([8, i]).choice(T, size=min(rows_per_gemm, T), replace=False)
             t0 = time.perf_counter()
-            oracle.grouped_fp8_gemm(c["X"], c["sX"], c["W"], c["sW"], c["m_sizes"], g["N"], g["K"],
-                                    rows=np.sort(rows), nthreads=nthreads)
+            if g["kind"] == "grouped_bf16":
+                oracle.grouped_bf16_gemm(c["X"], c["W"], c["m_sizes"], g["N"], g["K"],
+                                         rows=np.sort(rows), nthreads=nthreads)
+            else:
+                oracle.grouped_fp8_gemm(c["X"], c["sX"], c["W"], c["sW"], c["m_sizes"], g["N"],
+                                        g["K"], rows=np.sort(rows), nthreads=nthreads)
             secs += time.perf_counter() - t0
             flops += 2.0 * len(rows) * g["N"] * g["K"]
         else:
@@ -876,7 +914,8 @@ def run_reference(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded N(0,1), MX-quantised)",
+        "data": "synthetic (seeded N(0,1) truncated to BF16)" if args.workload == "grouped_bf16"
+                else "synthetic (seeded N(0,1), MX-quantised)",
         "config": {"workload": args.workload + ": " + WORKLOAD_TEXT[args.workload],
                    "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cores, "kind": "oracle",
@@ -895,7 +934,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mxfp8_dense",
                     choices=["mxfp8_dense", "mxfp8_bias_gelu", "mxfp8_256", "mxfp4_dense",
-                             "linear_triple", "grouped_fp8", "grouped_fp8_packed", "quantize"])
+                             "linear_triple", "grouped_fp8", "grouped_fp8_packed", "grouped_bf16",
+                             "quantize"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
     ap.add_argument("--grouped-width", type=int, default=0, choices=[0, 128, 256],

@@ -27,6 +27,7 @@ import torch
 from .build import LIB_PATH, build
 
 __all__ = ["mx_gemm", "mx_gemm_tiled", "mx_gemm_noalloc", "grouped_fp8_gemm", "grouped_fp8_pack_weights",
+           "grouped_bf16_gemm",
            "mx_scale_relayout",
            "mx_quantize", "fp8_group_quantize", "fp8_block_quantize", "autotune_configure",
            "autotune_lookup",
@@ -71,6 +72,7 @@ def load(path: str | None = None):
         lib.grouped_fp8_gemm.argtypes = [p, p, p, p, p, p, i64, i32, i64, i64, p]
         lib.grouped_fp8_gemm_packed.argtypes = [p, p, p, p, p, p, i64, i32, i64, i64, p]
         lib.grouped_fp8_pack_weights.argtypes = [p, i64, i64, i64, p, p]
+        lib.grouped_bf16_gemm.argtypes = [p, p, p, p, i64, i32, i64, i64, p]
         lib.mx_scale_relayout.argtypes = [p, i64, i64, i32, p, p]
         lib.mx_scale_tiled_bytes.argtypes = [i64, i64, i32]
         lib.mx_scale_tiled_bytes.restype = i64
@@ -214,6 +216,26 @@ def grouped_fp8_gemm(X, sX, W, sW, m_sizes, out=None, stream=None, packed=False)
               _ptr(W), _ptr(sW), _ptr(out) if total_M else None,
               _ptr(m_sizes), total_M, G, N, K, _stream(stream)),
            "grouped_fp8_gemm_packed" if packed else "grouped_fp8_gemm")
+    return out
+
+
+def grouped_bf16_gemm(X, W, m_sizes, out=None, stream=None):
+    """Grouped BF16 GEMM (see ``grouped_bf16_gemm`` in bsmma.h): D[r] = X[r] . W[g(r)]^T.
+
+    X [total_M, K] and W [G, N, K] BF16 tensors (or int16/uint16 holding BF16 bit
+    patterns), m_sizes int64 [G] on the device; returns D [total_M, N] BF16.
+    """
+    total_M, K = X.shape
+    G, N, _ = W.shape
+    if m_sizes.dtype != torch.int64 or m_sizes.numel() != G or m_sizes.dim() != 1:
+        raise ValueError("m_sizes must be a 1-D int64 tensor of length G")
+    if X.element_size() != 2 or W.element_size() != 2:
+        raise ValueError("X and W must hold 16-bit BF16 values")
+    if out is None:
+        out = torch.empty((total_M, N), dtype=torch.bfloat16, device=W.device)
+    _check(load().grouped_bf16_gemm(_ptr(X) if total_M else None, _ptr(W),
+                                    _ptr(out) if total_M else None, _ptr(m_sizes), total_M, G,
+                                    N, K, _stream(stream)), "grouped_bf16_gemm")
     return out
 
 

@@ -12,7 +12,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libbsmma.so")
 SOURCES = ["api.cu", "relayout.cu", "mx_gemm.cu", "grouped_gemm.cu", "noalloc.cu",
-           "mx_gemm_2sm.cu", "quantize.cu", "autotune.cu"]
+           "mx_gemm_2sm.cu", "quantize.cu", "autotune.cu", "grouped_bf16.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 

@@ -462,6 +462,22 @@ bsmma_status grouped_fp8_pack_weights(const uint8_t* W, int64_t G, int64_t N, in
   return launch_pack_weights(W, G, N, K, W_packed, reinterpret_cast<cudaStream_t>(stream));
 }
 
+bsmma_status grouped_bf16_gemm(const void* X, const void* W, void* D, const int64_t* m_sizes,
+                               int64_t total_M, int G, int64_t N, int64_t K,
+                               bsmma_stream stream) {
+  if (G < 1 || G > 64 || total_M < 0 || N <= 0 || K <= 0) return BSMMA_ERR_INVALID_ARG;
+  if (N % 8 != 0 || K % 8 != 0) return BSMMA_ERR_INVALID_ARG;
+  if (!W || !m_sizes) return BSMMA_ERR_INVALID_ARG;
+  if (total_M > 0 && (!X || !D)) return BSMMA_ERR_INVALID_ARG;
+  if (!aligned16(W) || (total_M > 0 && (!aligned16(X) || !aligned16(D))) ||
+      (reinterpret_cast<uintptr_t>(m_sizes) & 7u) != 0)
+    return BSMMA_ERR_MISALIGNED;
+  if (total_M >= INT32_MAX || static_cast<int64_t>(G) * N >= INT32_MAX || 2 * K > kMaxStride)
+    return BSMMA_ERR_INVALID_ARG;
+  return launch_grouped_bf16(X, W, D, m_sizes, total_M, G, N, K,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
 bsmma_status mx_quantize(const void* x, bsmma_dtype x_dtype, int64_t rows, int64_t cols,
                          bsmma_fmt fmt, int colwise, uint8_t* codes, uint8_t* scales,
                          bsmma_stream stream) {

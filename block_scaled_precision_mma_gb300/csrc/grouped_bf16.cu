@@ -1,0 +1,336 @@
+// grouped_bf16.cu -- grouped BF16 GEMM for sm_103a.
+//
+// X [total_M][K] BF16, W [G][N][K] BF16, groups of uneven or zero size (m_sizes on the
+// device), BF16 output D[r] = X[r] . W[g(r)]^T with FP32 accumulation ("PyTorch on AMD
+// GPUs gains a FlyDSL backend", Interpretation: grouped GEMM over uneven and empty
+// expert groups, the BF16 grouped-GEMM cases).  No scales: the tensor core accumulates
+// the whole of K in tensor memory.
+//
+// One persistent, warp-specialised launch, grid = #SMs at most, tiles of 128 rows x BN
+// columns in the grouped tile order (grouped_sched.cuh):
+//   warp 0      TMA producer: 128 x 64 X and BN x 64 W tiles (128-byte rows, 128-byte
+//               swizzle) into a ring of stages;
+//   warp 1      lane 0 issues kind::f16 MMAs (M=128, N=BN, K=16; four per stage) into
+//               one of two FP32 accumulators in tensor memory, so that a tile's output
+//               stage overlaps the next tile's main loop;
+//   warps 2-9   output stage: two warps per 32-lane quarter, each reading half of the
+//               tile's columns with tcgen05.ld, rounding to BF16 (nearest-even) and
+//               storing 16 bytes per lane, only rows of the tile's group and columns
+//               below N.
+// K need only be a multiple of 8 (16-byte rows): the last stage's columns past K are
+// filled with zeros by the tensor copy.  N need only be a multiple of 8: columns of the
+// last column block past N are computed from whatever rows the copy returns (the next
+// group's weights, or zeros past the tensor) and never stored.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "grouped_sched.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace bsmma {
+namespace {
+
+using grouped::find_group;
+using grouped::GroupTable;
+using grouped::kBM;
+using grouped::tile_coords;
+constexpr int kBKBytes = 128;                 // one 128-byte swizzle row: 64 BF16 of K
+constexpr int kATileBytes = kBM * kBKBytes;   // 16 KB
+
+// Instruction descriptor of kind::f16: FP32 accumulator, BF16 A and B, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D(tmem) (+)= A(smem) x B(smem), BF16 operands, FP32 accumulation.
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+template <int BN>
+struct BCfg {
+  static constexpr int kOutWarps = 8;
+  static constexpr int kOutWarp0 = 2;
+  static constexpr int kThreads = (kOutWarp0 + kOutWarps) * 32;
+  static constexpr int kCols = BN / 2;             // accumulator columns per output warp
+  static constexpr int kBTileBytes = BN * kBKBytes;
+  static constexpr int kStageBytes = kATileBytes + kBTileBytes;
+  static constexpr int kStages = BN == 128 ? 6 : 4;
+  static constexpr uint32_t kTmemCols = 2 * BN;    // two accumulators
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 2048;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct Bf16Params {
+  __nv_bfloat16* D;
+  const int64_t* m_sizes;
+  int64_t total_M, N;
+  int G, num_n_tiles, num_kb;
+  uint32_t idesc;
+  int* status;
+  uint64_t limit_ns;
+};
+
+template <int BN>
+__global__ void __launch_bounds__(BCfg<BN>::kThreads, 1)
+    grouped_bf16_kernel(const __grid_constant__ CUtensorMap tmX,
+                        const __grid_constant__ CUtensorMap tmW, const Bf16Params p) {
+  using C = BCfg<BN>;
+  constexpr int kStages = C::kStages, kStageBytes = C::kStageBytes, kOutWarps = C::kOutWarps;
+  constexpr uint32_t kTmemCols = C::kTmemCols;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;    // [2]
+  uint64_t* acc_empty = acc_full + 2;      // [2]
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  GroupTable& gt = *reinterpret_cast<GroupTable*>(reinterpret_cast<uint8_t*>(full) + 512);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.G;
+  grouped::build_group_table(gt, p.m_sizes, G, p.total_M, p.status, [&] {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], kOutWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmX);
+    prefetch_tmap(&tmW);
+  });
+  if (gt.bad) return;   // uniform across the block; nothing allocated, nothing written
+
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int NT = p.num_n_tiles, KB = p.num_kb;
+  const int total_tiles = gt.tile_start[G] * NT;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // -------------------------------------------------------------- producer
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_parity = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        int mt, nt;
+        tile_coords(t, NT, gt.tile_start[G], mt, nt);
+        const int g = find_group(gt, G, mt);
+        const int row0 = static_cast<int>(gt.start[g] + static_cast<int64_t>(mt - gt.tile_start[g]) * kBM);
+        const int wrow0 = static_cast<int>(static_cast<int64_t>(g) * p.N + static_cast<int64_t>(nt) * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.limit_ns, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          uint8_t* dst = ring + stage * kStageBytes;
+          tma_load_2d(&tmX, &full[stage], dst, kb * kBKBytes, row0);
+          tma_load_2d(&tmW, &full[stage], dst + kATileBytes, kb * kBKBytes, wrow0);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // no copy may land after the block has finished
+      for (int s = 0; s < kStages; ++s)
+        if (armed & (1u << s)) {
+          volatile int no_abort = 0;
+          mbar_wait(&full[s], (armed_parity >> s) & 1u, p.limit_ns / 4 + 1, &no_abort, nullptr);
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------------------------------------------------------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0, tcount = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++tcount) {
+        const uint32_t buf = tcount & 1;
+        if (!mbar_wait(&acc_empty[buf], ((tcount >> 1) & 1) ^ 1, p.limit_ns, abort_flag,
+                       p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + buf * BN;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&full[stage], phase, p.limit_ns, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(ring + stage * kStageBytes);
+          const uint32_t b_base = a_base + kATileBytes;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            mma_bf16(d, make_sdesc(a_base + j * 32, 16, 1024, kSwizzle128B),
+                     make_sdesc(b_base + j * 32, 16, 1024, kSwizzle128B), p.idesc,
+                     (kb | j) != 0);
+          tc_commit(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[buf]);
+      }
+      tc_commit(drain);
+      volatile int no_abort = 0;
+      mbar_wait(drain, 0, p.limit_ns, &no_abort, nullptr);
+    }
+  } else {
+    // ---------------------------------------------------------------- output stage
+    constexpr int kCols = C::kCols, kPieces = kCols / 32;
+    const int q = warp & 3;                            // tensor-memory lane quarter
+    const int h = (warp - C::kOutWarp0) >> 2;          // which half of the tile's columns
+    uint32_t tcount = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++tcount) {
+      int mt, nt;
+      tile_coords(t, NT, gt.tile_start[G], mt, nt);
+      const int g = find_group(gt, G, mt);
+      const int64_t l = static_cast<int64_t>(mt - gt.tile_start[g]) * kBM + q * 32 + lane;
+      const bool valid = l < gt.size[g];
+      const uint32_t buf = tcount & 1;
+      if (!mbar_wait(&acc_full[buf], (tcount >> 1) & 1, p.limit_ns, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + h * kCols;
+      // the warp's whole slice in one round trip; the accumulator is released before
+      // the stores
+      uint32_t r[kPieces][32];
+#pragma unroll
+      for (int c = 0; c < kPieces; ++c) tmem_ld32(taddr + c * 32, r[c]);
+      tmem_ld_wait(r[0]);
+#pragma unroll
+      for (int c = 1; c < kPieces; ++c) reg_fence(r[c]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      if (valid) {
+        const int64_t col0 = static_cast<int64_t>(nt) * BN + h * kCols;
+        __nv_bfloat16* out = p.D + (gt.start[g] + l) * p.N + col0;
+#pragma unroll
+        for (int c = 0; c < kPieces; ++c)
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            if (col0 + c * 32 + v * 8 < p.N) {
+              const uint32_t* x = &r[c][v * 8];
+              st_global_v4_cs(out + c * 32 + v * 8,
+                              pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                              pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                              pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                              pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
+            }
+          }
+      }
+    }
+  }
+  // every MMA and tensor-memory read has been issued and fenced
+  tc_fence_before();
+  named_barrier_sync(1, C::kThreads);
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int BN>
+bsmma_status launch_bf16_bn(const CUtensorMap& tx, const CUtensorMap& tw, Bf16Params p,
+                            int64_t total_M, int G, int sm_count, cudaStream_t stream) {
+  using C = BCfg<BN>;
+  p.num_n_tiles = static_cast<int>((p.N + BN - 1) / BN);
+  p.idesc = idesc_bf16(kBM, BN);
+  const int64_t bound = ((total_M + kBM - 1) / kBM + G) * p.num_n_tiles;
+  int64_t grid = bound < sm_count ? bound : sm_count;
+  if (grid < 1) grid = 1;
+  static bool attr_set = false;   // benign race: setting the attribute twice is harmless
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(grouped_bf16_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
+      return BSMMA_ERR_CUDA;
+    attr_set = true;
+  }
+  grouped_bf16_kernel<BN><<<static_cast<int>(grid), C::kThreads, C::kSmemBytes, stream>>>(tx, tw, p);
+  count_launches(1);
+  return cuda_ok(cudaGetLastError());
+}
+
+bsmma_status launch_bf16_width(const void* X, const void* W, void* D, const int64_t* m_sizes,
+                               int64_t total_M, int G, int64_t N, int64_t K, int bn,
+                               const DeviceInfo* dev, cudaStream_t stream) {
+  CUtensorMap tx, tw;
+  // BF16 rows as bytes: a 128-byte box is 64 BF16 of K, the same shared-memory image.
+  // With no rows there is no X tile to load; W's address stands in for the map.
+  bsmma_status st = encode_tmap_u8(&tx, total_M > 0 ? X : W, K * 2, total_M > 0 ? total_M : 1,
+                                   K * 2, kBKBytes, kBM);
+  if (st != BSMMA_OK) return st;
+  st = encode_tmap_u8(&tw, W, K * 2, static_cast<uint64_t>(G) * N, K * 2, kBKBytes, bn);
+  if (st != BSMMA_OK) return st;
+  Bf16Params p;
+  p.D = static_cast<__nv_bfloat16*>(D);
+  p.m_sizes = m_sizes;
+  p.total_M = total_M;
+  p.N = N;
+  p.G = G;
+  p.num_kb = static_cast<int>((K + 63) / 64);
+  p.status = dev->status;
+  p.limit_ns = wait_limit_ns();
+  if (bn == 256) return launch_bf16_bn<256>(tx, tw, p, total_M, G, dev->sm_count, stream);
+  return launch_bf16_bn<128>(tx, tw, p, total_M, G, dev->sm_count, stream);
+}
+
+}  // namespace
+
+bsmma_status launch_grouped_bf16(const void* X, const void* W, void* D, const int64_t* m_sizes,
+                                 int64_t total_M, int G, int64_t N, int64_t K,
+                                 cudaStream_t stream) {
+  bsmma_status st;
+  const DeviceInfo* dev = current_device(&st);
+  if (!dev) return st;
+  static_assert(sizeof(GroupTable) + 512 <= 2048, "group table fits its shared-memory slot");
+  // Wide tiles halve the MMA issue count and the reads of X per flop; they lose only when
+  // too few tiles remain to keep every SM streaming W (row blocks estimated from total_M:
+  // each group adds on average half a partial block).
+  const int64_t row_blocks_est = (total_M + kBM - 1) / kBM + G / 2;
+  const int forced = grouped_tile_width();
+  int bn = (N > 128 && row_blocks_est * ((N + 255) / 256) * 2 >= dev->sm_count) ? 256 : 128;
+  if (forced == 128 || forced == 256) bn = forced;
+  if (forced == 0 && N > 128) {
+    // opt-in autotuning per (nextPow2(total_M), N, K, G)
+    const std::string key = "grouped_bf16 " + std::to_string(next_pow2(total_M)) + " " +
+                            std::to_string(N) + " " + std::to_string(K) + " " + std::to_string(G);
+    bn = autotune_pick(key, {256, 128}, bn, stream, [&](int c) {
+      return launch_bf16_width(X, W, D, m_sizes, total_M, G, N, K, c, dev, stream);
+    });
+  }
+  return launch_bf16_width(X, W, D, m_sizes, total_M, G, N, K, bn, dev, stream);
+}
+
+}  // namespace bsmma

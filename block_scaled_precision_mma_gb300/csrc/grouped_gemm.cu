@@ -27,13 +27,17 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "grouped_sched.cuh"
 #include "ptx.cuh"
 
 namespace bsmma {
 namespace {
 
-constexpr int kBM = 128, kBK = 128;
-constexpr int kMaxG = 64;
+using grouped::find_group;
+using grouped::GroupTable;
+using grouped::kBM;
+using grouped::tile_coords;
+constexpr int kBK = 128;
 constexpr int kATileBytes = kBM * kBK;
 
 // Tile 128 x BN; each of the 8 fold warps owns one 32-lane quarter x BN/2 columns.
@@ -72,37 +76,6 @@ struct GroupedParams {
   uint64_t limit_ns;
 };
 
-struct GroupTable {
-  int64_t start[kMaxG + 1];   // first row of each group
-  int64_t size[kMaxG];
-  int tile_start[kMaxG + 1];  // first 128-row block id of each group
-  int bad;
-};
-
-// Tile t -> (128-row block mt, column block nt).  Tiles are walked in bands of kBandRows
-// row blocks: within a band the row block varies fastest, so the CTAs resident at one
-// time share a few weight column blocks and a band's rows of X, both of which stay in
-// L2 while the band is walked along N (row-fastest over all rows re-read every group's
-// whole weight matrix from DRAM for every few row blocks).
-constexpr int kBandRows = 16;
-__device__ __forceinline__ void tile_coords(int t, int NT, int rows, int& mt, int& nt) {
-  const int per_band = kBandRows * NT;
-  const int b = t / per_band;
-  const int r0 = b * kBandRows;
-  const int h = rows - r0 < kBandRows ? rows - r0 : kBandRows;
-  const int v = t - b * per_band;
-  mt = r0 + v % h;
-  nt = v / h;
-}
-
-// Group owning 128-row block `mt` (tile_start is non-decreasing; empty groups own none).
-__device__ __forceinline__ int find_group(const GroupTable& gt, int G, int mt) {
-  int g = 0;
-  for (int i = 1; i < G; ++i)
-    if (gt.tile_start[i] <= mt) g = i;
-  return g;
-}
-
 // 12 warps (three warpgroups) share an SM's four register-file quarters (16384
 // registers each) three to a quarter, so a thread launches with at most
 // 16384 / (3 * 32) = 170 registers (168 allocated); the warpgroups then rebalance.
@@ -136,26 +109,7 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G;
-  if (threadIdx.x < G) gt.size[threadIdx.x] = p.m_sizes[threadIdx.x];
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int64_t row = 0;
-    int tiles = 0, bad = 0;
-    for (int g = 0; g < G; ++g) {
-      const int64_t m = gt.size[g];
-      if (m < 0 || m > p.total_M) bad = 1;
-      gt.start[g] = row;
-      gt.tile_start[g] = tiles;
-      if (!bad) {
-        row += m;
-        tiles += static_cast<int>((m + kBM - 1) / kBM);
-      }
-    }
-    if (row != p.total_M) bad = 1;
-    gt.start[G] = row;
-    gt.tile_start[G] = tiles;
-    gt.bad = bad;
-    if (bad && blockIdx.x == 0) report_status(p.status, kDevBadMSizes);
+  grouped::build_group_table(gt, p.m_sizes, G, p.total_M, p.status, [&] {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
@@ -169,8 +123,7 @@ __global__ void __launch_bounds__(384, 1)
     fence_mbar_init();
     prefetch_tmap(&tmX);
     prefetch_tmap(&tmW);
-  }
-  __syncthreads();
+  });
   if (gt.bad) return;   // uniform across the block; nothing allocated, nothing written
 
   if (warp == 1) {

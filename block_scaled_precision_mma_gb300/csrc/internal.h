@@ -78,6 +78,9 @@ bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B
 bsmma_status launch_grouped(const uint8_t* X, const float* sX, const uint8_t* W, const float* sW,
                             void* D, const int64_t* m_sizes, int64_t total_M, int G, int64_t N,
                             int64_t K, cudaStream_t stream, bool packed = false);
+bsmma_status launch_grouped_bf16(const void* X, const void* W, void* D, const int64_t* m_sizes,
+                                 int64_t total_M, int G, int64_t N, int64_t K,
+                                 cudaStream_t stream);
 bsmma_status launch_pack_weights(const uint8_t* W, int64_t G, int64_t N, int64_t K, uint8_t* Wp,
                                  cudaStream_t stream);
 

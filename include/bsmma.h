@@ -195,6 +195,29 @@ bsmma_status grouped_fp8_gemm_packed(const uint8_t* A, const float* sA, const ui
                                      bsmma_stream stream);
 
 /*
+ * grouped_bf16_gemm -- grouped BF16 GEMM: for row r of group g,
+ *   D[r][n] = sum_k X[r][k] * W[g][n][k]
+ * with BF16 operands, FP32 accumulation and BF16 output (round to nearest even), over
+ * groups of uneven or zero size.  Source: "PyTorch on AMD GPUs gains a FlyDSL backend",
+ * Interpretation: grouped GEMM that tolerates uneven and empty expert groups, measured
+ * on BF16 grouped-GEMM cases (F.grouped_mm).  No scales.
+ *   X        [total_M][K] BF16, row-major, device.
+ *   W        [G][N][K] BF16 (one [N][K] matrix per group, K contiguous), device.
+ *   D        [total_M][N] BF16, row-major, device; every row of every group written.
+ *   m_sizes  [G] int64, device (read by the kernel: no host synchronisation); rows of
+ *            group g are the m_sizes[g] rows after those of groups 0..g-1.
+ * Preconditions: 1 <= G <= 64, total_M >= 0, N > 0 and K > 0 multiples of 8 (16-byte
+ * rows), 16-byte-aligned X, W and D, 8-byte-aligned m_sizes, total_M and G*N below
+ * 2^31.  BSMMA_ERR_INVALID_ARG / BSMMA_ERR_MISALIGNED otherwise, with nothing launched.
+ * m_sizes that has a negative entry or does not sum to total_M is found on the device:
+ * nothing is written and BSMMA_DEV_BAD_MSIZES is latched (bsmma_device_status).  One
+ * launch; the caller owns every buffer; asynchronous on `stream`.
+ */
+bsmma_status grouped_bf16_gemm(const void* X, const void* W, void* D, const int64_t* m_sizes,
+                               int64_t total_M, int G, int64_t N, int64_t K,
+                               bsmma_stream stream);
+
+/*
  * mx_scale_relayout -- rearranges plain E8M0 scales s_plain [rows][kblocks] into the
  * tiled layout the GEMM kernels copy into tensor memory (128 lanes x 32 bytes per
  * copy).  Source: "[gfx1250] Add MXFP4 GEMM support to FlyDSL backend", Description

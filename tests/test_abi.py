@@ -31,7 +31,7 @@ def test_header_declares_entry_points():
     names = declared_functions()
     for n in ("mx_gemm", "mx_gemm_tiled", "grouped_fp8_gemm", "mx_scale_relayout",
               "mx_scale_tiled_bytes", "bsmma_device_status", "bsmma_status_string",
-              "mx_quantize", "fp8_group_quantize", "fp8_block_quantize"):
+              "mx_quantize", "fp8_group_quantize", "fp8_block_quantize", "grouped_bf16_gemm"):
         assert n in names
 
 
@@ -97,6 +97,26 @@ def test_dense_validation(lib, args, expect):
 ])
 def test_grouped_validation(lib, args, expect):
     assert lib.grouped_fp8_gemm(*args, None) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    # (X, W, D, m_sizes, total_M, G, N, K)
+    ((FAKE, FAKE, FAKE, FAKE, 256, 8, 100, 256), 1),      # N % 8
+    ((FAKE, FAKE, FAKE, FAKE, 256, 8, 256, 36), 1),       # K % 8
+    ((FAKE, FAKE, FAKE, FAKE, 256, 0, 256, 256), 1),      # G = 0
+    ((FAKE, FAKE, FAKE, FAKE, 256, 65, 256, 256), 1),     # G > 64
+    ((FAKE, FAKE, FAKE, FAKE, -1, 8, 256, 256), 1),       # negative total_M
+    ((FAKE, FAKE, FAKE, FAKE, 256, 8, 0, 256), 1),        # N = 0
+    ((FAKE, FAKE, FAKE, None, 256, 8, 256, 256), 1),      # null m_sizes
+    ((None, FAKE, FAKE, FAKE, 256, 8, 256, 256), 1),      # null X with rows
+    ((FAKE, ODD, FAKE, FAKE, 256, 8, 256, 256), 3),       # W misaligned
+    ((FAKE, FAKE, ODD, FAKE, 256, 8, 256, 256), 3),       # D misaligned
+    ((FAKE, FAKE, FAKE, FAKE + 4, 256, 8, 256, 256), 3),  # m_sizes not 8-aligned
+    ((FAKE, FAKE, FAKE, FAKE, 1 << 31, 8, 256, 256), 1),  # total_M past 32-bit rows
+    ((FAKE, FAKE, FAKE, FAKE, 256, 64, 1 << 26, 256), 1), # G*N past 32-bit rows
+])
+def test_grouped_bf16_validation(lib, args, expect):
+    assert lib.grouped_bf16_gemm(*args, None) == expect
 
 
 def test_relayout_validation(lib):

@@ -99,6 +99,7 @@ def load(path: str | None = None):
                      "mx_scale_relayout",
                      "bsmma_reserve_workspace", "bsmma_device_status", "bsmma_set_wait_limit_ns",
                      "bsmma_set_dense_variant", "bsmma_set_grouped_tile_width",
+                     "grouped_bf16_gemm",
                      "bsmma_probe_wait_timeout", "mx_quantize", "fp8_group_quantize",
                      "fp8_block_quantize", "mx_gemm_bias_act", "mx_gemm_tiled_bias_act",
                      "bsmma_autotune_configure"):

@@ -247,7 +247,7 @@ bsmma_status split_workspace(cudaStream_t stream, float** part, int** arrivals) 
   if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return BSMMA_ERR_CUDA;
   if (cap != cudaStreamCaptureStatusNone) return BSMMA_ERR_WORKSPACE;
   const int64_t sms = dev->sm_count;
-  const int64_t counter_bytes = align_up(sms * 4, 256);
+  const int64_t counter_bytes = align_up(sms * 8 * 4, 256);
   const int64_t bytes = counter_bytes + 2 * sms * 128 * 256 * 4;
   void* p = nullptr;
   if (cudaMalloc(&p, static_cast<size_t>(bytes)) != cudaSuccess) return BSMMA_ERR_CUDA;

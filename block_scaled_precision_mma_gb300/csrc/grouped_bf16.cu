@@ -220,34 +220,37 @@ __global__ void __launch_bounds__(BCfg<BN>::kThreads, 1)
       const uint32_t buf = tcount & 1;
       if (!mbar_wait(&acc_full[buf], (tcount >> 1) & 1, p.limit_ns, abort_flag, p.status)) break;
       tc_fence_after();
+      // 32-column pieces of 32 lanes x 32 values (tcgen05.ld.32x32b), two in flight; the
+      // accumulator is released after the warp's last load
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + h * kCols;
-      // the warp's whole slice in one round trip; the accumulator is released before
-      // the stores
-      uint32_t r[kPieces][32];
+      const int64_t col0 = static_cast<int64_t>(nt) * BN + h * kCols;
+      __nv_bfloat16* out = p.D + (gt.start[g] + l) * p.N + col0;
+      auto store_piece = [&](int c, const uint32_t* x) {
 #pragma unroll
-      for (int c = 0; c < kPieces; ++c) tmem_ld32(taddr + c * 32, r[c]);
-      tmem_ld_wait(r[0]);
+        for (int e = 0; e < 4; ++e)
+          if (col0 + c * 32 + e * 8 < p.N)
+            st_global_v4_cs(out + c * 32 + e * 8,
+                            pack_bf16x2(__uint_as_float(x[e * 8 + 0]), __uint_as_float(x[e * 8 + 1])),
+                            pack_bf16x2(__uint_as_float(x[e * 8 + 2]), __uint_as_float(x[e * 8 + 3])),
+                            pack_bf16x2(__uint_as_float(x[e * 8 + 4]), __uint_as_float(x[e * 8 + 5])),
+                            pack_bf16x2(__uint_as_float(x[e * 8 + 6]), __uint_as_float(x[e * 8 + 7])));
+      };
 #pragma unroll
-      for (int c = 1; c < kPieces; ++c) reg_fence(r[c]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
-      if (valid) {
-        const int64_t col0 = static_cast<int64_t>(nt) * BN + h * kCols;
-        __nv_bfloat16* out = p.D + (gt.start[g] + l) * p.N + col0;
-#pragma unroll
-        for (int c = 0; c < kPieces; ++c)
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            if (col0 + c * 32 + v * 8 < p.N) {
-              const uint32_t* x = &r[c][v * 8];
-              st_global_v4_cs(out + c * 32 + v * 8,
-                              pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
-                              pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
-                              pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
-                              pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
-            }
-          }
+      for (int c = 0; c < kPieces; c += 2) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(taddr + c * 32, ra);
+        tmem_ld32(taddr + (c + 1) * 32, rb);
+        tmem_ld_wait(ra);
+        reg_fence(rb);
+        if (c + 2 == kPieces) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        }
+        if (valid) {
+          store_piece(c, ra);
+          store_piece(c + 1, rb);
+        }
       }
     }
   }

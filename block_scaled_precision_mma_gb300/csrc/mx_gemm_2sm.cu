@@ -32,6 +32,7 @@
 #include "internal.h"
 #include "epilogue.cuh"
 #include "ptx.cuh"
+#include "stream_k.cuh"
 
 namespace bsmma {
 namespace {
@@ -153,76 +154,6 @@ constexpr int kMinGranules = 8;
 // k-stages of the unit's own MMA time.
 constexpr int kSplitCostStages = 40;
 
-// The clusters' share of the units: units [0, t_dp) whole and round robin; the P clusters
-// with a stream-K range share W granules (a granule: the stages one row-scale chunk
-// covers) of units [t_dp, units), gpu granules per unit.
-struct DSched {
-  int units, KS, gran, gpu, t_dp, P, W;
-};
-__device__ __forceinline__ DSched make_dsched(int units, int KS, int gran, int clusters,
-                                              bool can_split) {
-  DSched s;
-  s.units = units;
-  s.KS = KS;
-  s.gran = gran;
-  s.gpu = (KS + gran - 1) / gran;
-  s.t_dp = units;
-  s.P = 0;
-  s.W = 0;
-  const int rem = units % clusters;
-  // Worth it only when the split tail, rem / clusters of a unit's KS stages plus a fixed
-  // cost, beats the last wave's one unit: a split range pays for its own pipeline start
-  // and for writing and summing partial sums, about kSplitCostStages stages' time as
-  // measured (8192^3 FP8, KS 64, 36 leftover units of 76: 2.5% slower; 4096x4096x14336,
-  // KS 112, 28 of 76: 3.3% faster; FP4 8192^3, KS 32: 4.9% slower).
-  if (can_split && rem != 0 &&
-      static_cast<int64_t>(rem) * KS <= static_cast<int64_t>(clusters) * (KS - kSplitCostStages)) {
-    const int64_t W = static_cast<int64_t>(rem) * s.gpu;
-    int64_t P = W / kMinGranules;
-    if (P > clusters) P = clusters;
-    if (P > rem && W < INT32_MAX) {   // only when it puts more clusters to work
-      s.t_dp = units - rem;
-      s.P = static_cast<int>(P);
-      s.W = static_cast<int>(W);
-    }
-  }
-  return s;
-}
-__device__ __forceinline__ int dsk_begin(const DSched& s, int c) {
-  return static_cast<int>(static_cast<int64_t>(c) * s.W / s.P);
-}
-__device__ __forceinline__ int dsk_owner(const DSched& s, int it) {
-  return static_cast<int>((static_cast<int64_t>(it + 1) * s.P - 1) / s.W);
-}
-// Work item of a warp: unit u, stages [ks0, ks1).  The position (next whole unit, next
-// granule, end) lives in shared memory, one copy per warp, so it costs no registers.
-__device__ __forceinline__ void dwork_init(const DSched& s, volatile int* st, int c) {
-  st[0] = c;
-  st[1] = c < s.P ? dsk_begin(s, c) : 0;
-  st[2] = c < s.P ? dsk_begin(s, c + 1) : 0;
-}
-__device__ __forceinline__ bool dwork_next(const DSched& s, volatile int* st, int clusters, int& u,
-                                           int& ks0, int& ks1) {
-  const int dp = st[0];
-  if (dp < s.t_dp) {
-    u = dp;
-    ks0 = 0;
-    ks1 = s.KS;
-    st[0] = dp + clusters;
-    return true;
-  }
-  const int it = st[1], end = st[2];
-  if (it >= end) return false;
-  const int v = it / s.gpu;
-  const int g0 = it - v * s.gpu;
-  const int g1 = s.gpu - g0 <= end - it ? s.gpu : g0 + (end - it);
-  st[1] = it + (g1 - g0);
-  u = s.t_dp + v;
-  ks0 = g0 * s.gran;
-  ks1 = g1 * s.gran < s.KS ? g1 * s.gran : s.KS;
-  return true;
-}
-
 // Unit u -> (256-row unit row ur, 256-column tile nt), banded along N for L2 reuse.
 __device__ __forceinline__ void unit_tile2(const Pair2Params& p, int u, int& ur, int& nt) {
   const int per_band = kBandUnits * p.num_n_tiles;
@@ -261,8 +192,7 @@ __global__ void __maxnreg__(168)
   uint64_t* drain = acc_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* last_flag = abort_flag + 1;           // this CTA finishes the current split unit
-  DSched& sched = *reinterpret_cast<DSched*>(const_cast<int*>(abort_flag + 2));
+  DSched& sched = *reinterpret_cast<DSched*>(const_cast<int*>(abort_flag + 2));   // + 1 unused
   volatile int* work_state = abort_flag + 2 + (sizeof(DSched) + 3) / 4;   // [10 warps][4]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -278,8 +208,12 @@ __global__ void __maxnreg__(168)
     mbar_init(acc_empty, 2 * kEpiWarps);   // used in the leader: epilogues of both CTAs
     mbar_init(drain, 1);
     *abort_flag = 0;
+    // the split cost as measured (8192^3 FP8, KS 64, 36 leftover units of 76: 2.5% slower
+    // with splits; 4096x4096x14336, KS 112, 28 of 76: 3.3% faster; FP4 8192^3, KS 32:
+    // 4.9% slower)
     sched = make_dsched(p.num_unit_rows * p.num_n_tiles, p.num_k_stages, C::kStagesPerChunk,
-                        static_cast<int>(gridDim.x >> 1), p.part != nullptr);
+                        static_cast<int>(gridDim.x >> 1), p.part != nullptr, kSplitCostStages,
+                        kMinGranules);
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
@@ -514,8 +448,8 @@ __global__ void __maxnreg__(168)
       const int v = u - sched.t_dp;
       float4* const part = reinterpret_cast<float4*>(p.part) + (q * 2 + h) * (kChunks * 8 * 32) + lane;
       auto slot_of = [&](int c) -> float4* {
-        const int which = dsk_begin(sched, c) / sched.gpu == v ? 0 : 1;
-        return part + static_cast<uint32_t>((c * 2 + which) * 2 + static_cast<int>(rank)) * (128 * 256 / 4);
+        return part + static_cast<uint32_t>((c * 2 + dsk_slot(sched, c, v)) * 2 + static_cast<int>(rank)) *
+                          (128 * 256 / 4);
       };
       float4* mine = slot_of(cluster_id);
 #pragma unroll
@@ -525,22 +459,23 @@ __global__ void __maxnreg__(168)
           __stcg(mine + (c * 8 + j) * 32,
                  make_float4(__uint_as_float(r[c][4 * j]), __uint_as_float(r[c][4 * j + 1]),
                              __uint_as_float(r[c][4 * j + 2]), __uint_as_float(r[c][4 * j + 3])));
+      // each epilogue warp counts itself in on the unit's counter for its own rows and
+      // columns, and the warp that arrives last for that part adds the slots: no barrier
+      // between warps, so a warp that gives up on a wait blocks no other
       __threadfence();
-      named_barrier_sync(2, kEpiWarps * 32);
-      if (threadIdx.x == 64) {
-        const int nseg = dsk_owner(sched, (v + 1) * sched.gpu - 1) - dsk_owner(sched, v * sched.gpu) + 1;
-        const int arrived = atomicAdd(&p.arrivals[v * 2 + rank], 1) + 1;
-        const int last = arrived == nseg;
-        if (last) p.arrivals[v * 2 + rank] = 0;   // every contributor has counted itself in
-        *last_flag = last;
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) {
+        int* ctr = p.arrivals + (v * 2 + static_cast<int>(rank)) * kEpiWarps + (warp - 2);
+        const int nseg = dsk_last_worker(sched, v) - dsk_first_worker(sched, v) + 1;
+        last = atomicAdd(ctr, 1) + 1 == nseg;
+        if (last) *ctr = 0;   // every contributor has counted itself in
       }
-      named_barrier_sync(2, kEpiWarps * 32);
-      if (!*last_flag) continue;
+      if (!__shfl_sync(0xffffffffu, last, 0)) continue;
       __threadfence();
       // the last to arrive: every contributor's slot summed in stage order, a 32-column
       // piece at a time, and stored
-      const int c_lo = dsk_owner(sched, v * sched.gpu);
-      const int c_hi = dsk_owner(sched, (v + 1) * sched.gpu - 1);
+      const int c_lo = dsk_first_worker(sched, v), c_hi = dsk_last_worker(sched, v);
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) {
         uint32_t sum[32];

@@ -211,7 +211,7 @@ bsmma_status grouped_fp8_gemm_packed(const uint8_t* A, const float* sA, const ui
  * 2^31.  BSMMA_ERR_INVALID_ARG / BSMMA_ERR_MISALIGNED otherwise, with nothing launched.
  * m_sizes that has a negative entry or does not sum to total_M is found on the device:
  * nothing is written and BSMMA_DEV_BAD_MSIZES is latched (bsmma_device_status).  One
- * launch; the caller owns every buffer; asynchronous on `stream`.
+ * launch; the caller owns every buffer; asynchronous on `stream`; allocates nothing.
  */
 bsmma_status grouped_bf16_gemm(const void* X, const void* W, void* D, const int64_t* m_sizes,
                                int64_t total_M, int G, int64_t N, int64_t K,
@@ -383,10 +383,11 @@ bsmma_status bsmma_set_wait_limit_ns(int64_t ns);
  * testing control. */
 bsmma_status bsmma_set_dense_variant(int variant);
 
-/* Selects the grouped kernel's tile width for later grouped_fp8_gemm calls: 0
- * automatic (default: 256 when the wide tiles fill the GPU at least twice and N %
- * 256 == 0, else 128), 128 or 256 (used only when N % 256 == 0).  Same result;
- * a tuning and testing control. */
+/* Selects the grouped kernels' tile width for later grouped_fp8_gemm and
+ * grouped_bf16_gemm calls: 0 automatic (default: 256 when the wide tiles fill the GPU
+ * at least twice and, for grouped_fp8_gemm, N % 256 == 0; else 128), 128 or 256
+ * (grouped_fp8_gemm: used only when N % 256 == 0).  Same result; a tuning and testing
+ * control. */
 bsmma_status bsmma_set_grouped_tile_width(int width);
 
 /* Human-readable name of a status code (static storage). */

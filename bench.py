@@ -6,7 +6,8 @@ Default workload (one "step"): the dense MXFP8 NT GEMMs
 each one pass of the path: scale relayout of sA and sB, then the tcgen05 GEMM.
 Inputs are seeded N(0,1) values quantised per 32-wide K block (E8M0 scale
 2^(floor(log2 amax) - emax)), resident in HBM before timing.  L2 is flushed (256
-MiB write) before every GEMM, outside the timed events.
+MiB write) before every GEMM, outside the timed events; a 256 MiB read follows the write,
+so the flush's dirty lines are written back before the GEMM starts rather than during it.
 
 Other workloads (``--workload``): mxfp4_dense (8192^3 and 1024x14336x4096),
 grouped_fp8 (G=8, totM 128/1024/16384 x three (N,K)), grouped_bf16 (the same shapes
@@ -151,6 +152,19 @@ _TRIPLE = None
 
 
 # ----------------------------------------------------------------------------- helpers
+class L2Flush:
+    """Empties L2 of the step's inputs between timed GEMMs: a 256 MiB write (twice the
+    129 MB L2), then a 256 MiB read, which writes the first buffer's dirty lines back to
+    DRAM before the GEMM starts instead of during it, and leaves only clean lines behind."""
+
+    def __init__(self, torch, dev):
+        self.w = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(64 * 1024 * 1024, dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.max()
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -315,6 +329,8 @@ def run_ours(args):
     bs.set_grouped_tile_width(args.grouped_width)
     dev = torch.device("cuda", local)
     spec = workload_spec(args.workload)
+    if args.gemm is not None:
+        spec = [spec[args.gemm]]    # one GEMM of the step (profiling a single shape)
 
     gemms = []
     for g in spec:
@@ -354,7 +370,7 @@ def run_ours(args):
             g.setdefault("b", c["b_fmt"])
         host["D"] = torch.empty(t["D"].shape, dtype=torch.bfloat16).pin_memory()
         gemms.append((g, t, host))
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream()
     step_flops = sum(flops_of(g) for g, _, _ in gemms)
 
@@ -379,7 +395,7 @@ def run_ours(args):
 
     def step(events):
         for (g, t, _), ev in zip(gemms, events):
-            flush.zero_()
+            flush()
             one_gemm(g, t, ev)
 
     mk = lambda: [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in gemms]
@@ -513,8 +529,10 @@ def run_ours(args):
                   "fp8": "mxfp8(e4m3/e5m2)+e8m0->f32acc"}[kind],
         "data": "synthetic (seeded N(0,1) truncated to BF16)" if is_bf16
                 else "synthetic (seeded N(0,1), MX-quantised)",
-        "config": {"workload": args.workload + ": " + WORKLOAD_TEXT[args.workload],
-                   "l2": "flushed before every GEMM by a 256 MiB write outside the timed events",
+        "config": {"workload": args.workload + ": " + WORKLOAD_TEXT[args.workload]
+                   + ("" if args.gemm is None else f" -- only GEMM {args.gemm}: {describe(spec[0])}"),
+                   "l2": "flushed before every GEMM by a 256 MiB write, then a 256 MiB read (the "
+                         "write's dirty lines leave L2 before the GEMM), outside the timed events",
                    "parallelism": f"replicas x{ws}",
                    "dense_variant": args.dense_variant,
                    "grouped_width": args.grouped_width,
@@ -671,13 +689,13 @@ def run_quantize(args):
                         out=quant_outputs(torch, kind, shape, dev),
                         outh=quant_outputs(torch, kind, shape, dev, pinned=True),
                         bytes=quant_bytes(kind, shape)))
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream()
     step_bytes = sum(o["bytes"] for o in ops)
 
     def step(events):
         for o, ev in zip(ops, events):
-            flush.zero_()
+            flush()
             ev[0].record(stream)
             quant_call(bs, o["kind"], o["x"], o["out"], ms)
             ev[1].record(stream)
@@ -775,7 +793,8 @@ def run_quantize(args):
         "vs_baseline": None, "dtype": "bf16 in, e4m3 + e8m0/f32 scales out",
         "data": "synthetic (seeded N(0,1) as BF16)",
         "config": {"workload": "quantize: " + QUANT_TEXT,
-                   "l2": "flushed before every call by a 256 MiB write outside the timed events",
+                   "l2": "flushed before every call by a 256 MiB write, then a 256 MiB read (the "
+                         "write's dirty lines leave L2 before the call), outside the timed events",
                    "parallelism": f"replicas x{ws}",
                    "per_call_ms": {o["name"]: round(t, 4) for o, t in zip(ops, per_op_ms)},
                    "per_call_gbs": {o["name"]: round(o["bytes"] / (t * 1e-3) / 1e9, 1)
@@ -942,6 +961,9 @@ def main():
                     help="grouped tile width: 0 automatic, 128 or 256 (tuning only)")
     ap.add_argument("--dense-variant", type=int, default=0, choices=[0, 1, 3],
                     help="0 automatic, 1 single-CTA tiles, 3 SM-pair MMAs (tuning only)")
+    ap.add_argument("--gemm", type=int, default=None,
+                    help="run only this GEMM (index into the workload's list) in each step; "
+                         "for profiling one shape, not a bench line of the workload")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     args = ap.parse_args()

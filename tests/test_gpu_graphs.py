@@ -1,5 +1,5 @@
-"""CUDA-graph capture of mx_gemm, grouped_fp8_gemm and the three quantisers, and
-concurrent streams.  Each call is captured once, then replayed after new inputs (and, for
+"""CUDA-graph capture of mx_gemm, grouped_fp8_gemm, grouped_bf16_gemm and the three
+quantisers, and concurrent streams.  Each call is captured once, then replayed after new inputs (and, for
 the grouped calls, a different m_sizes split of the same total_M) have been copied into the
 captured buffers.  Every replay is compared with the oracle on the new inputs, so nothing
 may have been read on the host or baked into the graph at capture time.  A captured
@@ -122,6 +122,27 @@ def test_grouped_replays_with_new_split():
         assert bs.device_status() == 0
         ref = oracle.grouped_fp8_gemm(c["X"], c["sX"], c["W"], c["sW"], ms, N, K)
         assert_close(D.float().cpu().numpy(), ref, f"grouped replay {ms.tolist()}")
+
+
+def test_grouped_bf16_replays_with_new_split():
+    N, K = 264, 200
+    ms1 = np.array([100, 0, 200, 37, 0, 63], dtype=np.int64)
+    ms2 = np.array([0, 250, 1, 0, 149, 0], dtype=np.int64)          # same total_M = 400
+    c1 = synthetic.grouped_bf16_operands((93, 1), ms1, N, K)
+    c2 = synthetic.grouped_bf16_operands((93, 2), ms2, N, K)
+    as_dev = lambda c: [to_dev(c["X"].view(np.int16)), to_dev(c["W"].view(np.int16)),
+                        to_dev(c["m_sizes"])]
+    bufs = as_dev(c1)
+    D = torch.empty((400, N), dtype=torch.bfloat16, device="cuda")
+    g = capture(lambda: bs.grouped_bf16_gemm(*bufs, out=D))
+    for c, ms in ((c2, ms2), (c1, ms1)):
+        for b, h in zip(bufs, as_dev(c)):
+            b.copy_(h)
+        g.replay()
+        torch.cuda.synchronize()
+        assert bs.device_status() == 0
+        ref = oracle.grouped_bf16_gemm(c["X"], c["W"], ms, N, K)
+        assert_close(D.float().cpu().numpy(), ref, f"grouped bf16 replay {ms.tolist()}")
 
 
 def test_quantisers_replay_with_new_inputs():

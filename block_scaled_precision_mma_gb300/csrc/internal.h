@@ -58,8 +58,9 @@ bsmma_status launch_wide_relayout(const uint8_t* sa, int64_t rows_a, uint8_t* ou
 // The dense SM-pair kernel's split workspace for (current device, stream): arrival
 // counters [#SMs][8 epilogue warps] (zero between launches) and partial-sum slots
 // [2 * #SMs][128 x 256 FP32].
-// Allocated, its counters zeroed, by the first call on a stream, which must not be
-// captured (BSMMA_ERR_WORKSPACE otherwise); a fixed size per device.
+// Allocated, its counters zeroed, by the first call on a stream outside a capture
+// (inside one it returns BSMMA_ERR_WORKSPACE, and the caller runs without splits); a
+// fixed size per device.
 bsmma_status split_workspace(cudaStream_t stream, float** part, int** arrivals);
 
 // Launchers (arguments already validated by the entry points).

@@ -593,7 +593,12 @@ bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B
   p.arrivals = nullptr;
   if (may_split) {
     st = split_workspace(stream, &p.part, &p.arrivals);
-    if (st != BSMMA_OK) return st;
+    if (st == BSMMA_ERR_WORKSPACE) {   // captured on a stream without one: no unit is split
+      p.part = nullptr;
+      p.arrivals = nullptr;
+    } else if (st != BSMMA_OK) {
+      return st;
+    }
   }
   p.D = static_cast<__nv_bfloat16*>(D);
   p.epi.bias = static_cast<const __nv_bfloat16*>(bias);

@@ -97,8 +97,9 @@ typedef enum { BSMMA_SCALES_A = 0, BSMMA_SCALES_B = 1 } bsmma_scale_role;
  * a unit adds the others' FP32 partial sums, in K order (the result does not depend on
  * which pair finishes last).  The partial sums live in a second per-(device, stream)
  * workspace of fixed size (two 128 KB slots per SM), allocated, its counters zeroed,
- * by the stream's first dense call; that first call must not be captured (it returns
- * BSMMA_ERR_WORKSPACE then; bsmma_reserve_workspace allocates it too).
+ * by the stream's first dense call outside a graph capture (bsmma_reserve_workspace
+ * allocates it too).  A call captured on a stream that has none splits no unit: it
+ * computes the same result, its split units' last bits rounded as unsplit ones are.
  * Two kernel launches per call (relayout, GEMM).
  */
 bsmma_status mx_gemm(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
@@ -111,7 +112,8 @@ bsmma_status mx_gemm(const void* A, const uint8_t* sA, const void* B, const uint
  * (mx_scale_tiled_bytes(M, K/32, BSMMA_SCALES_A) bytes), sB_tiled with role
  * BSMMA_SCALES_B for the N rows.  Lets callers relayout static weight scales once.
  * One kernel launch.  It allocates nothing but the fixed-size split workspace of
- * mx_gemm, on the stream's first dense call.
+ * mx_gemm, on the stream's first dense call outside a graph capture; it needs no
+ * reservation before capture.
  */
 bsmma_status mx_gemm_tiled(const void* A, const uint8_t* sA_tiled, const void* B,
                            const uint8_t* sB_tiled, void* D, int64_t M, int64_t N, int64_t K,

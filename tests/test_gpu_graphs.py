@@ -11,7 +11,7 @@ import torch
 import block_scaled_precision_mma_gb300 as bs
 import oracle
 import synthetic
-from tests.gpu_common import assert_close, to_dev
+from tests.gpu_common import assert_close, sample_rows, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -103,6 +103,28 @@ def test_mx_gemm_replay_after_workspace_growth():
         assert bs.device_status() == 0
         ref = oracle.mx_gemm(c["A"], c["sA"], c["B"], c["sB"], M, N, K, "NT")
         assert_close(D.float().cpu().numpy(), ref, "replay after workspace growth")
+
+
+def test_mx_gemm_tiled_captured_without_reservation():
+    """mx_gemm_tiled needs no reservation before capture: captured first thing on a fresh
+    stream (no split workspace), on a shape whose last wave is split when one exists, it
+    splits nothing and its replay matches the oracle."""
+    M, N, K = 512, 512, 8192
+    c = synthetic.mx_operands((94, 0), M, N, K, "NT", "e4m3", "e4m3")
+    A, sA, B, sB = (to_dev(c[k]) for k in ("A", "sA", "B", "sB"))
+    tA, tB = bs.mx_scale_relayout(sA, "A"), bs.mx_scale_relayout(sB, "B")
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        bs.mx_gemm_tiled(A, tA, B, tB, "NT", out=D, M=M, N=N, K=K)
+    g.replay()
+    torch.cuda.synchronize()
+    assert bs.device_status() == 0
+    rows = sample_rows(M, 48, 94)
+    ref = oracle.mx_gemm(c["A"], c["sA"], c["B"], c["sB"], M, N, K, "NT", "e4m3", "e4m3", rows=rows)
+    assert_close(D.float().cpu().numpy()[rows], ref, "mx_gemm_tiled captured without reservation")
 
 
 def test_grouped_replays_with_new_split():

@@ -285,8 +285,9 @@ bsmma_status mx_gemm_tiled_bias_act(const void* A, const uint8_t* sA_tiled, cons
  * disk, behind a gate, with a fixed choice when the gate is off and no tuning during
  * graph capture.
  *   Shape classes and candidates: grouped_fp8_gemm per (nextPow2(total_M), N, K, G),
- *   tile widths 256 and 128 (when N % 256 == 0); the dense GEMMs per (nextPow2(M), N, K,
- *   layout, a_fmt, b_fmt), the SM-pair and single-CTA kernels (3, 1).
+ *   tile widths 256 and 128 (when N % 256 == 0); grouped_bf16_gemm likewise (when
+ *   N > 128); the dense GEMMs per (nextPow2(M), N, K, layout, a_fmt, b_fmt), the
+ *   SM-pair and single-CTA kernels (3, 1).
  *   The first call of a new class on a non-capturing stream runs each candidate twice
  *   and waits for it (it synchronises that stream); later calls, and calls in any
  *   process that reads the same cache file, use the stored choice.  A variant or width

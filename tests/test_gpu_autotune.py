@@ -49,6 +49,30 @@ def test_grouped_tunes_once_and_stays_correct(tuned):
     assert bs.device_status() == 0
 
 
+def test_grouped_bf16_tunes_once_and_stays_correct(tuned):
+    ms = np.array([300, 0, 129, 211], dtype=np.int64)
+    N, K = 512, 392
+    c = synthetic.grouped_bf16_operands((80, 1), ms, N, K)
+    X, W, m = to_dev(c["X"].view(np.int16)), to_dev(c["W"].view(np.int16)), to_dev(ms)
+    n0 = bs.launch_count()
+    D = bs.grouped_bf16_gemm(X, W, m)
+    torch.cuda.synchronize()
+    first = bs.launch_count() - n0
+    key = f"grouped_bf16 {1024} {N} {K} {ms.size}"
+    choice = bs.autotune_lookup(key)
+    assert choice in (128, 256)
+    assert f"{key} {choice}" in tuned.read_text()
+    assert first == 5                          # two timed runs per candidate, then the call
+    ref = oracle.grouped_bf16_gemm(c["X"], c["W"], ms, N, K)
+    assert_close(D.float().cpu().numpy(), ref, "tuned grouped bf16")
+    n0 = bs.launch_count()
+    D2 = bs.grouped_bf16_gemm(X, W, m)
+    torch.cuda.synchronize()
+    assert bs.launch_count() - n0 == 1         # the stored choice, no tuning
+    assert_close(D2.float().cpu().numpy(), ref, "cached grouped bf16")
+    assert bs.device_status() == 0
+
+
 def test_dense_tunes_once_and_stays_correct(tuned):
     M, N, K = 384, 512, 256
     c = synthetic.mx_operands((81, 0), M, N, K, "NT", "e4m3", "e4m3")

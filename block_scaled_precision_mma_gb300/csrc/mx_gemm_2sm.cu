@@ -55,8 +55,8 @@ struct Cfg2 {
   static constexpr int kSfbBytes = kKgPerStage * kSfbRepl * 1024;
   static constexpr int kChunkBytes = 4096;                // row-scale chunk, in the stage that loads it
   static constexpr int kStageBytes = kABytes + kBBytes + kSfbBytes + kChunkBytes;
-  // output staging: 2 KB (32 x 32 BF16) per epilogue warp, when it leaves five stages
-  static constexpr bool kStaged = !FP4;
+  // output staging: 2 KB (32 x 32 BF16) per epilogue warp
+  static constexpr bool kStaged = true;
   static constexpr int kOutBytes = kStaged ? 8 * 2048 : 0;
   static constexpr int kStages0 = (kSmemLimit - 2048 - kOutBytes) / kStageBytes;
   static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
@@ -67,7 +67,7 @@ struct Cfg2 {
 struct Pair2Params {
   __nv_bfloat16* D;
   float* part;          // split-unit partial sums [clusters][2][2 CTAs][128 x 256], or null
-  int* arrivals;        // [2 * leftover units] CTAs counted in per split unit (zero between launches)
+  int* arrivals;        // [leftover units][2 CTAs][8 epilogue warps] arrivals (zero between launches)
   Epilogue epi;         // optional bias and activation
   int64_t M, N;
   int sfa_kq;           // row-scale chunks per 128-row block

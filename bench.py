@@ -327,6 +327,7 @@ def run_ours(args):
     bs.load()
     bs.set_dense_variant(args.dense_variant)
     bs.set_grouped_tile_width(args.grouped_width)
+    bs.set_grouped_variant(args.grouped_variant)
     dev = torch.device("cuda", local)
     spec = workload_spec(args.workload)
     if args.gemm is not None:
@@ -536,6 +537,7 @@ def run_ours(args):
                    "parallelism": f"replicas x{ws}",
                    "dense_variant": args.dense_variant,
                    "grouped_width": args.grouped_width,
+                   "grouped_variant": args.grouped_variant,
                    "per_gemm_kernel_ms": [round(x, 4) for x in per_gemm_ms]},
         "roofline": {"bound": "tensor", "kernel": kernel,
                      "launch": describe(dom_g),
@@ -959,6 +961,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
     ap.add_argument("--grouped-width", type=int, default=0, choices=[0, 128, 256],
                     help="grouped tile width: 0 automatic, 128 or 256 (tuning only)")
+    ap.add_argument("--grouped-variant", type=int, default=0, choices=[0, 1, 3],
+                    help="grouped BF16 tiles: 0 automatic, 1 one CTA, 3 SM pairs (tuning only)")
     ap.add_argument("--dense-variant", type=int, default=0, choices=[0, 1, 3],
                     help="0 automatic, 1 single-CTA tiles, 3 SM-pair MMAs (tuning only)")
     ap.add_argument("--gemm", type=int, default=None,

@@ -32,7 +32,7 @@ __all__ = ["mx_gemm", "mx_gemm_tiled", "mx_gemm_noalloc", "grouped_fp8_gemm", "g
            "mx_quantize", "fp8_group_quantize", "fp8_block_quantize", "autotune_configure",
            "autotune_lookup",
            "mx_scale_tiled_bytes", "device_status", "reserve_workspace", "set_wait_limit_ns",
-           "set_dense_variant", "set_grouped_tile_width",
+           "set_dense_variant", "set_grouped_tile_width", "set_grouped_variant",
            "launch_count", "probe_wait_timeout", "status_string", "BsmmaError", "load",
            "LAYOUTS", "FORMATS", "ROLES", "build", "LIB_PATH"]
 
@@ -81,6 +81,7 @@ def load(path: str | None = None):
         lib.bsmma_set_wait_limit_ns.argtypes = [i64]
         lib.bsmma_set_dense_variant.argtypes = [i32]
         lib.bsmma_set_grouped_tile_width.argtypes = [i32]
+        lib.bsmma_set_grouped_variant.argtypes = [i32]
         lib.bsmma_status_string.argtypes = [i32]
         lib.bsmma_status_string.restype = ctypes.c_char_p
         lib.bsmma_launch_count.argtypes = []
@@ -99,7 +100,7 @@ def load(path: str | None = None):
                      "mx_scale_relayout",
                      "bsmma_reserve_workspace", "bsmma_device_status", "bsmma_set_wait_limit_ns",
                      "bsmma_set_dense_variant", "bsmma_set_grouped_tile_width",
-                     "grouped_bf16_gemm",
+                     "grouped_bf16_gemm", "bsmma_set_grouped_variant",
                      "bsmma_probe_wait_timeout", "mx_quantize", "fp8_group_quantize",
                      "fp8_block_quantize", "mx_gemm_bias_act", "mx_gemm_tiled_bias_act",
                      "bsmma_autotune_configure"):
@@ -277,6 +278,11 @@ def set_dense_variant(variant: int):
 def set_grouped_tile_width(width: int):
     """0 automatic, 128 or 256 columns per grouped tile."""
     _check(load().bsmma_set_grouped_tile_width(int(width)), "bsmma_set_grouped_tile_width")
+
+
+def set_grouped_variant(variant: int):
+    """Grouped BF16 tiles: 0 automatic, 1 one CTA per tile, 3 SM-pair 256 x 256 tiles."""
+    _check(load().bsmma_set_grouped_variant(int(variant)), "bsmma_set_grouped_variant")
 
 
 def launch_count() -> int:

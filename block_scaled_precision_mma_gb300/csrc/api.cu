@@ -34,6 +34,7 @@ std::atomic<int64_t> g_launches{0};
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_dense_variant{0};
 std::atomic<int> g_grouped_width{0};
+std::atomic<int> g_grouped_variant{0};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -92,6 +93,7 @@ const DeviceInfo* current_device(bsmma_status* err) {
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
 int dense_variant() { return g_dense_variant.load(); }
 int grouped_tile_width() { return g_grouped_width.load(); }
+int grouped_variant() { return g_grouped_variant.load(); }
 void count_launches(int n) { g_launches += n; }
 
 bsmma_status encode_tmap_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
@@ -569,6 +571,12 @@ bsmma_status bsmma_set_dense_variant(int variant) {
 bsmma_status bsmma_set_grouped_tile_width(int width) {
   if (width != 0 && width != 128 && width != 256) return BSMMA_ERR_INVALID_ARG;
   g_grouped_width = width;
+  return BSMMA_OK;
+}
+
+bsmma_status bsmma_set_grouped_variant(int variant) {
+  if (variant != 0 && variant != 1 && variant != 3) return BSMMA_ERR_INVALID_ARG;
+  g_grouped_variant = variant;
   return BSMMA_OK;
 }
 

@@ -21,14 +21,15 @@ constexpr int kMaxG = 64;   // groups per launch
 struct GroupTable {
   int64_t start[kMaxG + 1];   // first row of each group
   int64_t size[kMaxG];
-  int tile_start[kMaxG + 1];  // first 128-row block id of each group
+  int tile_start[kMaxG + 1];  // first row-block id of each group
   int bad;
 };
 
-// Fills `gt` from m_sizes; called by every thread of the block (needs blockDim >= G).
-// A bad table latches kDevBadMSizes once (block 0) and sets gt.bad for every block.
-// `init` runs on thread 0 between the table and the closing barrier (barrier setup).
-template <typename Init>
+// Fills `gt` from m_sizes, counting row blocks of TR rows; called by every thread of the
+// block (needs blockDim >= G).  A bad table latches kDevBadMSizes once (block 0) and sets
+// gt.bad for every block.  `init` runs on thread 0 between the table and the closing
+// barrier (barrier setup).
+template <int TR = kBM, typename Init>
 __device__ __forceinline__ void build_group_table(GroupTable& gt, const int64_t* m_sizes, int G,
                                                   int64_t total_M, int* status, Init init) {
   if (threadIdx.x < G) gt.size[threadIdx.x] = m_sizes[threadIdx.x];
@@ -43,7 +44,7 @@ __device__ __forceinline__ void build_group_table(GroupTable& gt, const int64_t*
       gt.tile_start[g] = tiles;
       if (!bad) {
         row += m;
-        tiles += static_cast<int>((m + kBM - 1) / kBM);
+        tiles += static_cast<int>((m + TR - 1) / TR);
       }
     }
     if (row != total_M) bad = 1;
@@ -56,7 +57,7 @@ __device__ __forceinline__ void build_group_table(GroupTable& gt, const int64_t*
   __syncthreads();
 }
 
-// Tile t -> (128-row block mt, column block nt).  Tiles are walked in bands of kBandRows
+// Tile t -> (row block mt, column block nt).  Tiles are walked in bands of kBandRows
 // row blocks: within a band the row block varies fastest, so the CTAs resident at one
 // time share a few weight column blocks and a band's rows of X, both of which stay in
 // L2 while the band is walked along N (row-fastest over all rows re-read every group's
@@ -72,7 +73,7 @@ __device__ __forceinline__ void tile_coords(int t, int NT, int rows, int& mt, in
   nt = v / h;
 }
 
-// Group owning 128-row block `mt` (tile_start is non-decreasing; empty groups own none).
+// Group owning row block `mt` (tile_start is non-decreasing; empty groups own none).
 __device__ __forceinline__ int find_group(const GroupTable& gt, int G, int mt) {
   int g = 0;
   for (int i = 1; i < G; ++i)

@@ -26,6 +26,7 @@ const DeviceInfo* current_device(bsmma_status* err);
 uint64_t wait_limit_ns();
 int dense_variant();   // 0 automatic, 1 single CTAs, 3 SM-pair MMAs
 int grouped_tile_width();   // 0 automatic, 128 or 256
+int grouped_variant();      // grouped BF16: 0 automatic, 1 one CTA per tile, 3 SM-pair tiles
 void count_launches(int n);
 
 // Encodes a 2-D uint8 tensor map with 128-byte swizzle: `inner` contiguous bytes per

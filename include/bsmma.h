@@ -286,12 +286,14 @@ bsmma_status mx_gemm_tiled_bias_act(const void* A, const uint8_t* sA_tiled, cons
  * graph capture.
  *   Shape classes and candidates: grouped_fp8_gemm per (nextPow2(total_M), N, K, G),
  *   tile widths 256 and 128 (when N % 256 == 0); grouped_bf16_gemm likewise (when
- *   N > 128); the dense GEMMs per (nextPow2(M), N, K, layout, a_fmt, b_fmt), the
- *   SM-pair and single-CTA kernels (3, 1).
+ *   N > 128), with SM-pair 256 x 256 tiles as a third candidate (2); the dense GEMMs
+ *   per (nextPow2(M), N, K, layout, a_fmt, b_fmt), the SM-pair and single-CTA kernels
+ *   (3, 1).
  *   The first call of a new class on a non-capturing stream runs each candidate twice
  *   and waits for it (it synchronises that stream); later calls, and calls in any
  *   process that reads the same cache file, use the stored choice.  A variant or width
- *   set with bsmma_set_dense_variant / bsmma_set_grouped_tile_width takes precedence.
+ *   set with bsmma_set_dense_variant / bsmma_set_grouped_tile_width /
+ *   bsmma_set_grouped_variant takes precedence.
  *   Every candidate computes the same result.
  * bsmma_autotune_configure -- enable: 1 on, 0 off, -1 from the environment
  *   (BSMMA_AUTOTUNE=1 turns it on); cache_path: the file, or NULL for
@@ -392,6 +394,13 @@ bsmma_status bsmma_set_dense_variant(int variant);
  * (grouped_fp8_gemm: used only when N % 256 == 0).  Same result; a tuning and testing
  * control. */
 bsmma_status bsmma_set_grouped_tile_width(int width);
+
+/* Selects grouped_bf16_gemm's tiles for later calls: 0 automatic (default: 256 x 256 tiles
+ * on SM pairs -- 2-CTA clusters issuing M = 256 MMAs -- when N > 128 and the groups average
+ * at least 128 rows, else one CTA per 128-row tile of 128 or 256 columns), 1 one CTA per
+ * tile, 3 SM-pair tiles.  Any other value returns BSMMA_ERR_INVALID_ARG.  Same result; a
+ * tuning and testing control. */
+bsmma_status bsmma_set_grouped_variant(int variant);
 
 /* Human-readable name of a status code (static storage). */
 const char* bsmma_status_string(bsmma_status status);

@@ -21,12 +21,15 @@ def _lib():
     torch.cuda.init()
 
 
-@pytest.fixture(params=[128, 256], ids=["bn128", "bn256"])
+@pytest.fixture(params=[(1, 128), (1, 256), (3, 0)], ids=["bn128", "bn256", "pair256"])
 def bwidth(request):
-    """Runs the test with 128- and 256-column tiles."""
-    bs.set_grouped_tile_width(request.param)
-    yield request.param
+    """Runs the test with one-CTA tiles of 128 and 256 columns, and SM-pair 256 x 256 tiles."""
+    variant, width = request.param
+    bs.set_grouped_variant(variant)
+    bs.set_grouped_tile_width(width)
+    yield width
     bs.set_grouped_tile_width(0)
+    bs.set_grouped_variant(0)
 
 
 def bf16_bits(v) -> np.ndarray:

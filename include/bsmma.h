@@ -399,7 +399,7 @@ bsmma_status bsmma_set_grouped_tile_width(int width);
  * on SM pairs -- 2-CTA clusters issuing M = 256 MMAs -- when N > 128 and the groups average
  * at least 128 rows, else one CTA per 128-row tile of 128 or 256 columns), 1 one CTA per
  * tile, 3 SM-pair tiles.  Any other value returns BSMMA_ERR_INVALID_ARG.  Same result; a
- * tuning and testing control. */
+ * tuning and testing control.  (grouped_fp8_gemm always uses one CTA per tile.) */
 bsmma_status bsmma_set_grouped_variant(int variant);
 
 /* Human-readable name of a status code (static storage). */

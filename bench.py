@@ -27,6 +27,7 @@ import atexit
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -289,12 +290,19 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """C++ source without its comments (a record stays valid across comment edits)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (line.split("//", 1)[0].rstrip() for line in text.splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_source_hash(workload: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_scaled_precision_mma_gb300", "csrc")
     for f in KERNEL_SOURCES[workload if workload in KERNEL_SOURCES else "dense"]:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -17,6 +17,9 @@
 //               tile's columns with tcgen05.ld, rounding to BF16 (nearest-even) and
 //               storing 16 bytes per lane, only rows of the tile's group and columns
 //               below N.
+// Groups of many rows go instead to grouped_bf16_pair_kernel: the same roles on 256 x 256
+// tiles spread over the two CTAs of a cluster (an SM pair), whose M = 256 MMAs read a third
+// less shared memory per flop.
 // K need only be a multiple of 8 (16-byte rows): the last stage's columns past K are
 // filled with zeros by the tensor copy.  N need only be a multiple of 8: columns of the
 // last column block past N are computed from whatever rows the copy returns (the next

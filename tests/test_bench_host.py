@@ -49,3 +49,11 @@ def test_traffic_record_requires_matching_sources(tmp_path, monkeypatch):
     assert bench.recorded_traffic("grouped_bf16") == 123.0
     monkeypatch.setattr(bench, "kernel_source_hash", lambda w: "ffffffffffffffff")
     assert bench.recorded_traffic("grouped_bf16") is None
+
+
+def test_source_hash_ignores_comments_only():
+    code = "int f(int x) {  // doubles\n  return 2 * x; /* no overflow check */\n}\n"
+    same = "// a comment line added\nint f(int x) {\n  return 2 * x;\n}\n"
+    other = "int f(int x) {\n  return 3 * x;\n}\n"
+    assert bench._code_only(code) == bench._code_only(same)
+    assert bench._code_only(code) != bench._code_only(other)

@@ -146,7 +146,16 @@ def test_grouped_replays_with_new_split():
         assert_close(D.float().cpu().numpy(), ref, f"grouped replay {ms.tolist()}")
 
 
-def test_grouped_bf16_replays_with_new_split():
+@pytest.mark.parametrize("variant", [1, 3], ids=["one_cta", "pair"])
+def test_grouped_bf16_replays_with_new_split(variant):
+    bs.set_grouped_variant(variant)
+    try:
+        _grouped_bf16_replay()
+    finally:
+        bs.set_grouped_variant(0)
+
+
+def _grouped_bf16_replay():
     N, K = 264, 200
     ms1 = np.array([100, 0, 200, 37, 0, 63], dtype=np.int64)
     ms2 = np.array([0, 250, 1, 0, 149, 0], dtype=np.int64)          # same total_M = 400

@@ -134,22 +134,30 @@ def test_grouped_bf16_many_tiles(bwidth):
     assert_close(got[rows], ref, "grouped bf16 many tiles")
 
 
-def test_grouped_bf16_deterministic():
+def test_grouped_bf16_deterministic(variant):
     ms = synthetic.gen_m_sizes(1024, 1)
     c = synthetic.grouped_bf16_operands((60, 78), ms, 512, 768)
     a = run_bf16(c["X"], c["W"], ms, 512, 768)
     assert np.array_equal(a, run_bf16(c["X"], c["W"], ms, 512, 768))
 
 
-def test_grouped_bf16_empty_total():
+@pytest.fixture(params=[1, 3], ids=["one_cta", "pair"])
+def variant(request):
+    bs.set_grouped_variant(request.param)
+    yield request.param
+    bs.set_grouped_variant(0)
+
+
+def test_grouped_bf16_empty_total(variant):
     c = synthetic.grouped_bf16_operands((60, 79), np.zeros(8, dtype=np.int64), 256, 256)
     assert run_bf16(c["X"], c["W"], c["m_sizes"], 256, 256).shape == (0, 256)
 
 
 @pytest.mark.parametrize("bad", [[10, -1, 11, 0], [10, 5, 4, 0], [30, 0, 0, 0]])
-def test_grouped_bf16_bad_m_sizes_writes_nothing(bad):
+def test_grouped_bf16_bad_m_sizes_writes_nothing(bad, variant):
     """Negative sizes or a sum different from total_M: nothing is written and
-    BSMMA_DEV_BAD_MSIZES is latched."""
+    BSMMA_DEV_BAD_MSIZES is latched (on SM pairs both CTAs of every cluster stop before
+    they allocate or wait for anything)."""
     N, K, T = 256, 128, 20
     c = synthetic.grouped_bf16_operands((60, 80), np.array([20, 0, 0, 0]), N, K)
     X, W = to_dev(c["X"].view(np.int16)), to_dev(c["W"].view(np.int16))

@@ -71,6 +71,7 @@ struct GroupedParams {
   const int64_t* m_sizes;
   int64_t total_M, N;
   int G, num_n_tiles, num_kb;
+  int d_align32;        // D is 32-byte aligned: rows are stored in 32-byte pieces
   uint32_t idesc;
   int* status;
   uint64_t limit_ns;
@@ -347,14 +348,30 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!ok) break;
       if (valid) {
+        // the fold warps' stores hold up the next tile's fold (and, two partial slots on, the
+        // MMAs), so they go out in as few instructions as the alignment allows: a full
+        // 32-byte sector per lane (rows are N*2 bytes, a multiple of 256)
         const int64_t row = gt.start[g] + l;
         __nv_bfloat16* out = p.D + row * p.N + static_cast<int64_t>(nt) * BN + h * kCols;
+        if (p.d_align32) {
 #pragma unroll
-        for (int v = 0; v < kCols / 8; ++v)
-          st_global_v4_cs(out + v * 8, pack_bf16x2(acc[v * 4 + 0].x, acc[v * 4 + 0].y),
-                          pack_bf16x2(acc[v * 4 + 1].x, acc[v * 4 + 1].y),
-                          pack_bf16x2(acc[v * 4 + 2].x, acc[v * 4 + 2].y),
-                          pack_bf16x2(acc[v * 4 + 3].x, acc[v * 4 + 3].y));
+          for (int v = 0; v < kCols / 16; ++v)
+            st_global_v8_cs(out + v * 16, pack_bf16x2(acc[v * 8 + 0].x, acc[v * 8 + 0].y),
+                            pack_bf16x2(acc[v * 8 + 1].x, acc[v * 8 + 1].y),
+                            pack_bf16x2(acc[v * 8 + 2].x, acc[v * 8 + 2].y),
+                            pack_bf16x2(acc[v * 8 + 3].x, acc[v * 8 + 3].y),
+                            pack_bf16x2(acc[v * 8 + 4].x, acc[v * 8 + 4].y),
+                            pack_bf16x2(acc[v * 8 + 5].x, acc[v * 8 + 5].y),
+                            pack_bf16x2(acc[v * 8 + 6].x, acc[v * 8 + 6].y),
+                            pack_bf16x2(acc[v * 8 + 7].x, acc[v * 8 + 7].y));
+        } else {
+#pragma unroll
+          for (int v = 0; v < kCols / 8; ++v)
+            st_global_v4_cs(out + v * 8, pack_bf16x2(acc[v * 4 + 0].x, acc[v * 4 + 0].y),
+                            pack_bf16x2(acc[v * 4 + 1].x, acc[v * 4 + 1].y),
+                            pack_bf16x2(acc[v * 4 + 2].x, acc[v * 4 + 2].y),
+                            pack_bf16x2(acc[v * 4 + 3].x, acc[v * 4 + 3].y));
+        }
       }
     }
     cp_async_wait_all();   // no scale copy may land after the block has finished
@@ -475,6 +492,7 @@ bsmma_status launch_grouped_width(const uint8_t* X, const float* sX, const uint8
   p.sW = sW;
   p.Wp = packed ? W : nullptr;
   p.D = static_cast<__nv_bfloat16*>(D);
+  p.d_align32 = (reinterpret_cast<uintptr_t>(D) & 31u) == 0;
   p.m_sizes = m_sizes;
   p.total_M = total_M;
   p.N = N;

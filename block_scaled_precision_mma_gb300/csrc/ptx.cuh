@@ -360,6 +360,15 @@ __device__ __forceinline__ void st_global_v4_cs(void* p, uint32_t a, uint32_t b,
                : "memory");
 }
 
+// 32 bytes (one full sector) at a 32-byte-aligned address, streaming (evict-first).
+__device__ __forceinline__ void st_global_v8_cs(void* p, uint32_t a, uint32_t b, uint32_t c,
+                                                uint32_t d, uint32_t e, uint32_t f, uint32_t g,
+                                                uint32_t h) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a),
+               "r"(b), "r"(c), "r"(d), "r"(e), "r"(f), "r"(g), "r"(h)
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

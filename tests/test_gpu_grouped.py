@@ -107,6 +107,26 @@ def test_grouped_many_tiles(gwidth):
     assert_close(got, ref, "grouped many tiles")
 
 
+def test_grouped_output_16_byte_aligned():
+    """D at an address that is 16- but not 32-byte aligned (the kernel then stores 16-byte
+    pieces instead of 32-byte ones) gives the same result as an aligned D."""
+    ms = np.array([130, 0, 257, 5], dtype=np.int64)
+    c = synthetic.grouped_operands((40, 83), ms, 512, 384)
+    X, sX, W, sW, m = (to_dev(c[k]) for k in ("X", "sX", "W", "sW", "m_sizes"))
+    T, N = int(ms.sum()), 512
+    buf = torch.full((T * N + 64,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    assert buf.data_ptr() % 32 == 0
+    D16 = buf[8:8 + T * N].view(T, N)                  # 16 bytes past a 32-byte boundary
+    bs.grouped_fp8_gemm(X, sX, W, sW, m, out=D16)
+    D32 = bs.grouped_fp8_gemm(X, sX, W, sW, m)
+    torch.cuda.synchronize()
+    assert bs.device_status() == 0
+    assert torch.isnan(buf[:8].float()).all() and torch.isnan(buf[8 + T * N:].float()).all()
+    assert torch.equal(D16, D32)
+    ref = oracle.grouped_fp8_gemm(c["X"], c["sX"], c["W"], c["sW"], ms, N, 384)
+    assert_close(D16.float().cpu().numpy(), ref, "grouped, 16-byte-aligned D")
+
+
 def test_grouped_deterministic():
     ms = synthetic.gen_m_sizes(1024, 1)
     c = synthetic.grouped_operands((40, 78), ms, 512, 768)

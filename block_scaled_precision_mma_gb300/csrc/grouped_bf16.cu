@@ -88,10 +88,33 @@ struct Bf16Params {
   const int64_t* m_sizes;
   int64_t total_M, N;
   int G, num_n_tiles, num_kb;
+  int d_align32;        // D 32-byte aligned and N % 16 == 0: rows stored in 32-byte pieces
   uint32_t idesc;
   int* status;
   uint64_t limit_ns;
 };
+
+// 32 columns of this lane's row (x: 32 FP32 values from tcgen05.ld), rounded to BF16 and
+// stored with streaming stores, columns at or past N skipped: 32-byte pieces (a full sector
+// per lane) when D is 32-byte aligned and N % 16 == 0, else 16-byte pieces.
+__device__ __forceinline__ void store32(__nv_bfloat16* out, int64_t col0, int c, const uint32_t* x,
+                                        const Bf16Params& p) {
+  auto pk = [&](int i) {
+    return pack_bf16x2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
+  };
+  if (p.d_align32) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+      if (col0 + c * 32 + e * 16 < p.N)
+        st_global_v8_cs(out + c * 32 + e * 16, pk(8 * e), pk(8 * e + 1), pk(8 * e + 2), pk(8 * e + 3),
+                        pk(8 * e + 4), pk(8 * e + 5), pk(8 * e + 6), pk(8 * e + 7));
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (col0 + c * 32 + e * 8 < p.N)
+        st_global_v4_cs(out + c * 32 + e * 8, pk(4 * e), pk(4 * e + 1), pk(4 * e + 2), pk(4 * e + 3));
+  }
+}
 
 template <int BN>
 __global__ void __launch_bounds__(BCfg<BN>::kThreads, 1)
@@ -240,16 +263,7 @@ __global__ void __launch_bounds__(BCfg<BN>::kThreads, 1)
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + h * kCols;
       const int64_t col0 = static_cast<int64_t>(nt) * BN + h * kCols;
       __nv_bfloat16* out = p.D + (gt.start[g] + l) * p.N + col0;
-      auto store_piece = [&](int c, const uint32_t* x) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (col0 + c * 32 + e * 8 < p.N)
-            st_global_v4_cs(out + c * 32 + e * 8,
-                            pack_bf16x2(__uint_as_float(x[e * 8 + 0]), __uint_as_float(x[e * 8 + 1])),
-                            pack_bf16x2(__uint_as_float(x[e * 8 + 2]), __uint_as_float(x[e * 8 + 3])),
-                            pack_bf16x2(__uint_as_float(x[e * 8 + 4]), __uint_as_float(x[e * 8 + 5])),
-                            pack_bf16x2(__uint_as_float(x[e * 8 + 6]), __uint_as_float(x[e * 8 + 7])));
-      };
+      auto store_piece = [&](int c, const uint32_t* x) { store32(out, col0, c, x, p); };
 #pragma unroll
       for (int c = 0; c < kPieces; c += 2) {
         uint32_t ra[32], rb[32];
@@ -461,16 +475,7 @@ __global__ void __launch_bounds__(PCfg::kThreads, 1)
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + h * kCols;
       const int64_t col0 = static_cast<int64_t>(nt) * BN + h * kCols;
       __nv_bfloat16* out = p.D + (gt.start[g] + l) * p.N + col0;
-      auto store_piece = [&](int c, const uint32_t* x) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (col0 + c * 32 + e * 8 < p.N)
-            st_global_v4_cs(out + c * 32 + e * 8,
-                            pack_bf16x2(__uint_as_float(x[e * 8 + 0]), __uint_as_float(x[e * 8 + 1])),
-                            pack_bf16x2(__uint_as_float(x[e * 8 + 2]), __uint_as_float(x[e * 8 + 3])),
-                            pack_bf16x2(__uint_as_float(x[e * 8 + 4]), __uint_as_float(x[e * 8 + 5])),
-                            pack_bf16x2(__uint_as_float(x[e * 8 + 6]), __uint_as_float(x[e * 8 + 7])));
-      };
+      auto store_piece = [&](int c, const uint32_t* x) { store32(out, col0, c, x, p); };
 #pragma unroll
       for (int c = 0; c < kPieces; c += 2) {
         uint32_t ra[32], rb[32];
@@ -589,6 +594,7 @@ bsmma_status launch_bf16_width(const void* X, const void* W, void* D, const int6
   if (st != BSMMA_OK) return st;
   Bf16Params p;
   p.D = static_cast<__nv_bfloat16*>(D);
+  p.d_align32 = (reinterpret_cast<uintptr_t>(D) & 31u) == 0 && N % 16 == 0;
   p.m_sizes = m_sizes;
   p.total_M = total_M;
   p.N = N;

@@ -34,11 +34,6 @@ void count_launches(int n);
 bsmma_status encode_tmap_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                             uint64_t row_stride, uint32_t box_inner, uint32_t box_outer);
 
-// Encodes a 2-D BF16 tensor map for stores with 64-byte swizzle: `cols` contiguous BF16
-// values per row (a multiple of 8), `rows` rows, box of box_cols x box_rows.
-bsmma_status encode_tmap_bf16_out(CUtensorMap* map, const void* base, uint64_t cols,
-                                  uint64_t rows, uint32_t box_cols, uint32_t box_rows);
-
 // Host-side argument checks shared by the dense entry points.
 bsmma_status validate_dense(const void* A, const void* sA, const void* B, const void* sB,
                             const void* D, int64_t M, int64_t N, int64_t K, bsmma_layout layout,

@@ -98,35 +98,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// 2-D tiled tensor store from shared memory (this CTA's), tracked by the thread's bulk
-// async-group; coordinates past the tensor's extent are not written.
-__device__ __forceinline__ void tma_store_2d(const void* tmap, const void* src, int32_t c0,
-                                             int32_t c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-          reinterpret_cast<uint64_t>(tmap)),
-      "r"(c0), "r"(c1), "r"(smem_u32(src))
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Waits until at most N of the thread's bulk async-groups still read shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_group_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// Waits until at most N of the thread's bulk async-groups are incomplete.
-template <int N>
-__device__ __forceinline__ void bulk_wait_group() {
-  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
-}
-// Makes this thread's generic-proxy shared-memory writes visible to the async proxy
-// (tensor copies that read them).
-__device__ __forceinline__ void fence_proxy_async_shared() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

@@ -138,6 +138,33 @@ def test_tiled_scales_match_plain():
     assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("af,epi", [("e4m3", False), ("e2m1", False), ("e4m3", True)],
+                         ids=["fp8", "fp4", "fp8_bias_gelu"])
+def test_dense_output_16_byte_aligned(af, epi, variant):
+    """D at an address that is 16- but not 32-byte aligned (the kernels then store 16-byte
+    pieces instead of 32-byte ones) gives the same result as an aligned D, with and
+    without the bias / activation stage."""
+    M, N, K = 300, 512, 384
+    c = synthetic.mx_operands((2, 603), M, N, K, "NT", af, af)
+    A, sA, B, sB = (to_dev(c[k]) for k in ("A", "sA", "B", "sB"))
+    kw = {}
+    if epi:
+        g = torch.Generator().manual_seed(603)
+        kw = dict(bias=torch.randn(N, generator=g).bfloat16().cuda(), act="gelu")
+    buf = torch.full((M * N + 64,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    assert buf.data_ptr() % 32 == 0
+    D16 = buf[8:8 + M * N].view(M, N)                  # 16 bytes past a 32-byte boundary
+    bs.mx_gemm(A, sA, B, sB, "NT", af, af, out=D16, M=M, N=N, K=K, **kw)
+    D32 = bs.mx_gemm(A, sA, B, sB, "NT", af, af, M=M, N=N, K=K, **kw)
+    torch.cuda.synchronize()
+    assert bs.device_status() == 0
+    assert torch.isnan(buf[:8].float()).all() and torch.isnan(buf[8 + M * N:].float()).all()
+    assert torch.equal(D16, D32)
+    if not epi:
+        ref = oracle.mx_gemm(c["A"], c["sA"], c["B"], c["sB"], M, N, K, "NT", af, af)
+        assert_close(D16.float().cpu().numpy(), ref, f"{af}, 16-byte-aligned D")
+
+
 def test_deterministic():
     c = synthetic.mx_operands((2, 601), 512, 768, 1024, "NN", "e4m3", "e5m2")
     assert np.array_equal(run_dense(c), run_dense(c))

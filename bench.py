@@ -286,7 +286,7 @@ KERNEL_SOURCES = {
     "grouped_fp8": ("grouped_gemm.cu", "grouped_sched.cuh", "ptx.cuh", "internal.h"),
     "grouped_bf16": ("grouped_bf16.cu", "grouped_sched.cuh", "ptx.cuh", "internal.h"),
     "quantize": ("quantize.cu", "ptx.cuh", "internal.h"),
-    "dense": ("mx_gemm_2sm.cu", "mx_gemm.cu", "ptx.cuh", "internal.h"),
+    "dense": ("mx_gemm_2sm.cu", "mx_gemm.cu", "store_stage.cuh", "ptx.cuh", "internal.h"),
 }
 
 

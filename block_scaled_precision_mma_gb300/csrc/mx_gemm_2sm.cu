@@ -32,6 +32,7 @@
 #include "internal.h"
 #include "epilogue.cuh"
 #include "ptx.cuh"
+#include "store_stage.cuh"
 #include "stream_k.cuh"
 
 namespace bsmma {
@@ -55,9 +56,12 @@ struct Cfg2 {
   static constexpr int kSfbBytes = kKgPerStage * kSfbRepl * 1024;
   static constexpr int kChunkBytes = 4096;                // row-scale chunk, in the stage that loads it
   static constexpr int kStageBytes = kABytes + kBBytes + kSfbBytes + kChunkBytes;
-  static constexpr int kStages0 = (kSmemLimit - 2048) / kStageBytes;
+  // output staging: 2 KB (32 x 32 BF16) per epilogue warp
+  static constexpr bool kStaged = true;
+  static constexpr int kOutBytes = kStaged ? 8 * 2048 : 0;
+  static constexpr int kStages0 = (kSmemLimit - 2048 - kOutBytes) / kStageBytes;
   static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 512;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kOutBytes + 512;
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
 };
 
@@ -67,7 +71,6 @@ struct Pair2Params {
   int* arrivals;        // [leftover units][2 CTAs][8 epilogue warps] arrivals (zero between launches)
   Epilogue epi;         // optional bias and activation
   int64_t M, N;
-  int d_align32;        // D 32-byte aligned and N % 16 == 0: rows stored in 32-byte pieces
   int sfa_kq;           // row-scale chunks per 128-row block
   int sfb_kg;           // column-scale blocks per 256-column block
   int num_m_tiles;      // 128-row tiles of D
@@ -129,7 +132,8 @@ template <bool FP4, bool A_MN, bool B_MN, bool EPI>
 __global__ void __maxnreg__(168)
     mx_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmSFA,
-                       const __grid_constant__ CUtensorMap tmSFB, const Pair2Params p) {
+                       const __grid_constant__ CUtensorMap tmSFB,
+                       const __grid_constant__ CUtensorMap tmD, const Pair2Params p) {
   using C = Cfg2<FP4>;
   constexpr int kSfbRepl = C::kSfbRepl;
   extern __shared__ uint8_t smem_raw[];
@@ -139,7 +143,8 @@ __global__ void __maxnreg__(168)
   uint8_t* sB = sA + C::kStages * C::kABytes;
   uint8_t* sSFB = sB + C::kStages * C::kBBytes;
   uint8_t* sSFA = sSFB + C::kStages * C::kSfbBytes;        // one chunk slot per stage
-  uint64_t* full = reinterpret_cast<uint64_t*>(sSFA + C::kStages * C::kChunkBytes);
+  uint8_t* sOut = sSFA + C::kStages * C::kChunkBytes;       // output staging (FP8)
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + C::kOutBytes);
   uint64_t* empty = full + C::kStages;
   uint64_t* acc_full = empty + C::kStages;
   uint64_t* acc_empty = acc_full + 1;
@@ -173,6 +178,7 @@ __global__ void __maxnreg__(168)
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmSFA);
     prefetch_tmap(&tmSFB);
+    if (C::kStaged) prefetch_tmap(&tmD);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, kTmemCols);
@@ -330,51 +336,63 @@ __global__ void __maxnreg__(168)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
       const int64_t row = static_cast<int64_t>(mt) * 128 + q * 32 + lane;
+      const int64_t row0 = static_cast<int64_t>(mt) * 128 + q * 32;
       const int64_t col0 = static_cast<int64_t>(nt) * 256 + h * kCols;
+      uint8_t* stg = sOut + (warp - 2) * 2048;
       // Output of the 32-column piece c of this warp's 32 rows x 128 columns (vals: 32
-      // FP32 values of this lane's row), straight from registers: lane = row, 64
-      // contiguous bytes per lane, as two 32-byte stores (a whole sector each) when D
-      // allows, else four 16-byte ones.  Measured against staging the pieces in shared
-      // memory for a TMA tensor store: 0.6-1.5% faster on every dense shape, and the
-      // 8 KB FP4 stage that staging displaced comes back.
+      // FP32 values of this lane's row).  FP8: BF16 through the warp's buffer to a TMA
+      // tensor store -- lane = row, the 16-byte group v of 8 columns at position
+      // v ^ ((r / 2) % 4), the tensor map's 64-byte swizzle, so the lanes hit distinct
+      // banks.  FP4: 16-byte stores from registers.
       auto store_piece = [&](int c, const uint32_t* vals) {
-        if (row >= p.M) return;
-        __nv_bfloat16* out = p.D + row * p.N + col0;
-        if (p.d_align32) {
+        if constexpr (C::kStaged) {
+          if (row0 >= p.M || col0 + c * 32 >= p.N) return;   // warp-uniform
+          uint32_t o[4][4];
 #pragma unroll
-          for (int g = 0; g < 2; ++g) {
-            const int o = c * 32 + g * 16;
-            if (col0 + o < p.N) {
-              uint32_t w[2][4];
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const uint32_t* v = vals + g * 16 + e * 8;
-                if constexpr (EPI) {
-                  apply8(v, col0 + o + e * 8, p.epi, w[e]);
-                } else {
-#pragma unroll
-                  for (int j = 0; j < 4; ++j)
-                    w[e][j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-                }
+          for (int g = 0; g < 4; ++g) {
+            const int64_t col = col0 + c * 32 + g * 8;
+            if constexpr (EPI) {
+              if (col < p.N) {
+                apply8(vals + g * 8, col, p.epi, o[g]);
+                continue;
               }
-              st_global_v8_cs(out + o, w[0][0], w[0][1], w[0][2], w[0][3], w[1][0], w[1][1],
-                              w[1][2], w[1][3]);
             }
-          }
-          return;
-        }
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int o = c * 32 + g * 8;
-          if (col0 + o < p.N) {
-            if constexpr (EPI)
-              store8(out + o, vals + g * 8, col0 + o, p.epi);
-            else
-              st_global_v4_cs(out + o,
-                              pack_bf16x2(__uint_as_float(vals[g * 8 + 0]), __uint_as_float(vals[g * 8 + 1])),
-                              pack_bf16x2(__uint_as_float(vals[g * 8 + 2]), __uint_as_float(vals[g * 8 + 3])),
-                              pack_bf16x2(__uint_as_float(vals[g * 8 + 4]), __uint_as_float(vals[g * 8 + 5])),
-                              pack_bf16x2(__uint_as_float(vals[g * 8 + 6]), __uint_as_float(vals[g * 8 + 7])));
+            for (int j = 0; j < 4; ++j)
+              o[g][j] = pack_bf16x2(__uint_as_float(vals[g * 8 + 2 * j]),
+                                    __uint_as_float(vals[g * 8 + 2 * j + 1]));
+          }
+          if (lane == 0) bulk_wait_group_read<0>();   // the previous piece has been read
+          __syncwarp();
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint32_t a = smem_u32(stg + lane * 64 + ((g ^ ((lane >> 1) & 3)) * 16));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(o[g][0]),
+                         "r"(o[g][1]), "r"(o[g][2]), "r"(o[g][3])
+                         : "memory");
+          }
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmD, stg, static_cast<int32_t>(col0 + c * 32), static_cast<int32_t>(row0));
+            bulk_commit_group();
+          }
+        } else {
+          if (row >= p.M) return;
+          __nv_bfloat16* out = p.D + row * p.N + col0;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int o = c * 32 + g * 8;
+            if (col0 + o < p.N) {
+              if constexpr (EPI)
+                store8(out + o, vals + g * 8, col0 + o, p.epi);
+              else
+                st_global_v4_cs(out + o,
+                                pack_bf16x2(__uint_as_float(vals[g * 8 + 0]), __uint_as_float(vals[g * 8 + 1])),
+                                pack_bf16x2(__uint_as_float(vals[g * 8 + 2]), __uint_as_float(vals[g * 8 + 3])),
+                                pack_bf16x2(__uint_as_float(vals[g * 8 + 4]), __uint_as_float(vals[g * 8 + 5])),
+                                pack_bf16x2(__uint_as_float(vals[g * 8 + 6]), __uint_as_float(vals[g * 8 + 7])));
+            }
           }
         }
       };
@@ -436,6 +454,9 @@ __global__ void __maxnreg__(168)
         store_piece(c, sum);
       }
     }
+    // every tensor store of this warp has finished reading and writing before the
+    // buffers (and the block) go away
+    if (C::kStaged && lane == 0) bulk_wait_group<0>();
   }
   __syncthreads();
   cluster_sync();   // both CTAs are done with tensor memory and with each other's barriers
@@ -449,7 +470,7 @@ __global__ void __maxnreg__(168)
 
 template <bool FP4, bool A_MN, bool B_MN, bool EPI>
 bsmma_status launch_2sm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
-                        const CUtensorMap& tsb, const Pair2Params& p,
+                        const CUtensorMap& tsb, const CUtensorMap& td, const Pair2Params& p,
                         cudaStream_t stream) {
   using C = Cfg2<FP4>;
   auto kern = mx_gemm_2sm_kernel<FP4, A_MN, B_MN, EPI>;
@@ -491,7 +512,7 @@ bsmma_status launch_2sm(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, td, p);
   count_launches(1);
   return cuda_ok(e == cudaSuccess ? cudaGetLastError() : e);
 }
@@ -510,7 +531,9 @@ bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B
   const int64_t kblocks = K / 32;
   const int64_t kq = (kblocks + 7) / 8;                   // row-scale chunks per 128 rows
   const int64_t kgp = 2 * ((kblocks + 7) / 8);            // column-scale blocks per 256 columns
-  CUtensorMap ta, tb, tsa, tsb;
+  CUtensorMap ta, tb, tsa, tsb, td;
+  st = encode_tmap_bf16_out(&td, D, static_cast<uint64_t>(N), static_cast<uint64_t>(M), 32, 32);
+  if (st != BSMMA_OK) return st;
   if (layout == BSMMA_TN) st = encode_tmap_u8(&ta, A, M, K, M, 128, 128);
   else st = encode_tmap_u8(&ta, A, kbytes, M, kbytes, 128, 128);
   if (st != BSMMA_OK) return st;
@@ -541,7 +564,6 @@ bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B
   p.epi.act = act;
   p.M = M;
   p.N = N;
-  p.d_align32 = (reinterpret_cast<uintptr_t>(D) & 31u) == 0 && N % 16 == 0;
   p.sfa_kq = static_cast<int>(kq);
   p.sfb_kg = static_cast<int>(kgp);
   p.num_m_tiles = static_cast<int>((M + 127) / 128);
@@ -555,8 +577,8 @@ bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B
   p.limit_ns = wait_limit_ns();
   const bool epi = bias != nullptr || act != 0;
 #define BSMMA_2SM(F, A, B)                                                       \
-  (epi ? launch_2sm<F, A, B, true>(ta, tb, tsa, tsb, p, stream)              \
-       : launch_2sm<F, A, B, false>(ta, tb, tsa, tsb, p, stream))
+  (epi ? launch_2sm<F, A, B, true>(ta, tb, tsa, tsb, td, p, stream)              \
+       : launch_2sm<F, A, B, false>(ta, tb, tsa, tsb, td, p, stream))
   if (fp4) return BSMMA_2SM(true, false, false);
   switch (layout) {
     case BSMMA_NT: return BSMMA_2SM(false, false, false);

@@ -141,9 +141,10 @@ def test_tiled_scales_match_plain():
 @pytest.mark.parametrize("af,epi", [("e4m3", False), ("e2m1", False), ("e4m3", True)],
                          ids=["fp8", "fp4", "fp8_bias_gelu"])
 def test_dense_output_16_byte_aligned(af, epi, variant):
-    """D at an address that is 16- but not 32-byte aligned (the kernels then store 16-byte
-    pieces instead of 32-byte ones) gives the same result as an aligned D, with and
-    without the bias / activation stage."""
+    """D at an address that is 16- but not 32-byte aligned (the least the entry point
+    accepts; the SM-pair kernel's tensor stores start there) gives the same result as an
+    aligned D and writes nothing outside it, with and without the bias / activation
+    stage."""
     M, N, K = 300, 512, 384
     c = synthetic.mx_operands((2, 603), M, N, K, "NT", af, af)
     A, sA, B, sB = (to_dev(c[k]) for k in ("A", "sA", "B", "sB"))

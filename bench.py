@@ -284,9 +284,11 @@ def reduce_max(values, dist):
 # valid only while they are unchanged).
 KERNEL_SOURCES = {
     "grouped_fp8": ("grouped_gemm.cu", "grouped_sched.cuh", "ptx.cuh", "internal.h"),
+    "grouped_fp8_packed": ("grouped_gemm.cu", "grouped_sched.cuh", "ptx.cuh", "internal.h"),
     "grouped_bf16": ("grouped_bf16.cu", "grouped_sched.cuh", "ptx.cuh", "internal.h"),
     "quantize": ("quantize.cu", "ptx.cuh", "internal.h"),
-    "dense": ("mx_gemm_2sm.cu", "mx_gemm.cu", "store_stage.cuh", "ptx.cuh", "internal.h"),
+    "dense": ("mx_gemm_2sm.cu", "mx_gemm.cu", "epilogue.cuh", "store_stage.cuh", "stream_k.cuh",
+              "ptx.cuh", "internal.h"),
 }
 
 

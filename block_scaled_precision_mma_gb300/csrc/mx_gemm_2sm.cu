@@ -433,22 +433,36 @@ __global__ void __maxnreg__(168)
       if (!__shfl_sync(0xffffffffu, last, 0)) continue;
       __threadfence();
       // the last to arrive: every contributor's slot summed in stage order, a 32-column
-      // piece at a time, and stored
+      // piece at a time, and stored.  Two contributors' loads are in flight together (the
+      // sum sits at the end of the launch, and each round trip to L2 is on its path); the
+      // additions keep contributor order, so the bits do not change.
       const int c_lo = dsk_first_worker(sched, v), c_hi = dsk_last_worker(sched, v);
-#pragma unroll
+      auto add4 = [](uint32_t* acc, const float4& x) {
+        acc[0] = __float_as_uint(__uint_as_float(acc[0]) + x.x);
+        acc[1] = __float_as_uint(__uint_as_float(acc[1]) + x.y);
+        acc[2] = __float_as_uint(__uint_as_float(acc[2]) + x.z);
+        acc[3] = __float_as_uint(__uint_as_float(acc[3]) + x.w);
+      };
+#pragma unroll 1
       for (int c = 0; c < kChunks; ++c) {
         uint32_t sum[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) sum[i] = 0u;
-        for (int cc = c_lo; cc <= c_hi; ++cc) {
-          const float4* src = slot_of(cc) + c * 8 * 32;
+        for (int cc = c_lo; cc <= c_hi; cc += 2) {
+          const bool two = cc < c_hi;
+          const float4* src0 = slot_of(cc) + c * 8 * 32;
+          const float4* src1 = slot_of(two ? cc + 1 : cc) + c * 8 * 32;   // a repeat if alone
+          float4 x0[8], x1[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float4 x = __ldcg(src + j * 32);
-            sum[4 * j] = __float_as_uint(__uint_as_float(sum[4 * j]) + x.x);
-            sum[4 * j + 1] = __float_as_uint(__uint_as_float(sum[4 * j + 1]) + x.y);
-            sum[4 * j + 2] = __float_as_uint(__uint_as_float(sum[4 * j + 2]) + x.z);
-            sum[4 * j + 3] = __float_as_uint(__uint_as_float(sum[4 * j + 3]) + x.w);
+            x0[j] = __ldcg(src0 + j * 32);
+            x1[j] = __ldcg(src1 + j * 32);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) add4(sum + 4 * j, x0[j]);
+          if (two) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) add4(sum + 4 * j, x1[j]);
           }
         }
         store_piece(c, sum);

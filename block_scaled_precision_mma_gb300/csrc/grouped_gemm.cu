@@ -21,7 +21,8 @@
 //   warps 2-3   idle (with warps 0-1 they form warpgroup 0, whose registers go to the fold)
 //   warps 4-11  fold: acc += sX(row,kb) * sW(g,nblk,kb) * partial in FP32 registers
 //               (packed two-lane FMAs; scales copied four blocks ahead into shared memory),
-//               then BF16 round-to-nearest-even and masked 16-byte stores.
+//               then BF16 round-to-nearest-even and masked 32-byte stores (16-byte ones
+//               when D is only 16-byte aligned).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

@@ -20,10 +20,9 @@
 // (the same order whoever arrives last) before its output stage.
 //   both CTAs, warps 2-9  epilogue of the CTA's 128 accumulator rows: tensor memory ->
 //                       registers, an arrive on the leader's accumulator barrier (the next
-//                       unit's MMAs may start), then (FP8) BF16 pieces of 32 rows x 32
-//                       columns through a 2 KB shared-memory buffer per warp to TMA
-//                       tensor stores, or (FP4, whose five stages leave no room for the
-//                       buffers) 16-byte stores from registers.
+//                       unit's MMAs may start), then BF16 pieces of 32 rows x 32 columns
+//                       through a 2 KB shared-memory buffer per warp to TMA tensor
+//                       stores.
 // Every wait is bounded; on a timeout each role unwinds to the common teardown.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -56,9 +55,7 @@ struct Cfg2 {
   static constexpr int kSfbBytes = kKgPerStage * kSfbRepl * 1024;
   static constexpr int kChunkBytes = 4096;                // row-scale chunk, in the stage that loads it
   static constexpr int kStageBytes = kABytes + kBBytes + kSfbBytes + kChunkBytes;
-  // output staging: 2 KB (32 x 32 BF16) per epilogue warp
-  static constexpr bool kStaged = true;
-  static constexpr int kOutBytes = kStaged ? 8 * 2048 : 0;
+  static constexpr int kOutBytes = 8 * 2048;               // output staging: 2 KB per epilogue warp
   static constexpr int kStages0 = (kSmemLimit - 2048 - kOutBytes) / kStageBytes;
   static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kOutBytes + 512;
@@ -143,7 +140,7 @@ __global__ void __maxnreg__(168)
   uint8_t* sB = sA + C::kStages * C::kABytes;
   uint8_t* sSFB = sB + C::kStages * C::kBBytes;
   uint8_t* sSFA = sSFB + C::kStages * C::kSfbBytes;        // one chunk slot per stage
-  uint8_t* sOut = sSFA + C::kStages * C::kChunkBytes;       // output staging (FP8)
+  uint8_t* sOut = sSFA + C::kStages * C::kChunkBytes;       // output staging
   uint64_t* full = reinterpret_cast<uint64_t*>(sOut + C::kOutBytes);
   uint64_t* empty = full + C::kStages;
   uint64_t* acc_full = empty + C::kStages;
@@ -178,7 +175,7 @@ __global__ void __maxnreg__(168)
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmSFA);
     prefetch_tmap(&tmSFB);
-    if (C::kStaged) prefetch_tmap(&tmD);
+    prefetch_tmap(&tmD);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, kTmemCols);
@@ -335,65 +332,45 @@ __global__ void __maxnreg__(168)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
-      const int64_t row = static_cast<int64_t>(mt) * 128 + q * 32 + lane;
       const int64_t row0 = static_cast<int64_t>(mt) * 128 + q * 32;
       const int64_t col0 = static_cast<int64_t>(nt) * 256 + h * kCols;
       uint8_t* stg = sOut + (warp - 2) * 2048;
       // Output of the 32-column piece c of this warp's 32 rows x 128 columns (vals: 32
-      // FP32 values of this lane's row).  FP8: BF16 through the warp's buffer to a TMA
-      // tensor store -- lane = row, the 16-byte group v of 8 columns at position
+      // FP32 values of this lane's row): BF16 through the warp's buffer to a TMA tensor
+      // store -- lane = row, the 16-byte group v of 8 columns at position
       // v ^ ((r / 2) % 4), the tensor map's 64-byte swizzle, so the lanes hit distinct
-      // banks.  FP4: 16-byte stores from registers.
+      // banks.
       auto store_piece = [&](int c, const uint32_t* vals) {
-        if constexpr (C::kStaged) {
-          if (row0 >= p.M || col0 + c * 32 >= p.N) return;   // warp-uniform
-          uint32_t o[4][4];
+        if (row0 >= p.M || col0 + c * 32 >= p.N) return;   // warp-uniform
+        uint32_t o[4][4];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const int64_t col = col0 + c * 32 + g * 8;
-            if constexpr (EPI) {
-              if (col < p.N) {
-                apply8(vals + g * 8, col, p.epi, o[g]);
-                continue;
-              }
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              o[g][j] = pack_bf16x2(__uint_as_float(vals[g * 8 + 2 * j]),
-                                    __uint_as_float(vals[g * 8 + 2 * j + 1]));
-          }
-          if (lane == 0) bulk_wait_group_read<0>();   // the previous piece has been read
-          __syncwarp();
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const uint32_t a = smem_u32(stg + lane * 64 + ((g ^ ((lane >> 1) & 3)) * 16));
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(o[g][0]),
-                         "r"(o[g][1]), "r"(o[g][2]), "r"(o[g][3])
-                         : "memory");
-          }
-          fence_proxy_async_shared();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmD, stg, static_cast<int32_t>(col0 + c * 32), static_cast<int32_t>(row0));
-            bulk_commit_group();
-          }
-        } else {
-          if (row >= p.M) return;
-          __nv_bfloat16* out = p.D + row * p.N + col0;
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const int o = c * 32 + g * 8;
-            if (col0 + o < p.N) {
-              if constexpr (EPI)
-                store8(out + o, vals + g * 8, col0 + o, p.epi);
-              else
-                st_global_v4_cs(out + o,
-                                pack_bf16x2(__uint_as_float(vals[g * 8 + 0]), __uint_as_float(vals[g * 8 + 1])),
-                                pack_bf16x2(__uint_as_float(vals[g * 8 + 2]), __uint_as_float(vals[g * 8 + 3])),
-                                pack_bf16x2(__uint_as_float(vals[g * 8 + 4]), __uint_as_float(vals[g * 8 + 5])),
-                                pack_bf16x2(__uint_as_float(vals[g * 8 + 6]), __uint_as_float(vals[g * 8 + 7])));
+        for (int g = 0; g < 4; ++g) {
+          const int64_t col = col0 + c * 32 + g * 8;
+          if constexpr (EPI) {
+            if (col < p.N) {
+              apply8(vals + g * 8, col, p.epi, o[g]);
+              continue;
             }
           }
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            o[g][j] = pack_bf16x2(__uint_as_float(vals[g * 8 + 2 * j]),
+                                  __uint_as_float(vals[g * 8 + 2 * j + 1]));
+        }
+        if (lane == 0) bulk_wait_group_read<0>();   // the previous piece has been read
+        __syncwarp();
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint32_t a = smem_u32(stg + lane * 64 + ((g ^ ((lane >> 1) & 3)) * 16));
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(o[g][0]),
+                       "r"(o[g][1]), "r"(o[g][2]), "r"(o[g][3])
+                       : "memory");
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmD, stg, static_cast<int32_t>(col0 + c * 32), static_cast<int32_t>(row0));
+          bulk_commit_group();
         }
       };
       if (ks0 == 0 && ks1 == p.num_k_stages) {
@@ -470,7 +447,7 @@ __global__ void __maxnreg__(168)
     }
     // every tensor store of this warp has finished reading and writing before the
     // buffers (and the block) go away
-    if (C::kStaged && lane == 0) bulk_wait_group<0>();
+    if (lane == 0) bulk_wait_group<0>();
   }
   __syncthreads();
   cluster_sync();   // both CTAs are done with tensor memory and with each other's barriers

@@ -41,15 +41,18 @@ __device__ __forceinline__ float gelu_erf(float x) {
 __device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 
 // Eight accumulator values (FP32 bits) of columns col .. col+7 of one row -> eight BF16
-// results packed two per word.  The bias is read with one 16-byte load (every lane of a
-// warp reads the same columns, so the load is a broadcast).
-__device__ __forceinline__ void apply8(const uint32_t* r, int64_t col, const Epilogue& e,
-                                       uint32_t (&o)[4]) {
+// results packed two per word, with the activation ACT (Epilogue::act) fixed at compile
+// time, so that a kernel carries only its own activation's code.  The bias is read with
+// one 16-byte load (every lane of a warp reads the same columns, so the load is a
+// broadcast).
+template <int ACT>
+__device__ __forceinline__ void apply8_act(const uint32_t* r, int64_t col,
+                                           const __nv_bfloat16* bias, uint32_t (&o)[4]) {
   float v[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[j]);
-  if (e.bias) {
-    const uint4 b = __ldg(reinterpret_cast<const uint4*>(e.bias + col));
+  if (bias) {
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias + col));
     const uint32_t w[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -57,13 +60,13 @@ __device__ __forceinline__ void apply8(const uint32_t* r, int64_t col, const Epi
       v[2 * j + 1] += __uint_as_float(w[j] & 0xFFFF0000u);
     }
   }
-  if (e.act == 1) {
+  if constexpr (ACT == 1) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = fmaxf(v[j], 0.f);
-  } else if (e.act == 2) {
+  } else if constexpr (ACT == 2) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = gelu_erf(v[j]);
-  } else if (e.act == 3) {
+  } else if constexpr (ACT == 3) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = silu(v[j]);
   }
@@ -71,6 +74,17 @@ __device__ __forceinline__ void apply8(const uint32_t* r, int64_t col, const Epi
   o[1] = pack_bf16x2(v[2], v[3]);
   o[2] = pack_bf16x2(v[4], v[5]);
   o[3] = pack_bf16x2(v[6], v[7]);
+}
+
+// Same, with the activation chosen at run time.
+__device__ __forceinline__ void apply8(const uint32_t* r, int64_t col, const Epilogue& e,
+                                       uint32_t (&o)[4]) {
+  switch (e.act) {
+    case 1: apply8_act<1>(r, col, e.bias, o); break;
+    case 2: apply8_act<2>(r, col, e.bias, o); break;
+    case 3: apply8_act<3>(r, col, e.bias, o); break;
+    default: apply8_act<0>(r, col, e.bias, o); break;
+  }
 }
 
 // Same, stored to out[0..7] with one streaming 16-byte store.

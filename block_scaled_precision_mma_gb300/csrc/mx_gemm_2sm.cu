@@ -123,9 +123,12 @@ __device__ __forceinline__ void unit_tile2(const Pair2Params& p, int u, int& ur,
 
 // 10 warps share an SM's four register-file quarters (16384 registers each) as
 // 3+3+2+2 warps, so a thread may hold at most 16384 / (3 * 32) = 170 registers.
-// EPI: the output stage adds a bias and / or applies an activation (a separate
-// instantiation, so the plain GEMM's registers and code are unchanged).
-template <bool FP4, bool A_MN, bool B_MN, bool EPI>
+// EPI: 0 for the plain output stage; else the stage adds the bias (when given) and
+// applies activation EPI - 1 (Epilogue::act).  Each is an instantiation of its own, so
+// the plain GEMM's registers and code are unchanged and an activated kernel carries only
+// its own activation's code (with every activation behind a run-time switch, even a
+// bias alone cost 4% at 8192^3: the epilogue's unrolled code grew about tenfold).
+template <bool FP4, bool A_MN, bool B_MN, int EPI>
 __global__ void __maxnreg__(168)
     mx_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmSFA,
@@ -346,9 +349,9 @@ __global__ void __maxnreg__(168)
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int64_t col = col0 + c * 32 + g * 8;
-          if constexpr (EPI) {
+          if constexpr (EPI != 0) {
             if (col < p.N) {
-              apply8(vals + g * 8, col, p.epi, o[g]);
+              apply8_act<EPI - 1>(vals + g * 8, col, p.epi.bias, o[g]);
               continue;
             }
           }
@@ -459,7 +462,7 @@ __global__ void __maxnreg__(168)
   cluster_sync();
 }
 
-template <bool FP4, bool A_MN, bool B_MN, bool EPI>
+template <bool FP4, bool A_MN, bool B_MN, int EPI>
 bsmma_status launch_2sm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                         const CUtensorMap& tsb, const CUtensorMap& td, const Pair2Params& p,
                         cudaStream_t stream) {
@@ -566,10 +569,14 @@ bsmma_status launch_mx_gemm_2sm(const void* A, const uint8_t* sfa, const void* B
   p.idesc = idesc_block_scaled(af, bf, layout == BSMMA_TN, layout != BSMMA_NT, 256, 256);
   p.status = dev->status;
   p.limit_ns = wait_limit_ns();
-  const bool epi = bias != nullptr || act != 0;
+  // output stage: 0 plain, else 1 + the activation (bias applied when given)
+  const int epi = bias == nullptr && act == 0 ? 0 : 1 + act;
 #define BSMMA_2SM(F, A, B)                                                       \
-  (epi ? launch_2sm<F, A, B, true>(ta, tb, tsa, tsb, td, p, stream)              \
-       : launch_2sm<F, A, B, false>(ta, tb, tsa, tsb, td, p, stream))
+  (epi == 0   ? launch_2sm<F, A, B, 0>(ta, tb, tsa, tsb, td, p, stream)          \
+   : epi == 1 ? launch_2sm<F, A, B, 1>(ta, tb, tsa, tsb, td, p, stream)          \
+   : epi == 2 ? launch_2sm<F, A, B, 2>(ta, tb, tsa, tsb, td, p, stream)          \
+   : epi == 3 ? launch_2sm<F, A, B, 3>(ta, tb, tsa, tsb, td, p, stream)          \
+              : launch_2sm<F, A, B, 4>(ta, tb, tsa, tsb, td, p, stream))
   if (fp4) return BSMMA_2SM(true, false, false);
   switch (layout) {
     case BSMMA_NT: return BSMMA_2SM(false, false, false);

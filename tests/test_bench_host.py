@@ -57,3 +57,21 @@ def test_source_hash_ignores_comments_only():
     other = "int f(int x) {\n  return 3 * x;\n}\n"
     assert bench._code_only(code) == bench._code_only(same)
     assert bench._code_only(code) != bench._code_only(other)
+
+
+def test_kernel_sources_cover_their_includes():
+    """Every header that a hashed kernel source includes from the library's own sources is
+    hashed too, so a change anywhere in a kernel's code invalidates its traffic record."""
+    import re
+    csrc = os.path.join(ROOT, "block_scaled_precision_mma_gb300", "csrc")
+    local = set(os.listdir(csrc))
+    for workload, files in bench.KERNEL_SOURCES.items():
+        todo, seen = list(files), set()
+        while todo:
+            f = todo.pop()
+            if f in seen:
+                continue
+            seen.add(f)
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                todo += [h for h in re.findall(r'#include "([^"]+)"', fh.read()) if h in local]
+        assert seen <= set(files), (workload, sorted(seen - set(files)))
